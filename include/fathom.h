@@ -1,0 +1,245 @@
+/*
+ * fathom.h -- C ABI of the Fathom decode-step hot path for NVIDIA GB300 (sm_103a).
+ *
+ * The method (sources cited by page and section):
+ *   [A] "Fathom" article on vivekkalyanarangan.hashnode.dev
+ *   [G] Glonce, "Fathom speeds long-context KV cache decoding 1.67x with
+ *       per-query reads"
+ *   [R] Rootconf 2026 proposal, "Decoding at a million tokens when the KV cache
+ *       lives in host memory: what actually bounds the step"
+ *
+ * A decode step ranks all n cached keys with a cheap index, keeps the top k
+ * and runs exact attention over those k ([A] "The first fix: stop attending
+ * to everything", "The catch").  Fathom's index is the 4-bit K cache stored
+ * channel-major as bit planes, so reading planes 0..t-1 of a channel yields
+ * exactly its t-bit quantiser ([A] "Bit planes: how a partial read becomes a
+ * valid read"); each query spends a budget of B bits per key by reverse
+ * water-filling over its channels' importances ([A] "How each query picks its
+ * own depth"; [G] paragraph 2).
+ *
+ * Conventions for every function below
+ *   - Return value: FATHOM_OK (0) or one of the FATHOM_E* codes; nothing
+ *     throws.  fathom_last_error() returns a message for the calling thread's
+ *     most recent failure.
+ *   - Memory: every buffer is owned by the caller.  "device" pointers are
+ *     device memory, or pinned host memory that the GPU can address (the
+ *     pointer returned by cudaHostAlloc / cudaHostRegister under unified
+ *     addressing); such host-resident index or K/V buffers are read over the
+ *     host link by the kernels themselves.  "host" pointers are ordinary CPU
+ *     memory.  The library allocates no memory; scratch comes from a caller
+ *     workspace sized by the matching *_workspace_bytes query.
+ *   - Streams: `stream` is a cudaStream_t passed as void* (NULL = legacy
+ *     default stream).  Work is enqueued asynchronously and nothing
+ *     synchronises except where a function says so.
+ *   - Shapes: d (channels per KV head) is 128.  A "row" is one independent
+ *     (layer or session, KV head) pair.  Query head h belongs to row h/group.
+ *   - Dtype codes: FATHOM_F32, FATHOM_F16, FATHOM_BF16.
+ */
+#ifndef FATHOM_H
+#define FATHOM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define FATHOM_OK 0
+#define FATHOM_EINVAL 1   /* invalid argument (shape, pointer, alignment, dtype) */
+#define FATHOM_ENOMEM 2   /* caller workspace smaller than the query returned */
+#define FATHOM_ECUDA 3    /* a CUDA runtime call failed */
+#define FATHOM_ETIMEOUT 4 /* reserved: a bounded device wait gave up */
+#define FATHOM_ENOTIMPL 5 /* combination not implemented */
+#define FATHOM_EDATA 6    /* input values invalid (non-finite, outside fp16 range) */
+
+#define FATHOM_F32 0
+#define FATHOM_F16 1
+#define FATHOM_BF16 2
+
+/* Bits that device-side checks OR into an optional int32 status word. */
+#define FATHOM_STATUS_NONFINITE 1     /* non-finite query or variance: that row gets no bits */
+#define FATHOM_STATUS_BUDGET_CLAMPED 2 /* a per-row budget above 4*d was clamped to 4*d */
+
+/* Shape of a packed bit-plane index.
+ * Layout (all little-endian, row-major in the order written):
+ *   planes: uint32 [rows][nsb][128 channels][4 planes][S/32]; nsb = ceil(n/S).
+ *           Token t of a row lives in superblock t/S, word (t%S)/32, bit t%32.
+ *           Plane j holds bit (3-j) of the 4-bit code: plane 0 is the most
+ *           significant bit.  Bits of tokens >= n are 0.
+ *   meta:   fp16 pairs [rows][128 channels][nblk][2] = (lo, delta), nblk =
+ *           ceil(n/128); one pair per channel per 128-token block.
+ *   var:    float [rows][128], population variance of each channel over n.
+ * The code of element x in a block is clamp(rint((x - lo)/delta), 0, 15),
+ * with lo = fp16(min), delta = fp16((max - min)/15) and code 0 when delta is
+ * 0; 128 channels x 4 bits + 128 x 4 B / 128 tokens = 68 B per token per KV
+ * head ([A] "Where this does not work" gives 68 B). */
+typedef struct fathom_index_desc {
+  int64_t n;          /* tokens per row, >= 1 */
+  int32_t rows;       /* rows, >= 1 */
+  int32_t d;          /* channels per row, must be 128 */
+  int32_t block;      /* quantisation block in tokens, must be 128 */
+  int32_t superblock; /* S, tokens per superblock: a power of two in [128, 65536] */
+} fathom_index_desc;
+
+/* Message for the calling thread's last failure ("" if none). */
+const char* fathom_last_error(void);
+
+/* ABI version of this header (increments on incompatible change). */
+int fathom_abi_version(void);
+
+/* Bytes of the planes and meta arrays for `desc` (host-only, no GPU needed).
+ * EINVAL on an invalid desc or NULL outputs. */
+int fathom_index_bytes(const fathom_index_desc* desc, size_t* plane_bytes, size_t* meta_bytes);
+
+/* Workspace bytes fathom_pack needs for `desc` (host-only). */
+int fathom_pack_workspace_bytes(const fathom_index_desc* desc, size_t* bytes);
+
+/* Pack a K cache into the bit-plane index ([A] "Bit planes: how a partial read
+ * becomes a valid read"; [G] paragraph 2).
+ *   K       device, [rows][n][128] of k_dtype (token-major keys as cached).
+ *   planes  device (or mapped host), written in full (padding bits zeroed).
+ *   meta    device (or mapped host), written in full.
+ *   var     device, [rows][128]; fp64 two-pass population variance, each
+ *           block of 128 tokens summed in token order, block sums added in
+ *           block order, rounded once to float.
+ *   workspace/ws_bytes  device scratch of fathom_pack_workspace_bytes.
+ * Synchronises `stream` before returning, to report EDATA when an element
+ * of K is non-finite or outside the fp16 range (|x| > 65504); on EDATA the
+ * outputs are unspecified. */
+int fathom_pack(const fathom_index_desc* desc, const void* K, int k_dtype, uint32_t* planes, uint16_t* meta,
+                float* var, void* workspace, size_t ws_bytes, void* stream);
+
+/* Per-query allocation by reverse water-filling ([A] "How each query picks its
+ * own depth").
+ *   q        device, [rows*group][128] of q_dtype.
+ *   var      device, [rows][128] from fathom_pack.
+ *   budgets  device uint16 [rows] bits per token per row, or NULL to use
+ *            `budget` for every row.  Values above 4*128 are clamped to 512
+ *            and flagged FATHOM_STATUS_BUDGET_CLAMPED.
+ *   bits     device uint8 [rows][128] out: depth b_c in {0..4}, sum = budget.
+ *   qbar     device float [rows][128] out: the group's query sum
+ *            ((q_0 + q_1) + q_2) + ... in fp32.
+ *   status   device int32 or NULL: FATHOM_STATUS_* bits are OR-ed in.
+ * Definition: w_c = (qbar_c*qbar_c)*var_c (fp32); the gain of plane j of
+ * channel c is w_c multiplied j times by 0.25; the `budget` (c, j) pairs with
+ * the largest gains are taken, ties going to the smaller j and then to the
+ * smaller c; b_c counts the pairs taken for c.  EINVAL if budget is outside
+ * [0, 512] when budgets is NULL. */
+int fathom_allocate(int rows, int group, const void* q, int q_dtype, const float* var, const uint16_t* budgets,
+                    int budget, uint8_t* bits, float* qbar, int32_t* status, void* stream);
+
+/* Variable-depth scan ([A] "How each query picks its own depth": read only
+ * the chosen planes; channels with no bits are skipped entirely).
+ *   planes, meta  device or mapped host, as packed by fathom_pack.
+ *   bits, qbar    device, from fathom_allocate.
+ *   scores        device float [rows][n] out:
+ *     s(t) = sum over c with b_c >= 1 of qbar_c * (lo + delta*(m*p + (m-1)/2)),
+ *     m = 2^(4-b_c), p = the b_c-bit prefix read from planes 0..b_c-1, (lo,
+ *     delta) of t's block.  fp32 accumulation. */
+int fathom_scan(const fathom_index_desc* desc, const uint32_t* planes, const uint16_t* meta, const uint8_t* bits,
+                const float* qbar, float* scores, void* stream);
+
+/* Workspace bytes of fathom_topk (host-only). */
+int fathom_topk_workspace_bytes(int rows, int64_t n, int64_t k, size_t* bytes);
+
+/* Top-k selection ([A] "The first fix": score every key, take the top k).
+ *   scores  device float [rows][n].
+ *   idx     device int32 [rows][k] out: the k largest scores' indices, ties to
+ *           the lower index, -0.0 equal to +0.0, written in ascending index
+ *           order; if k > n the first n entries are 0..n-1 and the rest -1.
+ *   vals    device float [rows][k] out (scores at idx, -inf for padding), or NULL.
+ * EINVAL for k < 1, n < 1 or n >= 2^31. */
+int fathom_topk(int rows, int64_t n, int64_t k, const float* scores, int32_t* idx, float* vals, void* workspace,
+                size_t ws_bytes, void* stream);
+
+/* Workspace bytes of fathom_sparse_attn (host-only). */
+int fathom_sparse_attn_workspace_bytes(int rows, int group, int64_t k, size_t* bytes);
+
+/* Exact attention over the selected keys, each query head with its own q
+ * ([A] "What the model keeps in memory"; "The first fix").
+ *   q        device [rows*group][128] of q_dtype.
+ *   K, V     device or mapped host, [rows][n][128] of kv_dtype (original
+ *            16-bit or fp32 rows, not the 4-bit index).
+ *   idx      device int32 [rows][k]; entries < 0 are skipped.
+ *   out      device float [rows*group][128] out, softmax(q.K/sqrt(128)).V.
+ *   out_bf16 device uint16 (bf16 bits) [rows*group][128] out, or NULL: the
+ *            round-to-nearest-even bf16 of out. */
+int fathom_sparse_attn(int rows, int group, int64_t n, int64_t k, const void* q, int q_dtype, const void* K,
+                       const void* V, int kv_dtype, const int32_t* idx, float* out, uint16_t* out_bf16,
+                       void* workspace, size_t ws_bytes, void* stream);
+
+/* One decode step over `index.rows` rows: allocate -> scan -> top-k ->
+ * sparse attention ([R] summary: the index scan ranks all n keys to choose
+ * the top k; the selected rows are attended).  Same definitions as the
+ * individual calls; scores and bits are kept in the workspace. */
+typedef struct fathom_step_desc {
+  fathom_index_desc index;
+  int32_t group;            /* query heads per KV head, 1..8 */
+  int32_t budget;           /* bits per token when budgets == NULL, 0..512 */
+  int64_t k;                /* winners per row, >= 1 */
+  int32_t q_dtype;          /* dtype of q */
+  int32_t kv_dtype;         /* dtype of K and V */
+  const uint32_t* planes;   /* index (device or mapped host) */
+  const uint16_t* meta;     /* index (device or mapped host) */
+  const float* var;         /* device [rows][128] */
+  const uint16_t* budgets;  /* device [rows] or NULL */
+  const void* q;            /* device [rows*group][128] */
+  const void* K;            /* device or mapped host [rows][n][128] */
+  const void* V;            /* device or mapped host [rows][n][128] */
+  int32_t* idx;             /* device [rows][k] out */
+  float* out;               /* device [rows*group][128] out */
+  uint16_t* out_bf16;       /* device [rows*group][128] out or NULL */
+  int32_t* status;          /* device int32 or NULL (FATHOM_STATUS_* bits) */
+} fathom_step_desc;
+
+int fathom_decode_step_workspace_bytes(const fathom_step_desc* step, size_t* bytes);
+int fathom_decode_step(const fathom_step_desc* step, void* workspace, size_t ws_bytes, void* stream);
+
+/* ---------------- fixed 136-bit comparator index ----------------------------
+ * The fixed-depth scans the pages compare against keep 32 channels read at 4
+ * bits plus a scale, about 136 bits per token ([A] "The catch": Double
+ * Sparsity keeps 32 channels chosen offline).  Here: the 32 channels of
+ * largest var (ties to the lower channel), ascending; per token a power-of-two
+ * scale 2^e with e the smallest integer such that 7*2^e >= max|x| over those
+ * channels (e = -127 if the max is 0) and signed codes clamp(rint(x/2^e), -7, 7).
+ *   chans  device int32 [rows][32] out.
+ *   codes  device uint8 [rows][n][16] out: byte i holds channel 2i in its low
+ *          nibble and channel 2i+1 in its high nibble (two's complement).
+ *   exps   device uint8 [rows][n] out: e + 127.
+ * Synchronises `stream` (EDATA as for fathom_pack). */
+int fathom_fixed136_pack(int rows, int64_t n, const void* K, int k_dtype, const float* var, int32_t* chans,
+                         uint8_t* codes, uint8_t* exps, void* stream);
+
+/* Scores of the comparator: s(t) = 2^e(t) * sum_i qbar_{chans_i} * code_i(t). */
+int fathom_fixed136_scan(int rows, int64_t n, const int32_t* chans, const uint8_t* codes, const uint8_t* exps,
+                         const float* qbar, float* scores, void* stream);
+
+/* One comparator decode step: qbar -> fixed136 scan -> top-k -> attention. */
+typedef struct fathom_fixed136_step_desc {
+  int64_t n;
+  int32_t rows;
+  int32_t group;
+  int64_t k;
+  int32_t q_dtype;
+  int32_t kv_dtype;
+  const int32_t* chans;
+  const uint8_t* codes;  /* device or mapped host */
+  const uint8_t* exps;   /* device or mapped host */
+  const void* q;
+  const void* K;
+  const void* V;
+  int32_t* idx;
+  float* out;
+  uint16_t* out_bf16;
+} fathom_fixed136_step_desc;
+
+int fathom_fixed136_step_workspace_bytes(const fathom_fixed136_step_desc* step, size_t* bytes);
+int fathom_fixed136_decode_step(const fathom_fixed136_step_desc* step, void* workspace, size_t ws_bytes,
+                                void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FATHOM_H */

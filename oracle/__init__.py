@@ -1,0 +1,219 @@
+"""CPU oracle for the Fathom decode-step hot path -- TEST INFRASTRUCTURE.
+
+Only tests/, the smoke check in __graft_entry__ and the benchmark's CPU
+baseline leg may import this package.  The product library never does, and
+this package imports nothing from the product.  The arithmetic lives in
+fathom_oracle.c (plain C, fp64 where the method's result is real-valued);
+this module only marshals numpy arrays into it.
+
+Function map (each C function cites the page passage it follows):
+  pack            per-block min/max 4-bit codes -> MSB-first bit planes + var
+  allocate        reverse water-filling (threshold binary search)
+  waterfill       the same for one row of weights, any channel count
+  scan            fp64 score of every key from the chosen plane prefixes
+  topk_f32/_f64   k largest, ties to the lower index, ascending output
+  sparse_attn     fp64 softmax attention over the selected rows
+  fixed136_pack / fixed136_scan   the 136-bit fixed-channel comparator
+  decode_step     allocate -> scan -> top-k -> attention for many rows
+"""
+import ctypes
+import os
+
+import numpy as np
+
+from . import build as _build
+
+D = 128
+QBLOCK = 128
+
+_lib = None
+
+
+def lib():
+    global _lib
+    if _lib is None:
+        path = _build.build()
+        L = ctypes.CDLL(path)
+        P = ctypes.c_void_p
+        i64, i32 = ctypes.c_int64, ctypes.c_int
+        L.oracle_f32_to_f16.argtypes = [ctypes.c_float]
+        L.oracle_f32_to_f16.restype = ctypes.c_uint16
+        L.oracle_f16_to_f32.argtypes = [ctypes.c_uint16]
+        L.oracle_f16_to_f32.restype = ctypes.c_float
+        L.oracle_pack.argtypes = [i64, i32, i64, P, P, P, P]
+        L.oracle_pack.restype = i32
+        L.oracle_code_at.argtypes = [P, i64, i64, i64, i32, i64]
+        L.oracle_code_at.restype = i32
+        L.oracle_waterfill.argtypes = [i32, P, i32, P]
+        L.oracle_waterfill.restype = i32
+        L.oracle_allocate.argtypes = [i32, i32, P, P, P, P, P]
+        L.oracle_allocate.restype = i32
+        L.oracle_scan.argtypes = [i64, i32, i64, P, P, P, P, P, P]
+        L.oracle_scan.restype = None
+        L.oracle_topk_f32.argtypes = [i64, i32, i64, P, P]
+        L.oracle_topk_f32.restype = i32
+        L.oracle_topk_f64.argtypes = [i64, i32, i64, P, P]
+        L.oracle_topk_f64.restype = i32
+        L.oracle_sparse_attn.argtypes = [i32, i32, i64, i64, P, P, P, P, P]
+        L.oracle_sparse_attn.restype = None
+        L.oracle_fixed136_pack.argtypes = [i64, i32, P, P, P, P, P]
+        L.oracle_fixed136_pack.restype = i32
+        L.oracle_fixed136_scan.argtypes = [i64, i32, P, P, P, P, P, P]
+        L.oracle_fixed136_scan.restype = None
+        L.oracle_decode_step.argtypes = [i64, i32, i32, i64, i64, P, P, P, P, P, P, P, P, P]
+        L.oracle_decode_step.restype = i32
+        L.oracle_num_threads.argtypes = []
+        L.oracle_num_threads.restype = i32
+        _lib = L
+    return _lib
+
+
+def _p(a):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _c(a, dtype):
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+def index_shapes(n, rows, S):
+    nsb = -(-n // S)
+    nblk = -(-n // QBLOCK)
+    return (rows, nsb, D, 4, S // 32), (rows, D, nblk, 2)
+
+
+def pack(K, S):
+    """K: [rows][n][128] float32 -> (planes u32, meta u16, var f32)."""
+    K = _c(K, np.float32)
+    rows, n, d = K.shape
+    assert d == D
+    ps, ms = index_shapes(n, rows, S)
+    planes = np.zeros(ps, np.uint32)
+    meta = np.zeros(ms, np.uint16)
+    var = np.zeros((rows, D), np.float32)
+    if lib().oracle_pack(n, rows, S, _p(K), _p(planes), _p(meta), _p(var)):
+        raise ValueError("oracle_pack: invalid input")
+    return planes, meta, var
+
+
+def code_at(planes, n, S, row, c, t):
+    planes = _c(planes, np.uint32)
+    return lib().oracle_code_at(_p(planes), n, S, row, c, t)
+
+
+def waterfill(w, B):
+    w = _c(w, np.float32)
+    bits = np.zeros(w.shape[0], np.uint8)
+    if lib().oracle_waterfill(w.shape[0], _p(w), int(B), _p(bits)):
+        raise ValueError("oracle_waterfill: invalid input")
+    return bits
+
+
+def allocate(q, var, budget, group):
+    """q: [rows*group][128], var: [rows][128], budget: int or [rows]."""
+    q = _c(q, np.float32)
+    var = _c(var, np.float32)
+    rows = var.shape[0]
+    b = _c(np.broadcast_to(np.asarray(budget, np.int32), (rows,)), np.int32)
+    bits = np.zeros((rows, D), np.uint8)
+    qbar = np.zeros((rows, D), np.float32)
+    if lib().oracle_allocate(rows, group, _p(q), _p(var), _p(b), _p(bits), _p(qbar)):
+        raise ValueError("oracle_allocate: invalid input")
+    return bits, qbar
+
+
+def scan(planes, meta, bits, qbar, n, S):
+    planes = _c(planes, np.uint32)
+    meta = _c(meta, np.uint16)
+    bits = _c(bits, np.uint8)
+    qbar = _c(qbar, np.float32)
+    rows = bits.shape[0]
+    scores = np.zeros((rows, n), np.float64)
+    l1 = np.zeros((rows, n), np.float64)
+    lib().oracle_scan(n, rows, S, _p(planes), _p(meta), _p(bits), _p(qbar), _p(scores), _p(l1))
+    return scores, l1
+
+
+def topk_f32(scores, k):
+    s = _c(scores, np.float32)
+    rows, n = s.shape
+    idx = np.zeros((rows, k), np.int32)
+    if lib().oracle_topk_f32(n, rows, k, _p(s), _p(idx)):
+        raise ValueError("oracle_topk: invalid input")
+    return idx
+
+
+def topk_f64(scores, k):
+    s = _c(scores, np.float64)
+    rows, n = s.shape
+    idx = np.zeros((rows, k), np.int32)
+    if lib().oracle_topk_f64(n, rows, k, _p(s), _p(idx)):
+        raise ValueError("oracle_topk: invalid input")
+    return idx
+
+
+def sparse_attn(q, K, V, idx, group):
+    """q: [rows*group][128]; K, V: [rows][n][128]; idx: [rows][k] -> [rows*group][128] fp64."""
+    q = _c(q, np.float32)
+    K = _c(K, np.float32)
+    V = _c(V, np.float32)
+    idx = _c(idx, np.int32)
+    rows, n, _ = K.shape
+    k = idx.shape[1]
+    out = np.zeros((rows * group, D), np.float64)
+    lib().oracle_sparse_attn(rows, group, n, k, _p(q), _p(K), _p(V), _p(idx), _p(out))
+    return out
+
+
+def fixed136_pack(K, var):
+    K = _c(K, np.float32)
+    var = _c(var, np.float32)
+    rows, n, _ = K.shape
+    chans = np.zeros((rows, 32), np.int32)
+    codes = np.zeros((rows, n, 16), np.uint8)
+    exps = np.zeros((rows, n), np.uint8)
+    if lib().oracle_fixed136_pack(n, rows, _p(K), _p(var), _p(chans), _p(codes), _p(exps)):
+        raise ValueError("oracle_fixed136_pack: invalid input")
+    return chans, codes, exps
+
+
+def fixed136_scan(chans, codes, exps, qbar):
+    chans = _c(chans, np.int32)
+    codes = _c(codes, np.uint8)
+    exps = _c(exps, np.uint8)
+    qbar = _c(qbar, np.float32)
+    rows, n, _ = codes.shape
+    scores = np.zeros((rows, n), np.float64)
+    l1 = np.zeros((rows, n), np.float64)
+    lib().oracle_fixed136_scan(n, rows, _p(chans), _p(codes), _p(exps), _p(qbar), _p(scores), _p(l1))
+    return scores, l1
+
+
+def decode_step(planes, meta, var, q, budget, K, V, k, group, S):
+    """All rows of one step; returns (idx [rows][k], out fp64 [rows*group][128])."""
+    planes = _c(planes, np.uint32)
+    meta = _c(meta, np.uint16)
+    var = _c(var, np.float32)
+    q = _c(q, np.float32)
+    K = _c(K, np.float32)
+    V = _c(V, np.float32)
+    rows, n, _ = K.shape
+    b = _c(np.broadcast_to(np.asarray(budget, np.int32), (rows,)), np.int32)
+    idx = np.zeros((rows, k), np.int32)
+    out = np.zeros((rows * group, D), np.float64)
+    if lib().oracle_decode_step(n, rows, group, S, k, _p(planes), _p(meta), _p(var), _p(q), _p(b), _p(K), _p(V),
+                                _p(idx), _p(out)):
+        raise ValueError("oracle_decode_step: invalid input")
+    return idx, out
+
+
+def num_threads():
+    return lib().oracle_num_threads()
+
+
+def f32_to_f16_bits(x):
+    return lib().oracle_f32_to_f16(float(x))
+
+
+def f16_bits_to_f32(h):
+    return lib().oracle_f16_to_f32(int(h))

@@ -1,0 +1,509 @@
+/*
+ * fathom_oracle.c -- plain, slow CPU oracle for the Fathom decode-step hot path.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product library links, includes or
+ * calls this file; only the tests, the smoke check and the benchmark's CPU
+ * baseline leg load it.  It shares no code, header, table or constant with the
+ * CUDA path.  Floating point follows plain IEEE-754 semantics: it is built with
+ * -O2 -ffp-contract=off (no fused multiply-add), round-to-nearest-even.
+ *
+ * Sources (web pages about the method; cited by page and section):
+ *   [A] "Fathom" article on vivekkalyanarangan.hashnode.dev
+ *   [G] Glonce, "Fathom speeds long-context KV cache decoding 1.67x with
+ *       per-query reads"
+ *   [R] Rootconf 2026 proposal, "Decoding at a million tokens when the KV cache
+ *       lives in host memory: what actually bounds the step"
+ *
+ * What each function follows is written above it.  Where the pages leave a
+ * step open, the reading taken is stated in the comment ("reading: ...").
+ *
+ * Parity status: every function here is pinned by tests against closed forms,
+ * brute force, library routines or the pages' printed figure (see tests/).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define D_CH 128   /* channels per KV head (Qwen3-8B: 128 numbers per head, [A] "How big the cache actually gets") */
+#define QBLOCK 128 /* tokens per quantisation block (reading: gives 68 B/token/head, [A] "Where this does not work") */
+#define NPLANES 4  /* 4-bit K cache, [G] summary paragraph 2 */
+
+/* ------------------------------------------------------------------------ */
+/* IEEE binary16 conversions written from the format's definition.          */
+/* ------------------------------------------------------------------------ */
+
+/* Round a binary32 value to the nearest binary16 value, ties to even. */
+uint16_t oracle_f32_to_f16(float f) {
+  uint32_t x;
+  memcpy(&x, &f, 4);
+  uint32_t sign = (x >> 16) & 0x8000u;
+  uint32_t ax = x & 0x7fffffffu;
+  if (ax >= 0x7f800000u) return (uint16_t)(sign | (ax > 0x7f800000u ? 0x7e00u : 0x7c00u));
+  if (ax >= 0x477ff000u) return (uint16_t)(sign | 0x7c00u); /* >= 65520 rounds to infinity */
+  if (ax < 0x38800000u) {                                    /* below 2^-14: subnormal half */
+    float v;
+    memcpy(&v, &ax, 4);
+    float units = rintf(v * 16777216.0f); /* multiples of 2^-24, exact scaling, RNE */
+    return (uint16_t)(sign | (uint32_t)units);
+  }
+  uint32_t e = (ax >> 23) - 127u + 15u;
+  uint32_t m = ax & 0x7fffffu;
+  uint32_t h = (e << 10) | (m >> 13);
+  uint32_t rem = m & 0x1fffu;
+  if (rem > 0x1000u || (rem == 0x1000u && (h & 1u))) h += 1u;
+  return (uint16_t)(sign | h);
+}
+
+float oracle_f16_to_f32(uint16_t h) {
+  uint32_t e = (h >> 10) & 0x1fu, m = h & 0x3ffu;
+  float v;
+  if (e == 0) v = ldexpf((float)m, -24);
+  else if (e == 31) v = m ? NAN : INFINITY;
+  else v = ldexpf((float)(m | 0x400u), (int)e - 25);
+  return (h & 0x8000u) ? -v : v;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Layout helpers (the index layout is a definition, stated once here).     */
+/*   planes: u32 words, word index                                           */
+/*     (((row*nsb + sb)*128 + c)*4 + j)*(S/32) + (t % S)/32, bit t % 32,       */
+/*     sb = t / S; plane j holds bit (3-j) of the code (plane 0 = MSB).       */
+/*   meta:   u16 pairs, ((row*128 + c)*nblk + blk)*2 + {0: lo, 1: delta}.      */
+/* ------------------------------------------------------------------------ */
+
+static size_t plane_word(int64_t row, int64_t nsb, int64_t S, int c, int j, int64_t t) {
+  int64_t sb = t / S;
+  return (size_t)((((row * nsb + sb) * D_CH + c) * NPLANES + j) * (S / 32) + (t % S) / 32);
+}
+
+static int plane_bit(const uint32_t* planes, int64_t row, int64_t nsb, int64_t S, int c, int j, int64_t t) {
+  return (int)((planes[plane_word(row, nsb, S, c, j, t)] >> (t % 32)) & 1u);
+}
+
+/* ------------------------------------------------------------------------ */
+/* Pack: fp32 K -> per-channel, per-128-token-block min/max 4-bit codes ->    */
+/* MSB-first bit planes, channel-major; plus per-channel population variance. */
+/*                                                                            */
+/* [A] "Bit planes: how a partial read becomes a valid read": all the first   */
+/*   bits of a block of tokens go together, then all the second bits; plane 0 */
+/*   is the most significant bit.                                             */
+/* [G] paragraph 2: the 4-bit K cache is stored channel-major as bit planes.  */
+/* reading: scale/offset per (channel, 128-token block), stored as fp16       */
+/*   (lo, delta): 128 ch x 4 bit + 128 x 4 B / 128 tokens = 68 B per token per */
+/*   KV head, the storage figure of [A] "Where this does not work".           */
+/* reading: delta = (max - min) / 15 in fp32; code = rint((x - lo16)/delta16)  */
+/*   clamped to [0, 15]; code = 0 when delta16 == 0.                          */
+/* reading: var_c = population variance over the row's n tokens, fp64, two    */
+/*   passes (mean, then sum of squared deviations), summed sequentially inside */
+/*   each 128-token block and then over block partials in block order.        */
+/* Returns 0, or 1 if an input is not finite or outside the fp16 range.       */
+/* ------------------------------------------------------------------------ */
+int oracle_pack(int64_t n, int rows, int64_t S, const float* K, uint32_t* planes, uint16_t* meta, float* var) {
+  if (n <= 0 || rows <= 0 || S < QBLOCK || (S % QBLOCK) != 0) return 1;
+  int64_t nsb = (n + S - 1) / S;
+  int64_t nblk = (n + QBLOCK - 1) / QBLOCK;
+  size_t nwords = (size_t)rows * nsb * D_CH * NPLANES * (S / 32);
+  memset(planes, 0, nwords * sizeof(uint32_t));
+  for (int64_t i = 0; i < (int64_t)rows * n * D_CH; ++i) {
+    float x = K[i];
+    if (!(fabsf(x) <= 65504.0f)) return 1; /* also rejects NaN */
+  }
+  for (int row = 0; row < rows; ++row) {
+    const float* Kr = K + (size_t)row * n * D_CH;
+    for (int c = 0; c < D_CH; ++c) {
+      for (int64_t b = 0; b < nblk; ++b) {
+        int64_t t0 = b * QBLOCK, t1 = t0 + QBLOCK < n ? t0 + QBLOCK : n;
+        float lo = Kr[t0 * D_CH + c], hi = lo;
+        for (int64_t t = t0 + 1; t < t1; ++t) {
+          float x = Kr[t * D_CH + c];
+          if (x < lo) lo = x;
+          if (x > hi) hi = x;
+        }
+        float delta = (hi - lo) / 15.0f;
+        uint16_t lo16 = oracle_f32_to_f16(lo), d16 = oracle_f32_to_f16(delta);
+        size_t mi = (((size_t)row * D_CH + c) * nblk + b) * 2;
+        meta[mi + 0] = lo16;
+        meta[mi + 1] = d16;
+        float lof = oracle_f16_to_f32(lo16), df = oracle_f16_to_f32(d16);
+        for (int64_t t = t0; t < t1; ++t) {
+          int code = 0;
+          if (df != 0.0f) {
+            float qv = rintf((Kr[t * D_CH + c] - lof) / df);
+            code = qv < 0.0f ? 0 : (qv > 15.0f ? 15 : (int)qv);
+          }
+          for (int j = 0; j < NPLANES; ++j)
+            if ((code >> (3 - j)) & 1) planes[plane_word(row, nsb, S, c, j, t)] |= 1u << (t % 32);
+        }
+      }
+      /* variance, fixed summation order */
+      double total = 0.0;
+      for (int64_t b = 0; b < nblk; ++b) {
+        int64_t t0 = b * QBLOCK, t1 = t0 + QBLOCK < n ? t0 + QBLOCK : n;
+        double part = 0.0;
+        for (int64_t t = t0; t < t1; ++t) part = part + (double)Kr[t * D_CH + c];
+        total = total + part;
+      }
+      double mean = total / (double)n;
+      double m2 = 0.0;
+      for (int64_t b = 0; b < nblk; ++b) {
+        int64_t t0 = b * QBLOCK, t1 = t0 + QBLOCK < n ? t0 + QBLOCK : n;
+        double part = 0.0;
+        for (int64_t t = t0; t < t1; ++t) {
+          double dv = (double)Kr[t * D_CH + c] - mean;
+          part = part + dv * dv;
+        }
+        m2 = m2 + part;
+      }
+      var[(size_t)row * D_CH + c] = (float)(m2 / (double)n);
+    }
+  }
+  return 0;
+}
+
+/* Read the 4-bit code of (row, c, t) back from the planes (all four planes). */
+int oracle_code_at(const uint32_t* planes, int64_t n, int64_t S, int64_t row, int c, int64_t t) {
+  int64_t nsb = (n + S - 1) / S;
+  int code = 0;
+  for (int j = 0; j < NPLANES; ++j) code = (code << 1) | plane_bit(planes, row, nsb, S, c, j, t);
+  return code;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Allocation: reverse water-filling of a bit budget over channels.          */
+/*                                                                            */
+/* [A] "How each query picks its own depth": each channel has an importance   */
+/*   (the share of score variance it carries); one more bit on a channel      */
+/*   removes error proportional to that importance divided by 4^(bits spent);  */
+/*   pick a threshold, give each channel the bits that bring it to the        */
+/*   threshold, binary-search the threshold until the total equals the budget. */
+/* [G] paragraph 2: importance is variance-weighted; budget B bits per token. */
+/* reading: w_c = (qbar_c * qbar_c) * var_c in fp32, qbar = left-fold sum of    */
+/*   the group's query heads in fp32; gain of plane j of channel c is          */
+/*   w_c * 4^-j; exactly B (c, j) pairs are taken, ties broken by plane j     */
+/*   ascending then channel c ascending.                                      */
+/* ------------------------------------------------------------------------ */
+
+static uint32_t fbits(float f) { uint32_t u; memcpy(&u, &f, 4); return u; }
+
+/* number of (c, j) whose gain is >= the threshold whose fp32 bit pattern is tau */
+static int count_ge(int d, const float* w, uint32_t tau) {
+  int cnt = 0;
+  for (int c = 0; c < d; ++c) {
+    float g = w[c];
+    for (int j = 0; j < NPLANES; ++j) {
+      if (fbits(g) >= tau) cnt++;
+      g = g * 0.25f;
+    }
+  }
+  return cnt;
+}
+
+/* One row: w[d] (finite, >= 0), budget B in [0, 4d]  ->  bits[d].
+ * Threshold search as the page describes it: binary-search the threshold tau
+ * (over non-negative fp32 values, whose bit patterns order like integers) for
+ * the largest tau with at least B gains >= tau; every gain above tau gets its
+ * bit; the gains equal to tau are handed out by (j asc, c asc) until the total
+ * is exactly B.  Returns 0, or 1 on invalid input. */
+int oracle_waterfill(int d, const float* w, int B, uint8_t* bits) {
+  if (d <= 0 || B < 0 || B > NPLANES * d) return 1;
+  for (int c = 0; c < d; ++c) {
+    if (!(w[c] >= 0.0f) || isinf(w[c])) return 1;
+    bits[c] = 0;
+  }
+  if (B == 0) return 0;
+  uint32_t lo = 0u, hi = 0x7f800000u; /* count_ge(lo) = 4d >= B; search largest tau with count >= B */
+  while (lo < hi) {
+    uint32_t mid = lo + (hi - lo + 1u) / 2u;
+    if (count_ge(d, w, mid) >= B) lo = mid;
+    else hi = mid - 1u;
+  }
+  uint32_t tau = lo;
+  int above = 0;
+  for (int c = 0; c < d; ++c) {
+    float g = w[c];
+    for (int j = 0; j < NPLANES; ++j) {
+      if (fbits(g) > tau) { bits[c]++; above++; }
+      g = g * 0.25f;
+    }
+  }
+  int left = B - above;
+  for (int j = 0; j < NPLANES && left > 0; ++j) {
+    for (int c = 0; c < d && left > 0; ++c) {
+      float g = w[c];
+      for (int jj = 0; jj < j; ++jj) g = g * 0.25f;
+      if (fbits(g) == tau) { bits[c]++; left--; }
+    }
+  }
+  return left == 0 ? 0 : 1;
+}
+
+/* All rows.  q: [rows*group][128] fp32; var: [rows][128]; budget: [rows].
+ * Writes qbar [rows][128] and bits [rows][128].  Returns 0 or 1 (invalid). */
+int oracle_allocate(int rows, int group, const float* q, const float* var, const int32_t* budget, uint8_t* bits,
+                    float* qbar) {
+  if (rows <= 0 || group <= 0) return 1;
+  for (int r = 0; r < rows; ++r) {
+    float w[D_CH];
+    for (int c = 0; c < D_CH; ++c) {
+      float s = q[((size_t)r * group + 0) * D_CH + c];
+      for (int h = 1; h < group; ++h) s = s + q[((size_t)r * group + h) * D_CH + c];
+      if (!isfinite(s) || !isfinite(var[(size_t)r * D_CH + c])) return 1;
+      qbar[(size_t)r * D_CH + c] = s;
+      w[c] = (s * s) * var[(size_t)r * D_CH + c];
+    }
+    if (oracle_waterfill(D_CH, w, budget[r], bits + (size_t)r * D_CH)) return 1;
+  }
+  return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Scan: approximate score of every key from only the planes chosen.        */
+/*                                                                            */
+/* [A] "Bit planes ...": reading planes 0..t-1 is exactly the t-bit version    */
+/*   with the same scale factor.                                              */
+/* [A] "How each query picks its own depth": channels with no bits are        */
+/*   skipped entirely.                                                        */
+/* reading: the t-bit prefix p of a channel reconstructs at the centre of the  */
+/*   2^(4-t) merged 4-bit buckets: lo + delta*(m*p + (m-1)/2), m = 2^(4-t); at */
+/*   t = 4 this is the 4-bit dequantised value lo + delta*code.               */
+/* fp64 accumulation.  Also returns the per-key L1 norm sum_c |qbar_c x_c|.   */
+/* ------------------------------------------------------------------------ */
+void oracle_scan(int64_t n, int rows, int64_t S, const uint32_t* planes, const uint16_t* meta, const uint8_t* bits,
+                 const float* qbar, double* scores, double* l1) {
+  int64_t nsb = (n + S - 1) / S;
+  int64_t nblk = (n + QBLOCK - 1) / QBLOCK;
+  for (int r = 0; r < rows; ++r) {
+    for (int64_t t = 0; t < n; ++t) {
+      double s = 0.0, a = 0.0;
+      int64_t b = t / QBLOCK;
+      for (int c = 0; c < D_CH; ++c) {
+        int depth = bits[(size_t)r * D_CH + c];
+        if (depth == 0) continue;
+        size_t mi = (((size_t)r * D_CH + c) * nblk + b) * 2;
+        double lo = (double)oracle_f16_to_f32(meta[mi]), dl = (double)oracle_f16_to_f32(meta[mi + 1]);
+        int p = 0;
+        for (int j = 0; j < depth; ++j) p = (p << 1) | plane_bit(planes, r, nsb, S, c, j, t);
+        double m = (double)(1 << (NPLANES - depth));
+        double x = lo + dl * (m * (double)p + (m - 1.0) / 2.0);
+        double term = (double)qbar[(size_t)r * D_CH + c] * x;
+        s += term;
+        a += fabs(term);
+      }
+      scores[(size_t)r * n + t] = s;
+      if (l1) l1[(size_t)r * n + t] = a;
+    }
+  }
+}
+
+/* ------------------------------------------------------------------------ */
+/* Top-k: the k largest scores of a row, ties to the lower index, returned   */
+/* in ascending index order.  [A] "The first fix: stop attending to          */
+/* everything": score every key, take the top k.  reading: -0.0 equals +0.0;  */
+/* k >= n selects every key and pads idx with -1.                            */
+/* ------------------------------------------------------------------------ */
+typedef struct { double s; int64_t i; } scored;
+
+static int cmp_desc(const void* a, const void* b) {
+  const scored* x = (const scored*)a;
+  const scored* y = (const scored*)b;
+  if (x->s > y->s) return -1;
+  if (x->s < y->s) return 1;
+  return (x->i < y->i) ? -1 : (x->i > y->i);
+}
+
+static int cmp_i32(const void* a, const void* b) {
+  int32_t x = *(const int32_t*)a, y = *(const int32_t*)b;
+  return (x > y) - (x < y);
+}
+
+static void topk_row(int64_t n, int64_t k, scored* buf, int32_t* idx) {
+  qsort(buf, (size_t)n, sizeof(scored), cmp_desc);
+  int64_t take = k < n ? k : n;
+  for (int64_t i = 0; i < take; ++i) idx[i] = (int32_t)buf[i].i;
+  qsort(idx, (size_t)take, sizeof(int32_t), cmp_i32);
+  for (int64_t i = take; i < k; ++i) idx[i] = -1;
+}
+
+int oracle_topk_f32(int64_t n, int rows, int64_t k, const float* scores, int32_t* idx) {
+  if (n <= 0 || k <= 0) return 1;
+  scored* buf = (scored*)malloc(sizeof(scored) * (size_t)n);
+  if (!buf) return 1;
+  for (int r = 0; r < rows; ++r) {
+    for (int64_t t = 0; t < n; ++t) { buf[t].s = (double)scores[(size_t)r * n + t]; buf[t].i = t; }
+    topk_row(n, k, buf, idx + (size_t)r * k);
+  }
+  free(buf);
+  return 0;
+}
+
+int oracle_topk_f64(int64_t n, int rows, int64_t k, const double* scores, int32_t* idx) {
+  if (n <= 0 || k <= 0) return 1;
+  scored* buf = (scored*)malloc(sizeof(scored) * (size_t)n);
+  if (!buf) return 1;
+  for (int r = 0; r < rows; ++r) {
+    for (int64_t t = 0; t < n; ++t) { buf[t].s = scores[(size_t)r * n + t]; buf[t].i = t; }
+    topk_row(n, k, buf, idx + (size_t)r * k);
+  }
+  free(buf);
+  return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Sparse GQA attention over the winners, with the original K/V rows.        */
+/* [A] "What the model keeps in memory": the query is compared with keys and */
+/*   the values are mixed in proportion to relevance; [A] "The first fix":    */
+/*   attention over just the k selected tokens.  Softmax scaled by 1/sqrt(d); */
+/*   every query head h of KV head r = h / group uses its own q_h.  fp64.     */
+/*   idx entries < 0 are padding and are skipped.                             */
+/* ------------------------------------------------------------------------ */
+void oracle_sparse_attn(int rows, int group, int64_t n, int64_t k, const float* q, const float* K, const float* V,
+                        const int32_t* idx, double* out) {
+  double* z = (double*)malloc(sizeof(double) * (size_t)(k > 0 ? k : 1));
+  for (int r = 0; r < rows; ++r) {
+    const int32_t* id = idx + (size_t)r * k;
+    for (int h = 0; h < group; ++h) {
+      const float* qh = q + ((size_t)r * group + h) * D_CH;
+      double zmax = -INFINITY;
+      for (int64_t i = 0; i < k; ++i) {
+        if (id[i] < 0) { z[i] = -INFINITY; continue; }
+        const float* kt = K + ((size_t)r * n + id[i]) * D_CH;
+        double dot = 0.0;
+        for (int c = 0; c < D_CH; ++c) dot += (double)qh[c] * (double)kt[c];
+        z[i] = dot / sqrt((double)D_CH);
+        if (z[i] > zmax) zmax = z[i];
+      }
+      double denom = 0.0;
+      double acc[D_CH];
+      for (int c = 0; c < D_CH; ++c) acc[c] = 0.0;
+      for (int64_t i = 0; i < k; ++i) {
+        if (id[i] < 0) continue;
+        double p = exp(z[i] - zmax);
+        denom += p;
+        const float* vt = V + ((size_t)r * n + id[i]) * D_CH;
+        for (int c = 0; c < D_CH; ++c) acc[c] += p * (double)vt[c];
+      }
+      double* o = out + ((size_t)r * group + h) * D_CH;
+      for (int c = 0; c < D_CH; ++c) o[c] = denom > 0.0 ? acc[c] / denom : 0.0;
+    }
+  }
+  free(z);
+}
+
+/* ------------------------------------------------------------------------ */
+/* Fixed 136-bit comparator (Double-Sparsity style: 32 channels chosen        */
+/* offline, read at 4 bits, plus a scale), [A] "The catch": Double Sparsity    */
+/* keeps 32 channels chosen offline; these indexes land near 136 bits/token.  */
+/* reading: channels = the 32 largest var_c (ties to lower c), ascending c;   */
+/*   per token a power-of-two scale 2^e, e the smallest integer with           */
+/*   7*2^e >= max |x| over those channels (e = -127 when the max is 0), codes  */
+/*   clamp(rint(x / 2^e), -7, 7) as signed nibbles: 16 B + 1 B = 136 bits.     */
+/*   codes [rows][n][16] (byte i: channel 2i low nibble, 2i+1 high nibble),    */
+/*   exps [rows][n] = e + 127; chans [rows][32].                               */
+/* ------------------------------------------------------------------------ */
+int oracle_fixed136_pack(int64_t n, int rows, const float* K, const float* var, int32_t* chans, uint8_t* codes,
+                         uint8_t* exps) {
+  for (int r = 0; r < rows; ++r) {
+    const float* v = var + (size_t)r * D_CH;
+    int used[D_CH];
+    for (int c = 0; c < D_CH; ++c) used[c] = 0;
+    for (int i = 0; i < 32; ++i) {
+      int best = -1;
+      for (int c = 0; c < D_CH; ++c)
+        if (!used[c] && (best < 0 || v[c] > v[best])) best = c;
+      used[best] = 1;
+    }
+    int m = 0;
+    for (int c = 0; c < D_CH; ++c)
+      if (used[c]) chans[r * 32 + m++] = c;
+    for (int64_t t = 0; t < n; ++t) {
+      const float* x = K + ((size_t)r * n + t) * D_CH;
+      float mx = 0.0f;
+      for (int i = 0; i < 32; ++i) {
+        float a = fabsf(x[chans[r * 32 + i]]);
+        if (!(a <= 65504.0f)) return 1;
+        if (a > mx) mx = a;
+      }
+      int e = -127;
+      if (mx > 0.0f) {
+        int E;
+        frexpf(mx, &E); /* mx = f * 2^E, f in [0.5, 1) */
+        e = (7.0f * ldexpf(1.0f, E - 3) >= mx) ? E - 3 : E - 2;
+      }
+      exps[(size_t)r * n + t] = (uint8_t)(e + 127);
+      uint8_t* cb = codes + ((size_t)r * n + t) * 16;
+      for (int i = 0; i < 16; ++i) cb[i] = 0;
+      for (int i = 0; i < 32; ++i) {
+        int code = 0;
+        if (mx > 0.0f) {
+          float qv = rintf(ldexpf(x[chans[r * 32 + i]], -e));
+          code = qv < -7.0f ? -7 : (qv > 7.0f ? 7 : (int)qv);
+        }
+        cb[i / 2] |= (uint8_t)((code & 0xF) << (4 * (i % 2)));
+      }
+    }
+  }
+  return 0;
+}
+
+void oracle_fixed136_scan(int64_t n, int rows, const int32_t* chans, const uint8_t* codes, const uint8_t* exps,
+                          const float* qbar, double* scores, double* l1) {
+  for (int r = 0; r < rows; ++r) {
+    for (int64_t t = 0; t < n; ++t) {
+      const uint8_t* cb = codes + ((size_t)r * n + t) * 16;
+      double scale = ldexp(1.0, (int)exps[(size_t)r * n + t] - 127);
+      double s = 0.0, a = 0.0;
+      for (int i = 0; i < 32; ++i) {
+        int nib = (cb[i / 2] >> (4 * (i % 2))) & 0xF;
+        int code = nib >= 8 ? nib - 16 : nib;
+        double term = (double)qbar[(size_t)r * D_CH + chans[r * 32 + i]] * (double)code * scale;
+        s += term;
+        a += fabs(term);
+      }
+      scores[(size_t)r * n + t] = s;
+      if (l1) l1[(size_t)r * n + t] = a;
+    }
+  }
+}
+
+/* ------------------------------------------------------------------------ */
+/* One decode step over `rows` independent rows: allocate -> scan -> top-k   */
+/* -> sparse attention, [R] summary: the index scan ranks all n keys to pick  */
+/* the top-k, then attention runs over the selected rows.  The top-k here is  */
+/* taken on the oracle's own fp64 scores.  Rows run in parallel (OpenMP when  */
+/* built with it); the result does not depend on the thread count.            */
+/* ------------------------------------------------------------------------ */
+int oracle_decode_step(int64_t n, int rows, int group, int64_t S, int64_t k, const uint32_t* planes,
+                       const uint16_t* meta, const float* var, const float* q, const int32_t* budget, const float* K,
+                       const float* V, int32_t* idx, double* out) {
+  float* qbar = (float*)malloc(sizeof(float) * (size_t)rows * D_CH);
+  uint8_t* bits = (uint8_t*)malloc((size_t)rows * D_CH);
+  if (!qbar || !bits) return 1;
+  int bad = oracle_allocate(rows, group, q, var, budget, bits, qbar);
+  if (bad) { free(qbar); free(bits); return 1; }
+  int64_t nsb = (n + S - 1) / S, nblk = (n + QBLOCK - 1) / QBLOCK;
+  size_t pw = (size_t)nsb * D_CH * NPLANES * (S / 32);
+  size_t mw = (size_t)D_CH * nblk * 2;
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int r = 0; r < rows; ++r) {
+    double* s = (double*)malloc(sizeof(double) * (size_t)n);
+    oracle_scan(n, 1, S, planes + (size_t)r * pw, meta + (size_t)r * mw, bits + (size_t)r * D_CH,
+                qbar + (size_t)r * D_CH, s, NULL);
+    oracle_topk_f64(n, 1, k, s, idx + (size_t)r * k);
+    oracle_sparse_attn(1, group, n, k, q + (size_t)r * group * D_CH, K + (size_t)r * n * D_CH,
+                       V + (size_t)r * n * D_CH, idx + (size_t)r * k, out + (size_t)r * group * D_CH);
+    free(s);
+  }
+  free(qbar);
+  free(bits);
+  return 0;
+}
+
+int oracle_num_threads(void) {
+#ifdef _OPENMP
+  extern int omp_get_max_threads(void);
+  return omp_get_max_threads();
+#else
+  return 1;
+#endif
+}

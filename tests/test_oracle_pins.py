@@ -1,0 +1,480 @@
+"""Pins of the CPU oracle against what the pages and mathematics fix.
+
+Each test checks the oracle against something other than itself: the page's
+printed bit-plane figure, numpy's IEEE conversions and variance, brute force
+over all quantiser levels or all allocations, a plain sort, and textbook dense
+softmax attention.  A dropped term, a wrong sign, index or tie rule in the
+oracle fails at least one of them.  No GPU.
+"""
+import itertools
+import json
+import math
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+import oracle
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+D = 128
+
+
+# ---------------------------------------------------------------- helpers ---
+def read_bit(planes, n, S, row, c, j, t):
+    """Independent reader of the documented plane layout."""
+    nsb = -(-n // S)
+    flat = planes.reshape(-1)
+    w = (((row * nsb + t // S) * D + c) * 4 + j) * (S // 32) + (t % S) // 32
+    return int((flat[w] >> np.uint32(t % 32)) & np.uint32(1))
+
+
+def codes_from_planes(planes, n, S, rows):
+    """All 4-bit codes [rows][n][128] from the planes, by the documented layout (vectorised)."""
+    nsb = -(-n // S)
+    p = planes.reshape(rows, nsb, D, 4, S // 32)
+    t = np.arange(n)
+    sb, w, b = t // S, (t % S) // 32, (t % 32).astype(np.uint32)
+    out = np.zeros((rows, n, D), np.int64)
+    for j in range(4):
+        words = p[:, sb, :, j, w].transpose(1, 0, 2)  # advanced indices first -> [rows][n][128]
+        bit = (words >> b[None, :, None]) & np.uint32(1)
+        out = out * 2 + bit.astype(np.int64)
+    return out
+
+
+def meta_f32(meta):
+    return meta.view(np.float16).astype(np.float32)
+
+
+def rand_keys(rows, n, seed, dist="normal"):
+    rng = np.random.default_rng(seed)
+    s = np.exp(rng.uniform(np.log(0.1), np.log(4.0), D)).astype(np.float32)
+    if dist == "normal":
+        z = rng.standard_normal((rows, n, D))
+    elif dist == "uniform":
+        z = rng.uniform(-1, 1, (rows, n, D))
+    elif dist == "t3":
+        z = rng.standard_t(3, (rows, n, D))
+    else:
+        raise ValueError(dist)
+    return (z * s).astype(np.float32)
+
+
+# ------------------------------------------------------- fp16 conversions ---
+def test_f16_conversion_matches_numpy():
+    rng = np.random.default_rng(1)
+    vals = list(rng.standard_normal(2000).astype(np.float32) * np.float32(3.0))
+    vals += list((rng.standard_normal(500) * 1e-5).astype(np.float32))  # subnormal halves
+    vals += [0.0, -0.0, 65504.0, 65519.0, 65520.0, 1e9, -1e9, 6.0e-8, 2.98e-8, 3.0e-8, 5.96e-8]
+    # exact halfway cases between neighbouring halves
+    for h in [0x3C00, 0x3C01, 0x0001, 0x0002, 0x03FF, 0x0400, 0x7BFE]:
+        a = np.array([h, h + 1], np.uint16).view(np.float16).astype(np.float64)
+        vals.append(np.float32((a[0] + a[1]) / 2))
+    for v in vals:
+        v = np.float32(v)
+        with np.errstate(over="ignore"):
+            want16 = np.array([v], np.float32).astype(np.float16)
+        want = want16.view(np.uint16)[0]
+        got = oracle.f32_to_f16_bits(v)
+        assert got == want, (v, hex(got), hex(want))
+        if np.isfinite(want16[0]):
+            assert oracle.f16_bits_to_f32(want) == np.float32(np.array([want], np.uint16).view(np.float16)[0])
+
+
+# --------------------------------------------------- bit planes (figure) ---
+def test_bitplane_figure_golden():
+    """The page's figure: [1011][0110][1101][0010] -> planes 1010, 0110, 1101, 1010; planes 0-1 give 2 bits."""
+    g = json.load(open(os.path.join(GOLDEN, "bitplane_figure.json")))
+    codes = [int(b, 2) for b in g["codes_binary"]]
+    # A block whose min is 0 and max is 15 quantises integers to themselves (delta = 1).
+    n, S = 128, 128
+    K = np.zeros((1, n, D), np.float32)
+    K[0, :4, 5] = codes
+    K[0, 4, 5] = 0.0
+    K[0, 5, 5] = 15.0
+    planes, meta, _ = oracle.pack(K, S)
+    assert meta_f32(meta)[0, 5, 0, 0] == 0.0 and meta_f32(meta)[0, 5, 0, 1] == 1.0
+    for j, want in g["planes"].items():
+        got = "".join(str(read_bit(planes, n, S, 0, 5, int(j), t)) for t in range(4))
+        assert got == want, (j, got, want)
+    # two-plane prefix = every number rounded to 2 bits
+    two = ["".join(str(read_bit(planes, n, S, 0, 5, j, t)) for j in range(2)) for t in range(4)]
+    assert two == g["two_plane_prefix_binary"]
+
+
+# ------------------------------------------------------------- quantiser ---
+@pytest.mark.parametrize("dist", ["normal", "uniform", "t3"])
+@pytest.mark.parametrize("n,S", [(300, 256), (128, 128), (1000, 512), (77, 1024)])
+def test_quantiser_is_nearest_level_of_block_minmax_grid(dist, n, S):
+    rows = 2
+    K = rand_keys(rows, n, seed=n + S, dist=dist)
+    planes, meta, _ = oracle.pack(K, S)
+    codes = codes_from_planes(planes, n, S, rows)
+    mf = meta_f32(meta)
+    nblk = -(-n // 128)
+    for r in range(rows):
+        for b in range(nblk):
+            t0, t1 = b * 128, min(n, b * 128 + 128)
+            x = K[r, t0:t1, :]
+            # scale/offset: numpy fp16 of the block min and of (max - min)/15 computed in fp32
+            lo16 = x.min(0).astype(np.float16).astype(np.float32)
+            d16 = ((x.max(0) - x.min(0)) / np.float32(15)).astype(np.float32).astype(np.float16).astype(np.float32)
+            assert np.array_equal(mf[r, :, b, 0], lo16)
+            assert np.array_equal(mf[r, :, b, 1], d16)
+            # brute force over the 16 levels in exact arithmetic: the chosen level is the nearest
+            lv = lo16[None, :, None].astype(np.float64) + d16[None, :, None].astype(np.float64) * np.arange(16)
+            err = np.abs(x[:, :, None].astype(np.float64) - lv)  # [t][c][16]
+            c = codes[r, t0:t1, :]
+            chosen = np.take_along_axis(err, c[:, :, None], 2)[:, :, 0]
+            best = err.min(2)
+            slack = 4e-7 * (np.abs(x) + np.abs(lo16) + 16 * d16)  # fp32 rounding of (x - lo)/delta
+            ok = (chosen <= best + slack) | (d16[None, :] == 0)
+            assert ok.all()
+            # delta 0 gives code 0
+            assert (c[:, d16 == 0] == 0).all()
+    # padding bits past n are zero
+    codes_pad = codes_from_planes(planes, -(-n // S) * S, S, rows)
+    assert (codes_pad[:, n:, :] == 0).all()
+
+
+def test_min_and_max_take_end_codes():
+    K = rand_keys(1, 512, seed=3)
+    planes, meta, _ = oracle.pack(K, 512)
+    codes = codes_from_planes(planes, 512, 512, 1)
+    for b in range(4):
+        x = K[0, b * 128:(b + 1) * 128, :]
+        c = codes[0, b * 128:(b + 1) * 128, :]
+        amin, amax = x.argmin(0), x.argmax(0)
+        assert (c[amin, np.arange(D)] == 0).all()
+        assert (c[amax, np.arange(D)] == 15).all()
+
+
+def test_variance_matches_numpy():
+    for n in [1, 7, 128, 1000, 4096]:
+        K = rand_keys(2, n, seed=n)
+        _, _, var = oracle.pack(K, 128)
+        want = K.astype(np.float64).var(axis=1)
+        np.testing.assert_allclose(var, want, rtol=2e-7, atol=0)
+
+
+def test_pack_rejects_out_of_fp16_range():
+    K = rand_keys(1, 64, seed=2)
+    K[0, 3, 9] = 70000.0
+    with pytest.raises(ValueError):
+        oracle.pack(K, 128)
+    K[0, 3, 9] = np.nan
+    with pytest.raises(ValueError):
+        oracle.pack(K, 128)
+
+
+# ------------------------------------------------- prefix = t-bit quantiser ---
+def _reconstruct(planes, meta, n, S, depth, c):
+    """x_hat of channel c at the given depth, via the oracle's scan with qbar = e_c."""
+    bits = np.zeros((1, D), np.uint8)
+    bits[0, c] = depth
+    qbar = np.zeros((1, D), np.float32)
+    qbar[0, c] = 1.0
+    s, l1 = oracle.scan(planes, meta, bits, qbar, n, S)
+    return s[0]
+
+
+def test_prefix_reconstruction_is_centroid_of_merged_buckets():
+    """Reading planes 0..t-1 gives the t-bit quantiser with the same scale: its level for
+    prefix p is the mean of the 2^(4-t) four-bit levels it merges."""
+    n, S = 512, 256
+    K = rand_keys(1, n, seed=11)
+    planes, meta, _ = oracle.pack(K, S)
+    codes = codes_from_planes(planes, n, S, 1)[0]
+    mf = meta_f32(meta)[0]
+    for c in [0, 17, 64, 127]:
+        lo = mf[c, np.arange(n) // 128, 0].astype(np.float64)
+        dl = mf[c, np.arange(n) // 128, 1].astype(np.float64)
+        for t in range(1, 5):
+            m = 2 ** (4 - t)
+            got = _reconstruct(planes, meta, n, S, t, c)
+            p = codes[:, c] >> (4 - t)
+            merged = np.stack([lo + dl * (p * m + i) for i in range(m)])  # the 4-bit levels merged
+            np.testing.assert_allclose(got, merged.mean(0), rtol=1e-13, atol=1e-13)
+        assert np.all(_reconstruct(planes, meta, n, S, 0, c) == 0.0)  # skipped channel contributes nothing
+
+
+def test_each_bit_cuts_error_about_fourfold():
+    """'Each additional bit cuts that error by a factor of four' (uniform data, MSE)."""
+    n, S = 8192, 1024
+    rng = np.random.default_rng(5)
+    K = rng.uniform(-1, 1, (1, n, D)).astype(np.float32)
+    planes, meta, _ = oracle.pack(K, S)
+    mse = []
+    for t in range(1, 5):
+        e = []
+        for c in range(0, D, 16):
+            xh = _reconstruct(planes, meta, n, S, t, c)
+            e.append(np.mean((xh - K[0, :, c]) ** 2))
+        mse.append(np.mean(e))
+    for a, b in zip(mse, mse[1:]):
+        assert 3.5 < a / b < 4.5, mse
+
+
+# ------------------------------------------------------------------- scan ---
+def test_full_budget_scan_equals_4bit_dequantised_dot():
+    """B = 512 (every plane): scores equal the full 4-bit dequantised dot product."""
+    rows, n, S = 3, 700, 512
+    K = rand_keys(rows, n, seed=21)
+    planes, meta, var = oracle.pack(K, S)
+    rng = np.random.default_rng(2)
+    q = rng.standard_normal((rows * 4, D)).astype(np.float32)
+    bits, qbar = oracle.allocate(q, var, 512, 4)
+    assert (bits == 4).all()
+    s, l1 = oracle.scan(planes, meta, bits, qbar, n, S)
+    codes = codes_from_planes(planes, n, S, rows).astype(np.float64)
+    mf = meta_f32(meta).astype(np.float64)  # [rows][128][nblk][2]
+    blk = np.arange(n) // 128
+    lo = mf[:, :, blk, 0].transpose(0, 2, 1)
+    dl = mf[:, :, blk, 1].transpose(0, 2, 1)
+    deq = lo + dl * codes
+    want = np.einsum("rtc,rc->rt", deq, qbar.astype(np.float64))
+    np.testing.assert_allclose(s, want, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(l1, np.abs(deq * qbar[:, None, :]).sum(-1), rtol=1e-12)
+
+
+def test_zero_budget_scores_zero():
+    K = rand_keys(1, 300, seed=4)
+    planes, meta, var = oracle.pack(K, 256)
+    q = np.ones((1, D), np.float32)
+    bits, qbar = oracle.allocate(q, var, 0, 1)
+    assert bits.sum() == 0
+    s, _ = oracle.scan(planes, meta, bits, qbar, 300, 256)
+    assert (s == 0).all()
+
+
+def test_scan_reads_only_chosen_planes():
+    """Flipping a plane at or below a channel's depth changes nothing."""
+    rows, n, S = 1, 256, 256
+    K = rand_keys(rows, n, seed=9)
+    planes, meta, var = oracle.pack(K, S)
+    q = np.random.default_rng(0).standard_normal((1, D)).astype(np.float32)
+    bits, qbar = oracle.allocate(q, var, 92, 1)
+    s0, _ = oracle.scan(planes, meta, bits, qbar, n, S)
+    p2 = planes.copy()
+    for c in range(D):
+        for j in range(int(bits[0, c]), 4):
+            p2[0, :, c, j, :] ^= np.uint32(0xFFFFFFFF)
+    s1, _ = oracle.scan(p2, meta, bits, qbar, n, S)
+    assert np.array_equal(s0, s1)
+
+
+# ---------------------------------------------------------- water-filling ---
+def gains_f32(w):
+    """Gain of plane j: w multiplied j times by 0.25 in fp32."""
+    g = np.zeros((len(w), 4), np.float32)
+    cur = np.asarray(w, np.float32).copy()
+    for j in range(4):
+        g[:, j] = cur
+        cur = (cur * np.float32(0.25)).astype(np.float32)
+    return g
+
+
+def waterfill_by_sort(w, B):
+    """The definition: take the B largest gains, ties to smaller plane j, then smaller channel c."""
+    g = gains_f32(w)
+    cand = sorted(((-float(g[c, j]), j, c) for c in range(len(w)) for j in range(4)))
+    bits = np.zeros(len(w), np.int64)
+    for _, j, c in cand[:B]:
+        bits[c] += 1
+    return bits
+
+
+def test_waterfill_hand_example():
+    w = [16.0, 4.0, 1.0, 0.0]
+    want = {0: (0, 0, 0, 0), 1: (1, 0, 0, 0), 2: (1, 1, 0, 0), 3: (2, 1, 0, 0), 4: (2, 1, 1, 0),
+            5: (2, 2, 1, 0), 6: (3, 2, 1, 0), 7: (3, 2, 2, 0), 16: (4, 4, 4, 4)}
+    for B, b in want.items():
+        assert tuple(oracle.waterfill(np.array(w, np.float32), B)) == b, B
+
+
+def _random_weights(rng, kind):
+    if kind == "lognormal":
+        return np.exp(rng.normal(0, 3, D)).astype(np.float32)
+    if kind == "ties":
+        return rng.choice(np.array([0.0, 1.0, 4.0, 16.0, 0.25], np.float32), D)
+    if kind == "zeros":
+        w = np.exp(rng.normal(0, 1, D)).astype(np.float32)
+        w[rng.random(D) < 0.5] = 0.0
+        return w
+    if kind == "tiny":
+        return (rng.random(D) * 1e-38).astype(np.float32)  # subnormal gains
+    if kind == "equal":
+        return np.full(D, 2.5, np.float32)
+    raise ValueError(kind)
+
+
+@pytest.mark.parametrize("kind", ["lognormal", "ties", "zeros", "tiny", "equal"])
+def test_waterfill_threshold_search_equals_sort_definition(kind):
+    rng = np.random.default_rng(hash(kind) % 1000)
+    for trial in range(6):
+        w = _random_weights(rng, kind)
+        for B in [0, 1, 2, 48, 68, 92, 136, 256, 300, 511, 512]:
+            got = oracle.waterfill(w, B)
+            want = waterfill_by_sort(w, B)
+            assert np.array_equal(got.astype(np.int64), want), (kind, trial, B)
+            assert got.sum() == B
+            assert got.max() <= 4
+            order = np.argsort(-w.astype(np.float64), kind="stable")
+            for a, b in zip(order, order[1:]):  # monotone in w
+                if w[a] > w[b]:
+                    assert got[a] >= got[b]
+
+
+def test_waterfill_is_optimal_by_brute_force():
+    """Reverse water-filling maximises the total error reduction for the budget (exact arithmetic)."""
+    rng = np.random.default_rng(7)
+    for d in [2, 3, 4]:
+        for trial in range(20):
+            w = rng.choice(np.array([0, 1, 2, 3, 5, 8, 16, 64], np.float32), d)
+            for B in range(0, 4 * d + 1):
+                best = None
+                for b in itertools.product(range(5), repeat=d):
+                    if sum(b) != B:
+                        continue
+                    v = sum(Fraction(float(w[c])) / 4 ** j for c in range(d) for j in range(b[c]))
+                    best = v if best is None or v > best else best
+                got = oracle.waterfill(w, B)
+                v = sum(Fraction(float(w[c])) / 4 ** j for c in range(d) for j in range(int(got[c])))
+                assert v == best, (w, B, got)
+
+
+def test_allocate_uses_group_sum_and_variance():
+    rng = np.random.default_rng(3)
+    rows, g = 3, 4
+    q = rng.standard_normal((rows * g, D)).astype(np.float32)
+    var = np.exp(rng.normal(0, 1, (rows, D))).astype(np.float32)
+    bits, qbar = oracle.allocate(q, var, 92, g)
+    want_qbar = q.astype(np.float64).reshape(rows, g, D).sum(1)
+    np.testing.assert_allclose(qbar, want_qbar, rtol=1e-6, atol=1e-6)
+    for r in range(rows):
+        w = (qbar[r] * qbar[r]).astype(np.float32) * var[r]
+        assert np.array_equal(bits[r].astype(np.int64), waterfill_by_sort(w.astype(np.float32), 92))
+    # per-row budgets
+    bits2, _ = oracle.allocate(q, var, np.array([0, 68, 512], np.int32), g)
+    assert list(bits2.sum(1)) == [0, 68, 512]
+    with pytest.raises(ValueError):
+        oracle.allocate(q, var, 513, g)
+
+
+# ------------------------------------------------------------------ top-k ---
+def brute_topk(s, k):
+    order = sorted(range(len(s)), key=lambda i: (-float(s[i]), i))
+    sel = sorted(order[:k])
+    return sel + [-1] * (k - len(sel))
+
+
+@pytest.mark.parametrize("n", [1, 5, 64, 257, 4096])
+def test_topk_equals_brute_force_sort(n):
+    rng = np.random.default_rng(n)
+    for kind in ["cont", "ties", "zeros"]:
+        if kind == "cont":
+            s = rng.standard_normal(n).astype(np.float32)
+        elif kind == "ties":
+            s = rng.choice(np.linspace(-2, 2, 8).astype(np.float32), n)
+        else:
+            s = rng.choice(np.array([0.0, -0.0, 1.0], np.float32), n)
+        for k in sorted({1, max(1, n // 2), max(1, n - 1), n, n + 3}):
+            got = oracle.topk_f32(s[None, :], k)[0]
+            assert list(got) == brute_topk(s, k), (kind, n, k)
+            got64 = oracle.topk_f64(s[None, :].astype(np.float64), k)[0]
+            assert list(got64) == brute_topk(s, k)
+
+
+def test_topk_negative_zero_equals_positive_zero():
+    s = np.array([-0.0, 0.0, -0.0, 0.0], np.float32)
+    assert list(oracle.topk_f32(s[None], 2)[0]) == [0, 1]
+
+
+# -------------------------------------------------------------- attention ---
+def dense_attention(q, K, V):
+    z = q.astype(np.float64) @ K.astype(np.float64).T / math.sqrt(D)
+    z -= z.max(-1, keepdims=True)
+    p = np.exp(z)
+    p /= p.sum(-1, keepdims=True)
+    return p @ V.astype(np.float64)
+
+
+def test_sparse_attention_with_all_keys_is_dense_attention():
+    rng = np.random.default_rng(8)
+    rows, g, n = 2, 4, 200
+    q = rng.standard_normal((rows * g, D)).astype(np.float32)
+    K = rng.standard_normal((rows, n, D)).astype(np.float32)
+    V = rng.standard_normal((rows, n, D)).astype(np.float32)
+    idx = np.tile(np.arange(n, dtype=np.int32), (rows, 1))
+    out = oracle.sparse_attn(q, K, V, idx, g)
+    for r in range(rows):
+        np.testing.assert_allclose(out[r * g:(r + 1) * g], dense_attention(q[r * g:(r + 1) * g], K[r], V[r]),
+                                   rtol=1e-12, atol=1e-12)
+
+
+def test_sparse_attention_special_cases():
+    rng = np.random.default_rng(9)
+    n, g = 50, 2
+    q = rng.standard_normal((g, D)).astype(np.float32)
+    K = rng.standard_normal((1, n, D)).astype(np.float32)
+    V = rng.standard_normal((1, n, D)).astype(np.float32)
+    out1 = oracle.sparse_attn(q, K, V, np.array([[7]], np.int32), g)
+    np.testing.assert_array_equal(out1, np.repeat(V[0, 7][None].astype(np.float64), g, 0))  # one key: its value
+    sel = np.array([[3, 9, 20, 41]], np.int32)
+    a = oracle.sparse_attn(q, K, V, sel, g)
+    b = oracle.sparse_attn(q, K, V, np.array([[41, -1, 9, 3, 20, -1]], np.int32), g)  # order, padding
+    np.testing.assert_allclose(a, b, rtol=1e-14, atol=1e-15)
+    np.testing.assert_allclose(a, dense_attention(q, K[0, sel[0]], V[0, sel[0]]), rtol=1e-12, atol=1e-12)
+
+
+# ------------------------------------------------------- fixed 136 bits ---
+def test_fixed136_pack_and_scan():
+    rng = np.random.default_rng(10)
+    rows, n = 2, 300
+    K = rand_keys(rows, n, seed=12)
+    K[0, 5, :] = 0.0
+    var = K.astype(np.float64).var(1).astype(np.float32)
+    var[1, 10] = var[1, 11]  # a tie in the channel choice
+    chans, codes, exps = oracle.fixed136_pack(K, var)
+    for r in range(rows):
+        want = np.sort(np.argsort(-var[r].astype(np.float64), kind="stable")[:32])
+        assert np.array_equal(chans[r], want)
+    nib = np.zeros((rows, n, 32), np.int64)
+    for i in range(32):
+        v = (codes[:, :, i // 2] >> (4 * (i % 2))) & 0xF
+        nib[:, :, i] = np.where(v >= 8, v.astype(np.int64) - 16, v)
+    assert nib.min() >= -7 and nib.max() <= 7
+    e = exps.astype(np.int64) - 127
+    for r in range(rows):
+        x = K[r][:, chans[r]].astype(np.float64)
+        mx = np.abs(x).max(1)
+        nz = mx > 0
+        assert np.all(7 * 2.0 ** e[r][nz] >= mx[nz]) and np.all(7 * 2.0 ** (e[r][nz] - 1) < mx[nz])
+        scale = 2.0 ** e[r][:, None]
+        assert np.all(np.abs(x - nib[r] * scale) <= scale / 2 + 1e-12)
+        assert (nib[r][~nz] == 0).all()
+    qbar = rng.standard_normal((rows, D)).astype(np.float32)
+    s, _ = oracle.fixed136_scan(chans, codes, exps, qbar)
+    for r in range(rows):
+        want = (nib[r] * 2.0 ** e[r][:, None]) @ qbar[r, chans[r]].astype(np.float64)
+        np.testing.assert_allclose(s[r], want, rtol=1e-13, atol=1e-13)
+
+
+# ------------------------------------------------------------ decode step ---
+def test_decode_step_composes_the_steps():
+    rng = np.random.default_rng(13)
+    rows, g, n, S, k = 3, 4, 900, 512, 40
+    K = rand_keys(rows, n, seed=14)
+    V = rng.standard_normal((rows, n, D)).astype(np.float32)
+    q = rng.standard_normal((rows * g, D)).astype(np.float32)
+    planes, meta, var = oracle.pack(K, S)
+    budget = np.array([68, 92, 136], np.int32)
+    idx, out = oracle.decode_step(planes, meta, var, q, budget, K, V, k, g, S)
+    bits, qbar = oracle.allocate(q, var, budget, g)
+    s, _ = oracle.scan(planes, meta, bits, qbar, n, S)
+    idx2 = oracle.topk_f64(s, k)
+    assert np.array_equal(idx, idx2)
+    out2 = oracle.sparse_attn(q, K, V, idx2, g)
+    np.testing.assert_array_equal(out, out2)
