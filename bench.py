@@ -1,0 +1,538 @@
+#!/usr/bin/env python
+"""Benchmark of the Fathom decode step on one GB300.
+
+Workload (default "million"): 36 layers x 8 KV heads x 128 dims, 32 query heads
+(GQA 4), n = 2^20 tokens, bit-plane index and bf16 K/V in pinned host memory
+read over the host link, B = 92 bits per token, k = 2048 winners per KV head.
+A step is one decode step of the whole model: for each of the 36 layers in
+order, allocate -> scan -> top-k -> sparse attention (the layers run in
+sequence as in a real decode step), captured once as a CUDA graph.
+
+Reported (one JSON line):
+  value        keys scanned per second through the whole step (n x 288 / step)
+  ms_per_step  decode-step time (CUDA events on the launching stream)
+  scan         scan-only keys/s and GB/s of the scan kernel
+  roofline     the scan kernel against the host link's measured streaming-read
+               peak (index in host memory), and against HBM for the same
+               workload with everything in HBM (hbm_resident block)
+  comparator   the fixed 136-bit index on the same workload and residency
+  e2e          the same metric through the public API with the step's query
+               copied in from pinned host memory and its output copied back
+  cpu_baseline the CPU oracle on a bounded sample of rows, on the host cores
+
+--impl reference times the CPU oracle (the only "reference" in this repository:
+the pages ship no runnable code) on a bounded row sample of the same workload.
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+D = 128
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=3)
+    p.add_argument("--impl", default="fathom", choices=["fathom", "reference"])
+    p.add_argument("--workload", default="million")
+    p.add_argument("--budget", type=int, default=92)
+    p.add_argument("--residency", default="both", choices=["host", "device", "both"])
+    p.add_argument("--superblock", type=int, default=4096)
+    p.add_argument("--kv-layers", type=int, default=18,
+                   help="distinct layers of K/V stored (layer l uses the keys/values of l mod this)")
+    p.add_argument("--no-comparator", action="store_true")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--layers", type=int, default=None, help="override layer count (smaller runs)")
+    p.add_argument("--n", type=int, default=None, help="override tokens per row (smaller runs)")
+    p.add_argument("--profile", action="store_true", help="few launches, for ncu")
+    return p.parse_args()
+
+
+# --------------------------------------------------------------- clocks ---
+class Clocks:
+    """nvidia-smi sampled every 200 ms during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index=0):
+        self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        self.p = None
+        self.gpu = gpu_index
+
+    def start(self):
+        try:
+            self.p = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.Q,
+                                       "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.f,
+                                      stderr=subprocess.DEVNULL)
+        except OSError:
+            self.p = None
+
+    def stop(self):
+        if self.p is None:
+            return None
+        self.p.terminate()
+        self.p.wait()
+        self.f.flush()
+        rows = []
+        for line in open(self.f.name):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append(dict(sm=float(parts[1]), smax=float(parts[2]), power=float(parts[3]),
+                                 hw=parts[5], hwt=parts[6], swt=parts[7], pcap=parts[8]))
+            except ValueError:
+                continue
+        os.unlink(self.f.name)
+        if not rows:
+            return None
+        reasons = set()
+        for r in rows:
+            for key, name in [("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"), ("swt", "sw_thermal_slowdown"),
+                              ("pcap", "sw_power_cap")]:
+                if r[key].lower() == "active":
+                    reasons.add(name)
+        loaded = [r["sm"] for r in rows if r["power"] > 200] or [r["sm"] for r in rows]
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(r["smax"] for r in rows),
+                "reasons": sorted(reasons), "samples": len(rows)}
+
+
+# ------------------------------------------------------------- workload ---
+class Model:
+    """All layers of one workload: index, K/V and queries, in the chosen residency.
+
+    kv_layers < layers stores keys and values of only that many distinct layers:
+    layer l holds the same synthetic keys and values as layer l mod kv_layers
+    (its own copy of the index, its own queries), so every byte a step moves is
+    still moved, from distinct index memory, while the K/V store shrinks."""
+
+    def __init__(self, w, budget, S, residency, comparator, log, kv_layers=None):
+        import sparse_top_kv_fathom_gb300 as F
+        from sparse_top_kv_fathom_gb300 import synth
+        self.F, self.w, self.S, self.budget = F, w, S, budget
+        L, H, n = w.layers, w.kv_heads, w.n
+        self.kv_layers = KL = min(L, kv_layers or L)
+        rows = w.rows
+        dev = torch.device("cuda")
+        ps, ms = F.index_shapes(n, rows, S)
+        host = residency in ("host", "both")
+        devr = residency in ("device", "both")
+        t0 = time.time()
+        pin = dict(pin_memory=True)
+        self.h = {}
+        self.d = {}
+        kvrows = KL * H
+        for store, kw in ((self.h, pin), (self.d, dict(device=dev))):
+            if (store is self.h and not host) or (store is self.d and not devr):
+                continue
+            store["planes"] = torch.empty(ps, dtype=torch.int32, **kw)
+            store["meta"] = torch.empty(ms, dtype=torch.float16, **kw)
+            store["K"] = torch.empty((kvrows, n, D), dtype=w.kv_dtype, **kw)
+            store["V"] = torch.empty((kvrows, n, D), dtype=w.kv_dtype, **kw)
+            if comparator:
+                store["codes"] = torch.empty((rows, n, 16), dtype=torch.uint8, **kw)
+                store["exps"] = torch.empty((rows, n), dtype=torch.uint8, **kw)
+        log("allocated buffers in %.1f s" % (time.time() - t0))
+        self.var = torch.empty((rows, D), dtype=torch.float32, device=dev)
+        self.chans = torch.empty((rows, 32), dtype=torch.int32, device=dev)
+        self.q = torch.cat([synth.queries(w, l, dev) for l in range(L)]).contiguous()
+        t0 = time.time()
+        for src in range(KL):
+            s0, s1 = src * H, (src + 1) * H
+            K = torch.stack([synth.keys(w, r, dev) for r in range(s0, s1)])
+            V = torch.stack([synth.values(w, r, dev) for r in range(s0, s1)])
+            ix = F.pack(K, S)
+            fx = F.fixed136_pack(K, ix.var) if comparator else None
+            for store in (self.h, self.d):
+                if store:
+                    store["K"][s0:s1].copy_(K)
+                    store["V"][s0:s1].copy_(V)
+            for l in range(src, L, KL):
+                r0, r1 = l * H, (l + 1) * H
+                self.var[r0:r1] = ix.var
+                if fx is not None:
+                    self.chans[r0:r1] = fx.chans
+                for store in (self.h, self.d):
+                    if not store:
+                        continue
+                    store["planes"][r0:r1].copy_(ix.planes)
+                    store["meta"][r0:r1].copy_(ix.meta)
+                    if fx is not None:
+                        store["codes"][r0:r1].copy_(fx.codes)
+                        store["exps"][r0:r1].copy_(fx.exps)
+            del K, V, ix, fx
+        torch.cuda.synchronize()
+        log("generated and packed %d distinct layers (%d rows x %d tokens) in %.1f s"
+            % (KL, rows, n, time.time() - t0))
+
+    def kv_rows(self, l):
+        H = self.w.kv_heads
+        s = l % self.kv_layers
+        return s * H, (s + 1) * H
+
+    def layer_index(self, store, l):
+        H = self.w.kv_heads
+        r0, r1 = l * H, (l + 1) * H
+        return self.F.BitPlaneIndex(store["planes"][r0:r1], store["meta"][r0:r1], self.var[r0:r1], self.w.n, H,
+                                    self.S)
+
+    def steps(self, store, q, out, idx, ws=None):
+        """Per-layer DecodeStep objects sharing one workspace; outputs are views of out/idx."""
+        F, w = self.F, self.w
+        H, G = w.kv_heads, w.group
+        ix0 = self.layer_index(store, 0)
+        nb = F.DecodeStep.workspace_bytes(ix0, w.k, G)
+        ws = ws if ws is not None else torch.empty(nb, dtype=torch.uint8, device="cuda")
+        out_b = torch.empty(out.shape, dtype=torch.bfloat16, device="cuda")
+        res = []
+        for l in range(w.layers):
+            r0, r1 = l * H, (l + 1) * H
+            k0, k1 = self.kv_rows(l)
+            res.append(F.DecodeStep(self.layer_index(store, l), store["K"][k0:k1], store["V"][k0:k1],
+                                    q[r0 * G:r1 * G], w.k, G, self.budget, workspace=ws,
+                                    idx=idx[r0:r1], out=out[r0 * G:r1 * G], out_bf16=out_b[r0 * G:r1 * G]))
+        return res
+
+    def comparator_steps(self, store, q, out, idx):
+        F, w = self.F, self.w
+        H, G = w.kv_heads, w.group
+        res = []
+        ws = None
+        for l in range(w.layers):
+            r0, r1 = l * H, (l + 1) * H
+            k0, k1 = self.kv_rows(l)
+            fx = F.Fixed136Index(self.chans[r0:r1], store["codes"][r0:r1], store["exps"][r0:r1], w.n, H)
+            st = F.Fixed136Step(fx, store["K"][k0:k1], store["V"][k0:k1], q[r0 * G:r1 * G], w.k, G, workspace=ws,
+                                idx=idx[r0:r1], out=out[r0 * G:r1 * G])
+            ws = st.ws
+            res.append(st)
+        return res
+
+
+def capture(fns, stream):
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        for f in fns:  # warm (first-call attribute setup happens outside capture)
+            f()
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g, stream=stream):
+            for f in fns:
+                f()
+    torch.cuda.synchronize()
+    return g
+
+
+def time_graph(g, steps, warmup, stream, clocks=None):
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            g.replay()
+        torch.cuda.synchronize()
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+        if clocks:
+            clocks.start()
+        barrier()
+        torch.cuda.synchronize()
+        ev[0].record(stream)
+        for i in range(steps):
+            g.replay()
+            ev[i + 1].record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        ck = clocks.stop() if clocks else None
+    per = [ev[i].elapsed_time(ev[i + 1]) for i in range(steps)]
+    return ev[0].elapsed_time(ev[-1]), per, ck
+
+
+def barrier():
+    if torch.distributed.is_available() and torch.distributed.is_initialized():
+        torch.distributed.barrier()
+
+
+def max_over_ranks(x):
+    if torch.distributed.is_available() and torch.distributed.is_initialized():
+        t = torch.tensor([x], dtype=torch.float64, device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        return float(t.item())
+    return x
+
+
+def scan_timing(model, store, steps, stream):
+    """Average duration of the scan kernel launches of one step (per layer), with
+    allocate run once beforehand; CUDA events on the launching stream."""
+    F, w = model.F, model.w
+    H, G = w.kv_heads, w.group
+    layers = []
+    for l in range(w.layers):
+        ix = model.layer_index(store, l)
+        bits, qbar = F.allocate(model.q[l * H * G:(l + 1) * H * G], ix.var, model.budget, G)
+        scores = torch.empty((H, w.n), dtype=torch.float32, device="cuda")
+        layers.append((ix, bits, qbar, scores))
+    torch.cuda.synchronize()
+    import ctypes
+    from sparse_top_kv_fathom_gb300 import _native as N
+    L = F.load()
+    calls = []
+    for ix, bits, qbar, scores in layers:
+        d = ix.desc
+        calls.append((d, ctypes.c_void_p(ix.planes.data_ptr()), ctypes.c_void_p(ix.meta.data_ptr()),
+                      ctypes.c_void_p(bits.data_ptr()), ctypes.c_void_p(qbar.data_ptr()),
+                      ctypes.c_void_p(scores.data_ptr())))
+    sp = ctypes.c_void_p(stream.cuda_stream)
+    durs = []
+    with torch.cuda.stream(stream):
+        for rep in range(steps + 1):
+            evs = [torch.cuda.Event(enable_timing=True) for _ in range(2 * len(calls))]
+            for i, c in enumerate(calls):
+                evs[2 * i].record(stream)
+                N.check(L.fathom_scan(ctypes.byref(c[0]), c[1], c[2], c[3], c[4], c[5], sp))
+                evs[2 * i + 1].record(stream)
+            torch.cuda.synchronize()
+            if rep > 0:
+                durs += [evs[2 * i].elapsed_time(evs[2 * i + 1]) for i in range(len(calls))]
+    # algorithmic bytes per launch (one layer): plane bytes B*n/8 per row + 4 B of meta per active channel per block
+    nblk = -(-w.n // 128)
+    algo = []
+    for ix, bits, qbar, scores in layers:
+        b = bits.to(torch.int64)
+        algo.append(int(b.sum().item()) * w.n // 8 + int((b > 0).sum().item()) * nblk * 4)
+    return statistics.mean(durs), statistics.mean(algo), durs
+
+
+def link_peak(log):
+    """Host-link streaming-read peak: zero-copy 16 B loads over pinned host memory, best of several shapes."""
+    import sparse_top_kv_fathom_gb300 as F
+    buf = torch.empty(4 << 30, dtype=torch.uint8, pin_memory=True)
+    buf.fill_(1)
+    sink = torch.zeros(1, dtype=torch.int32, device="cuda")
+    best = 0.0
+    for bps in (2, 4, 8):
+        for thr in (256, 512, 1024):
+            for _ in range(2):
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                nb = F.probe_stream_read(buf, bps, thr, sink)
+                e1.record()
+                torch.cuda.synchronize()
+                best = max(best, nb / (e0.elapsed_time(e1) * 1e6))
+    h2d = 0.0
+    dbuf = torch.empty(buf.numel(), dtype=torch.uint8, device="cuda")
+    for _ in range(3):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        dbuf.copy_(buf, non_blocking=True)
+        e1.record()
+        torch.cuda.synchronize()
+        h2d = max(h2d, buf.numel() / (e0.elapsed_time(e1) * 1e6))
+    log("host link: zero-copy read %.1f GB/s, copy-engine H2D %.1f GB/s" % (best, h2d))
+    del buf, dbuf
+    return best, h2d
+
+
+def cpu_baseline(model, store, log, seconds=(10.0, 30.0)):
+    """The oracle's decode step on a bounded sample of rows (layer 0), on all host cores."""
+    import oracle
+    w = model.w
+    H, G = w.kv_heads, w.group
+    rows = H
+    planes = store["planes"][:rows].numpy().view(np.uint32)
+    meta = store["meta"][:rows].numpy().view(np.uint16)
+    var = model.var[:rows].cpu().numpy()
+    q = model.q[: rows * G].float().cpu().numpy()
+    K = store["K"][:rows].float().numpy() if store["K"].device.type == "cpu" else store["K"][:rows].float().cpu().numpy()
+    V = store["V"][:rows].float().numpy() if store["V"].device.type == "cpu" else store["V"][:rows].float().cpu().numpy()
+    reps, t = 0, 0.0
+    t0 = time.time()
+    while t < seconds[0] and reps < 50:
+        oracle.decode_step(planes, meta, var, q, model.budget, K, V, w.k, G, model.S)
+        reps += 1
+        t = time.time() - t0
+    keys = reps * rows * w.n
+    log("cpu oracle: %d reps of %d rows in %.1f s" % (reps, rows, t))
+    return {"value": keys / t, "unit": "keys/s", "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": "%d repetitions of the decode step (allocate, fp64 scan, top-k, attention) on the %d KV "
+                      "heads of layer 0 at n=%d, B=%d, k=%d; %.1f s" % (reps, rows, w.n, model.budget, w.k, t)}
+
+
+def run_reference(args, log):
+    """CPU oracle as the reference arm: each step = the oracle's decode step over a bounded row sample."""
+    import oracle
+    from sparse_top_kv_fathom_gb300 import synth
+    w = synth.WORKLOADS[args.workload]
+    if args.layers or args.n:
+        w = synth.scaled(w, layers=args.layers or w.layers, n=args.n or w.n)
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    rows = w.kv_heads
+    G = w.group
+    K = torch.stack([synth.keys(w, r, dev) for r in range(rows)]).float().cpu().numpy()
+    V = torch.stack([synth.values(w, r, dev) for r in range(rows)]).float().cpu().numpy()
+    q = synth.queries(w, 0, dev).float().cpu().numpy()
+    planes, meta, var = oracle.pack(K, args.superblock)
+    times = []
+    for i in range(args.warmup + args.steps):
+        t0 = time.time()
+        oracle.decode_step(planes, meta, var, q, args.budget, K, V, w.k, G, args.superblock)
+        if i >= args.warmup:
+            times.append(time.time() - t0)
+    per = statistics.mean(times)
+    value = rows * w.n / per
+    return {"impl": "reference", "metric": "decode-step scan throughput (keys/s) at n=%d, B=%d" % (w.n, args.budget),
+            "value": value, "unit": "keys/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": per * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "layers": w.layers, "kv_heads": w.kv_heads, "group": w.group, "n": w.n,
+                       "budget": args.budget, "k": w.k, "sample_rows": rows},
+            "cpu_baseline": {"value": value, "unit": "keys/s", "cores": oracle.num_threads(), "kind": "oracle",
+                             "sample": "each step: the oracle decode step on the %d KV heads of layer 0 at full n"
+                                       % rows},
+            "e2e": {"value": value, "unit": "keys/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    args = parse()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    def log(msg):
+        if rank == 0:
+            print("[bench] " + msg, file=sys.stderr, flush=True)
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        print(json.dumps(run_reference(args, log)), flush=True)
+        return
+
+    torch.cuda.set_device(local)
+    if world > 1:
+        torch.distributed.init_process_group("nccl")
+    import sparse_top_kv_fathom_gb300 as F
+    from sparse_top_kv_fathom_gb300 import synth
+    F.load()
+    w = synth.WORKLOADS[args.workload]
+    if args.layers or args.n:
+        w = synth.scaled(w, layers=args.layers or w.layers, n=args.n or w.n)
+    comparator = not args.no_comparator
+    log("workload %s: %d layers x %d KV heads, n=%d, B=%d, k=%d" % (w.name, w.layers, w.kv_heads, w.n, args.budget,
+                                                                  w.k))
+    peak = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))) if os.path.exists(
+        os.path.join(ROOT, "MEASURED_PEAKS.json")) else {}
+    hbm_peak = peak.get("hbm_gbs", 6800.0)
+    link_gbs, h2d_gbs = link_peak(log)
+    model = Model(w, args.budget, args.superblock, args.residency, comparator, log, args.kv_layers)
+    stream = torch.cuda.Stream()
+    keys_per_step = w.rows * w.n
+    result = {}
+    primary = "host" if args.residency in ("host", "both") else "device"
+    for res in (["host", "device"] if args.residency == "both" else [args.residency]):
+        store = model.h if res == "host" else model.d
+        q = model.q
+        out = torch.empty((w.rows * w.group, D), dtype=torch.float32, device="cuda")
+        idx = torch.empty((w.rows, w.k), dtype=torch.int32, device="cuda")
+        steps = model.steps(store, q, out, idx)
+        g = capture(steps, stream)
+        clocks = Clocks(local) if res == primary else None
+        total, per, ck = time_graph(g, args.steps, args.warmup, stream, clocks)
+        total = max_over_ranks(total)
+        ms = total / args.steps
+        scan_ms, scan_bytes, _ = scan_timing(model, store, max(3, args.steps // 4), stream)
+        r = {"ms_per_step": ms, "keys_per_s": keys_per_step * world / (ms * 1e-3), "per_step_ms": per,
+             "scan_ms_per_layer": scan_ms, "scan_algo_bytes_per_layer": scan_bytes,
+             "scan_gbs": scan_bytes / (scan_ms * 1e6),
+             "scan_keys_per_s": w.kv_heads * w.n / (scan_ms * 1e-3), "clocks": ck}
+        if comparator:
+            cout = torch.empty_like(out)
+            cidx = torch.empty_like(idx)
+            cg = capture(model.comparator_steps(store, q, cout, cidx), stream)
+            ctot, _, _ = time_graph(cg, args.steps, args.warmup, stream)
+            r["comparator_ms_per_step"] = max_over_ranks(ctot) / args.steps
+            r["comparator_bytes_per_step"] = w.rows * w.n * 17
+            del cg
+        if res == primary:
+            # e2e: q in from pinned host memory, output back to pinned host memory, every step
+            qh = model.q.cpu().pin_memory()
+            oh = torch.empty(out.shape, dtype=torch.float32, pin_memory=True)
+            with torch.cuda.stream(stream):
+                for i in range(args.warmup + args.steps):
+                    if i == args.warmup:
+                        torch.cuda.synchronize()
+                        barrier()
+                        e0 = torch.cuda.Event(enable_timing=True)
+                        e0.record(stream)
+                        w0 = time.time()
+                    model.q.copy_(qh, non_blocking=True)
+                    g.replay()
+                    oh.copy_(out, non_blocking=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e1.record(stream)
+                torch.cuda.synchronize()
+                barrier()
+                wall = time.time() - w0
+            e2e_ms = max_over_ranks(e0.elapsed_time(e1)) / args.steps
+            r["e2e"] = {"value": keys_per_step * world / (e2e_ms * 1e-3), "unit": "keys/s",
+                        "ms_per_step": e2e_ms, "wall_ms_per_step": wall * 1e3 / args.steps,
+                        "h2d_bytes_per_step": qh.numel() * qh.element_size(),
+                        "d2h_bytes_per_step": oh.numel() * oh.element_size()}
+        del g
+        result[res] = r
+    p = result[primary]
+    scan_peak = link_gbs if primary == "host" else hbm_peak
+    line = {
+        "metric": "scan keys/s and decode-step ms at n=%d, B=%d (36-layer step); GB/s vs HBM / host-link peak"
+                  % (w.n, args.budget),
+        "value": p["keys_per_s"], "unit": "keys/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": p["ms_per_step"], "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "u32/f32", "data": "synthetic",
+        "config": {"workload": w.name, "layers": w.layers, "kv_heads": w.kv_heads, "group": w.group, "n": w.n,
+                   "budget": args.budget, "k": w.k, "superblock": args.superblock,
+                   "kv_layers_stored": model.kv_layers,
+                   "residency": "index and K/V in pinned host memory" if primary == "host" else "HBM",
+                   "l2": "inputs larger than L2 (index %.1f GB per step)" % (p["scan_algo_bytes_per_layer"] *
+                                                                            w.layers / 1e9)},
+        "scan": {"keys_per_s": p["scan_keys_per_s"] * world, "gbs": p["scan_gbs"],
+                 "ms_per_layer": p["scan_ms_per_layer"]},
+        "roofline": {"bound": "host_link" if primary == "host" else "hbm", "achieved": p["scan_gbs"],
+                     "peak": scan_peak, "unit": "GB/s", "frac": p["scan_gbs"] / scan_peak, "traffic": None,
+                     "kernel": "scan_kernel",
+                     "peak_source": ("zero-copy streaming read of pinned host memory measured in this run"
+                                     if primary == "host" else "MEASURED_PEAKS.json hbm_gbs")},
+        "link": {"zero_copy_read_gbs": link_gbs, "copy_engine_h2d_gbs": h2d_gbs},
+        "e2e": p.get("e2e"),
+        "clocks": p.get("clocks"),
+        "gpu_launches": args.steps * w.layers * 7,
+    }
+    if "device" in result and primary == "host":
+        d = result["device"]
+        line["hbm_resident"] = {"ms_per_step": d["ms_per_step"], "keys_per_s": d["keys_per_s"],
+                                "scan_gbs": d["scan_gbs"], "scan_ms_per_layer": d["scan_ms_per_layer"],
+                                "scan_frac_of_hbm": d["scan_gbs"] / hbm_peak,
+                                "comparator_ms_per_step": d.get("comparator_ms_per_step")}
+    if comparator:
+        line["comparator"] = {"index": "fixed 136-bit (32 channels x 4 bit + 8-bit scale)",
+                              "ms_per_step": p.get("comparator_ms_per_step"),
+                              "fathom_speedup": p.get("comparator_ms_per_step", 0) / p["ms_per_step"]}
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(model, model.h if model.h else model.d, log)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -207,9 +207,11 @@ int fathom_decode_step(const fathom_step_desc* step, void* workspace, size_t ws_
  *   codes  device uint8 [rows][n][16] out: byte i holds channel 2i in its low
  *          nibble and channel 2i+1 in its high nibble (two's complement).
  *   exps   device uint8 [rows][n] out: e + 127.
+ *   workspace  device scratch of fathom_fixed136_pack_workspace_bytes.
  * Synchronises `stream` (EDATA as for fathom_pack). */
+int fathom_fixed136_pack_workspace_bytes(int rows, int64_t n, size_t* bytes);
 int fathom_fixed136_pack(int rows, int64_t n, const void* K, int k_dtype, const float* var, int32_t* chans,
-                         uint8_t* codes, uint8_t* exps, void* stream);
+                         uint8_t* codes, uint8_t* exps, void* workspace, size_t ws_bytes, void* stream);
 
 /* Scores of the comparator: s(t) = 2^e(t) * sum_i qbar_{chans_i} * code_i(t). */
 int fathom_fixed136_scan(int rows, int64_t n, const int32_t* chans, const uint8_t* codes, const uint8_t* exps,

@@ -1,0 +1,11 @@
+"""Fathom decode-step hot path on GB300 (sm_103a).
+
+Bit-plane packing of a 4-bit K cache, per-query reverse water-filling,
+variable-depth plane scan, exact top-k and sparse GQA attention, implemented as
+hand-written CUDA behind the C ABI of include/fathom.h (libfathom.so); this
+package only marshals torch tensors into that library.
+"""
+from ._native import FathomError, load  # noqa: F401
+from .api import (  # noqa: F401
+    BF16, D, F16, F32, QBLOCK, BitPlaneIndex, DecodeStep, Fixed136Index, Fixed136Step, allocate, decode_step,
+    fixed136_pack, fixed136_scan, index_bytes, index_shapes, pack, probe_stream_read, scan, sparse_attn, topk)

@@ -1,0 +1,86 @@
+"""ctypes declarations of libfathom.so (include/fathom.h).  Marshalling only."""
+import ctypes
+import os
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libfathom.so")
+
+P = ctypes.c_void_p
+I32 = ctypes.c_int
+I64 = ctypes.c_int64
+SZ = ctypes.c_size_t
+SZP = ctypes.POINTER(ctypes.c_size_t)
+
+
+class IndexDesc(ctypes.Structure):
+    _fields_ = [("n", ctypes.c_int64), ("rows", ctypes.c_int32), ("d", ctypes.c_int32),
+                ("block", ctypes.c_int32), ("superblock", ctypes.c_int32)]
+
+
+class StepDesc(ctypes.Structure):
+    _fields_ = [("index", IndexDesc), ("group", ctypes.c_int32), ("budget", ctypes.c_int32),
+                ("k", ctypes.c_int64), ("q_dtype", ctypes.c_int32), ("kv_dtype", ctypes.c_int32),
+                ("planes", P), ("meta", P), ("var", P), ("budgets", P), ("q", P), ("K", P), ("V", P),
+                ("idx", P), ("out", P), ("out_bf16", P), ("status", P)]
+
+
+class Fixed136StepDesc(ctypes.Structure):
+    _fields_ = [("n", ctypes.c_int64), ("rows", ctypes.c_int32), ("group", ctypes.c_int32),
+                ("k", ctypes.c_int64), ("q_dtype", ctypes.c_int32), ("kv_dtype", ctypes.c_int32),
+                ("chans", P), ("codes", P), ("exps", P), ("q", P), ("K", P), ("V", P),
+                ("idx", P), ("out", P), ("out_bf16", P)]
+
+
+IDP = ctypes.POINTER(IndexDesc)
+
+# name -> (argtypes, restype)
+SIGNATURES = {
+    "fathom_last_error": ([], ctypes.c_char_p),
+    "fathom_abi_version": ([], I32),
+    "fathom_index_bytes": ([IDP, SZP, SZP], I32),
+    "fathom_pack_workspace_bytes": ([IDP, SZP], I32),
+    "fathom_pack": ([IDP, P, I32, P, P, P, P, SZ, P], I32),
+    "fathom_allocate": ([I32, I32, P, I32, P, P, I32, P, P, P, P], I32),
+    "fathom_scan": ([IDP, P, P, P, P, P, P], I32),
+    "fathom_topk_workspace_bytes": ([I32, I64, I64, SZP], I32),
+    "fathom_topk": ([I32, I64, I64, P, P, P, P, SZ, P], I32),
+    "fathom_sparse_attn_workspace_bytes": ([I32, I32, I64, SZP], I32),
+    "fathom_sparse_attn": ([I32, I32, I64, I64, P, I32, P, P, I32, P, P, P, P, SZ, P], I32),
+    "fathom_decode_step_workspace_bytes": ([ctypes.POINTER(StepDesc), SZP], I32),
+    "fathom_decode_step": ([ctypes.POINTER(StepDesc), P, SZ, P], I32),
+    "fathom_fixed136_pack_workspace_bytes": ([I32, I64, SZP], I32),
+    "fathom_fixed136_pack": ([I32, I64, P, I32, P, P, P, P, P, SZ, P], I32),
+    "fathom_fixed136_scan": ([I32, I64, P, P, P, P, P, P], I32),
+    "fathom_fixed136_step_workspace_bytes": ([ctypes.POINTER(Fixed136StepDesc), SZP], I32),
+    "fathom_fixed136_decode_step": ([ctypes.POINTER(Fixed136StepDesc), P, SZ, P], I32),
+    "fathom_probe_stream_read": ([P, SZ, I32, I32, P, P], I32),
+}
+
+_lib = None
+
+
+def load(path=LIB_PATH):
+    """Load the CUDA library.  Raises if it has not been built: there is no fallback."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(path):
+            raise RuntimeError("libfathom.so not built (run __graft_entry__.build() or "
+                               "python sparse_top_kv_fathom_gb300/build.py): %s" % path)
+        lib = ctypes.CDLL(path)
+        for name, (args, res) in SIGNATURES.items():
+            f = getattr(lib, name)
+            f.argtypes = args
+            f.restype = res
+        _lib = lib
+    return _lib
+
+
+class FathomError(RuntimeError):
+    def __init__(self, code, msg):
+        super().__init__("fathom error %d: %s" % (code, msg))
+        self.code = code
+
+
+def check(rc):
+    if rc != 0:
+        raise FathomError(rc, _lib.fathom_last_error().decode(errors="replace"))

@@ -1,0 +1,291 @@
+"""Torch-facing wrappers over the C ABI (include/fathom.h).
+
+Argument marshalling only: every step of the decode path runs in libfathom's
+CUDA kernels.  Torch provides device memory, pinned host memory and streams.
+If the library is missing the calls raise; there is no CPU fallback.
+"""
+import ctypes
+from dataclasses import dataclass
+
+import torch
+
+from . import _native as N
+
+D = 128
+QBLOCK = 128
+F32, F16, BF16 = 0, 1, 2
+_DT = {torch.float32: F32, torch.float16: F16, torch.bfloat16: BF16}
+
+
+def lib():
+    return N.load()
+
+
+def _dt(t):
+    try:
+        return _DT[t.dtype]
+    except KeyError:
+        raise TypeError("unsupported dtype %s" % t.dtype)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _ws(nbytes, device):
+    return torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+
+
+def _desc(n, rows, S):
+    return N.IndexDesc(int(n), int(rows), D, QBLOCK, int(S))
+
+
+def index_bytes(n, rows, superblock):
+    """(plane bytes, meta bytes) of a packed index (host-only query)."""
+    L = lib()
+    pb, mb = ctypes.c_size_t(), ctypes.c_size_t()
+    d = _desc(n, rows, superblock)
+    N.check(L.fathom_index_bytes(ctypes.byref(d), ctypes.byref(pb), ctypes.byref(mb)))
+    return pb.value, mb.value
+
+
+@dataclass
+class BitPlaneIndex:
+    """Packed index.  planes: int32 (bit patterns) [rows][nsb][128][4][S/32];
+    meta: fp16 [rows][128][nblk][2] (lo, delta); var: fp32 [rows][128]."""
+    planes: torch.Tensor
+    meta: torch.Tensor
+    var: torch.Tensor
+    n: int
+    rows: int
+    superblock: int
+
+    @property
+    def desc(self):
+        return _desc(self.n, self.rows, self.superblock)
+
+    def to_host(self):
+        """A copy whose planes and meta live in pinned host memory (read over the host link)."""
+        return BitPlaneIndex(self.planes.cpu().pin_memory(), self.meta.cpu().pin_memory(), self.var, self.n,
+                             self.rows, self.superblock)
+
+
+def index_shapes(n, rows, superblock):
+    nsb = -(-n // superblock)
+    nblk = -(-n // QBLOCK)
+    return (rows, nsb, D, 4, superblock // 32), (rows, D, nblk, 2)
+
+
+def pack(K, superblock=4096, stream=None):
+    """K: [rows][n][128] cuda tensor (fp32/fp16/bf16) -> BitPlaneIndex on K's device."""
+    L = lib()
+    rows, n, d = K.shape
+    assert d == D and K.is_cuda and K.is_contiguous()
+    ps, ms = index_shapes(n, rows, superblock)
+    planes = torch.empty(ps, dtype=torch.int32, device=K.device)
+    meta = torch.empty(ms, dtype=torch.float16, device=K.device)
+    var = torch.empty((rows, D), dtype=torch.float32, device=K.device)
+    desc = _desc(n, rows, superblock)
+    wsb = ctypes.c_size_t()
+    N.check(L.fathom_pack_workspace_bytes(ctypes.byref(desc), ctypes.byref(wsb)))
+    ws = _ws(wsb.value, K.device)
+    N.check(L.fathom_pack(ctypes.byref(desc), _ptr(K), _dt(K), _ptr(planes), _ptr(meta), _ptr(var), _ptr(ws),
+                          wsb.value, _stream(stream)))
+    return BitPlaneIndex(planes, meta, var, n, rows, superblock)
+
+
+def allocate(q, var, budget, group, status=None, stream=None):
+    """q: [rows*group][128]; var: [rows][128]; budget: int or int16 cuda tensor [rows]
+    -> (bits uint8 [rows][128], qbar fp32 [rows][128])."""
+    L = lib()
+    rows = var.shape[0]
+    bits = torch.empty((rows, D), dtype=torch.uint8, device=q.device)
+    qbar = torch.empty((rows, D), dtype=torch.float32, device=q.device)
+    budgets = budget if isinstance(budget, torch.Tensor) else None
+    scalar = 0 if budgets is not None else int(budget)
+    N.check(L.fathom_allocate(rows, group, _ptr(q), _dt(q), _ptr(var), _ptr(budgets), scalar, _ptr(bits),
+                              _ptr(qbar), _ptr(status), _stream(stream)))
+    return bits, qbar
+
+
+def scan(index, bits, qbar, stream=None):
+    """Scores fp32 [rows][n] from only the planes each row's depths select."""
+    L = lib()
+    scores = torch.empty((index.rows, index.n), dtype=torch.float32, device=bits.device)
+    d = index.desc
+    N.check(L.fathom_scan(ctypes.byref(d), _ptr(index.planes), _ptr(index.meta), _ptr(bits), _ptr(qbar),
+                          _ptr(scores), _stream(stream)))
+    return scores
+
+
+def topk(scores, k, with_values=False, stream=None):
+    """Indices int32 [rows][k] (ascending; ties to the lower index; -1 padding when k > n)."""
+    L = lib()
+    rows, n = scores.shape
+    idx = torch.empty((rows, k), dtype=torch.int32, device=scores.device)
+    vals = torch.empty((rows, k), dtype=torch.float32, device=scores.device) if with_values else None
+    wsb = ctypes.c_size_t()
+    N.check(L.fathom_topk_workspace_bytes(rows, n, k, ctypes.byref(wsb)))
+    ws = _ws(wsb.value, scores.device)
+    N.check(L.fathom_topk(rows, n, k, _ptr(scores), _ptr(idx), _ptr(vals), _ptr(ws), wsb.value, _stream(stream)))
+    return (idx, vals) if with_values else idx
+
+
+def sparse_attn(q, K, V, idx, group, stream=None):
+    """Attention over the selected rows -> (out fp32 [rows*group][128], out bf16)."""
+    L = lib()
+    rows, n, _ = K.shape
+    k = idx.shape[1]
+    dev = q.device
+    out = torch.empty((rows * group, D), dtype=torch.float32, device=dev)
+    outb = torch.empty((rows * group, D), dtype=torch.bfloat16, device=dev)
+    wsb = ctypes.c_size_t()
+    N.check(L.fathom_sparse_attn_workspace_bytes(rows, group, k, ctypes.byref(wsb)))
+    ws = _ws(wsb.value, dev)
+    N.check(L.fathom_sparse_attn(rows, group, n, k, _ptr(q), _dt(q), _ptr(K), _ptr(V), _dt(K), _ptr(idx), _ptr(out),
+                                 _ptr(outb), _ptr(ws), wsb.value, _stream(stream)))
+    return out, outb
+
+
+class DecodeStep:
+    """A reusable decode step over one index: workspace and outputs are allocated once,
+    so repeated calls launch kernels only (and can be captured in a CUDA graph).
+
+    index: BitPlaneIndex (planes/meta on the device or in pinned host memory)
+    K, V:  [rows][n][128] (device or pinned host), q: [rows*group][128] (device)."""
+
+    def __init__(self, index, K, V, q, k, group, budget, status=None, device=None, workspace=None, idx=None,
+                 out=None, out_bf16=None):
+        self.L = lib()
+        self.index, self.K, self.V, self.q = index, K, V, q
+        dev = device if device is not None else q.device
+        rows = index.rows
+        self.idx = idx if idx is not None else torch.empty((rows, k), dtype=torch.int32, device=dev)
+        self.out = out if out is not None else torch.empty((rows * group, D), dtype=torch.float32, device=dev)
+        self.out_bf16 = (out_bf16 if out_bf16 is not None else
+                         torch.empty((rows * group, D), dtype=torch.bfloat16, device=dev))
+        self.budgets = budget if isinstance(budget, torch.Tensor) else None
+        self.status = status
+        self.desc = N.StepDesc()
+        self.desc.index = index.desc
+        self.desc.group = group
+        self.desc.budget = 0 if self.budgets is not None else int(budget)
+        self.desc.k = k
+        self.desc.q_dtype = _dt(q)
+        self.desc.kv_dtype = _dt(K)
+        self._bind()
+        wsb = ctypes.c_size_t()
+        N.check(self.L.fathom_decode_step_workspace_bytes(ctypes.byref(self.desc), ctypes.byref(wsb)))
+        if workspace is not None:
+            if workspace.numel() * workspace.element_size() < wsb.value:
+                raise ValueError("workspace smaller than %d bytes" % wsb.value)
+            self.ws = workspace
+        else:
+            self.ws = _ws(wsb.value, dev)
+        self.ws_bytes = wsb.value
+
+    @staticmethod
+    def workspace_bytes(index, k, group):
+        d = N.StepDesc()
+        d.index, d.group, d.k = index.desc, group, k
+        wsb = ctypes.c_size_t()
+        N.check(lib().fathom_decode_step_workspace_bytes(ctypes.byref(d), ctypes.byref(wsb)))
+        return wsb.value
+
+    def _bind(self):
+        d = self.desc
+        d.planes, d.meta, d.var = self.index.planes.data_ptr(), self.index.meta.data_ptr(), self.index.var.data_ptr()
+        d.budgets = self.budgets.data_ptr() if self.budgets is not None else None
+        d.q, d.K, d.V = self.q.data_ptr(), self.K.data_ptr(), self.V.data_ptr()
+        d.idx, d.out, d.out_bf16 = self.idx.data_ptr(), self.out.data_ptr(), self.out_bf16.data_ptr()
+        d.status = self.status.data_ptr() if self.status is not None else None
+
+    def __call__(self, stream=None):
+        N.check(self.L.fathom_decode_step(ctypes.byref(self.desc), _ptr(self.ws), self.ws_bytes, _stream(stream)))
+        return self.idx, self.out, self.out_bf16
+
+
+def decode_step(index, q, K, V, k, group, budget, stream=None):
+    st = DecodeStep(index, K, V, q, k, group, budget)
+    return st(stream)
+
+
+# ------------------------------------------------------- fixed 136-bit comparator ---
+@dataclass
+class Fixed136Index:
+    chans: torch.Tensor   # int32 [rows][32]
+    codes: torch.Tensor   # uint8 [rows][n][16]
+    exps: torch.Tensor    # uint8 [rows][n]
+    n: int
+    rows: int
+
+
+def fixed136_pack(K, var, stream=None):
+    L = lib()
+    rows, n, _ = K.shape
+    chans = torch.empty((rows, 32), dtype=torch.int32, device=K.device)
+    codes = torch.empty((rows, n, 16), dtype=torch.uint8, device=K.device)
+    exps = torch.empty((rows, n), dtype=torch.uint8, device=K.device)
+    wsb = ctypes.c_size_t()
+    N.check(L.fathom_fixed136_pack_workspace_bytes(rows, n, ctypes.byref(wsb)))
+    ws = _ws(wsb.value, K.device)
+    N.check(L.fathom_fixed136_pack(rows, n, _ptr(K), _dt(K), _ptr(var), _ptr(chans), _ptr(codes), _ptr(exps),
+                                   _ptr(ws), wsb.value, _stream(stream)))
+    return Fixed136Index(chans, codes, exps, n, rows)
+
+
+def fixed136_scan(index, qbar, stream=None):
+    L = lib()
+    scores = torch.empty((index.rows, index.n), dtype=torch.float32, device=qbar.device)
+    N.check(L.fathom_fixed136_scan(index.rows, index.n, _ptr(index.chans), _ptr(index.codes), _ptr(index.exps),
+                                   _ptr(qbar), _ptr(scores), _stream(stream)))
+    return scores
+
+
+class Fixed136Step:
+    """Reusable comparator decode step (qbar -> 136-bit scan -> top-k -> attention)."""
+
+    def __init__(self, index, K, V, q, k, group, device=None, workspace=None, idx=None, out=None, out_bf16=None):
+        self.L = lib()
+        self.index, self.K, self.V, self.q = index, K, V, q
+        dev = device if device is not None else q.device
+        self.idx = idx if idx is not None else torch.empty((index.rows, k), dtype=torch.int32, device=dev)
+        self.out = out if out is not None else torch.empty((index.rows * group, D), dtype=torch.float32, device=dev)
+        self.out_bf16 = (out_bf16 if out_bf16 is not None else
+                         torch.empty((index.rows * group, D), dtype=torch.bfloat16, device=dev))
+        d = self.desc = N.Fixed136StepDesc()
+        d.n, d.rows, d.group, d.k = index.n, index.rows, group, k
+        d.q_dtype, d.kv_dtype = _dt(q), _dt(K)
+        d.chans, d.codes, d.exps = index.chans.data_ptr(), index.codes.data_ptr(), index.exps.data_ptr()
+        d.q, d.K, d.V = q.data_ptr(), K.data_ptr(), V.data_ptr()
+        d.idx, d.out, d.out_bf16 = self.idx.data_ptr(), self.out.data_ptr(), self.out_bf16.data_ptr()
+        wsb = ctypes.c_size_t()
+        N.check(self.L.fathom_fixed136_step_workspace_bytes(ctypes.byref(d), ctypes.byref(wsb)))
+        if workspace is not None:
+            if workspace.numel() * workspace.element_size() < wsb.value:
+                raise ValueError("workspace smaller than %d bytes" % wsb.value)
+            self.ws = workspace
+        else:
+            self.ws = _ws(wsb.value, dev)
+        self.ws_bytes = wsb.value
+
+    def __call__(self, stream=None):
+        N.check(self.L.fathom_fixed136_decode_step(ctypes.byref(self.desc), _ptr(self.ws), self.ws_bytes,
+                                                   _stream(stream)))
+        return self.idx, self.out, self.out_bf16
+
+
+def probe_stream_read(buf, blocks_per_sm=4, threads=512, sink=None, stream=None):
+    """Launch one streaming read over `buf` (device or pinned host tensor)."""
+    L = lib()
+    if sink is None:
+        sink = torch.zeros(1, dtype=torch.int32, device="cuda")
+    nbytes = buf.numel() * buf.element_size()
+    nbytes -= nbytes % 16
+    N.check(L.fathom_probe_stream_read(_ptr(buf), nbytes, blocks_per_sm, threads, _ptr(sink), _stream(stream)))
+    return nbytes

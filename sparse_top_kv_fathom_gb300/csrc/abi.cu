@@ -1,0 +1,107 @@
+// Host-side plumbing of the C ABI: error reporting, pointer validation,
+// index geometry and size queries.  No kernels here.
+#include <stdarg.h>
+#include <stdio.h>
+
+#include "common.cuh"
+
+namespace fathom {
+
+static thread_local char g_err[512] = "";
+
+int set_error(int code, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_err, sizeof(g_err), fmt, ap);
+  va_end(ap);
+  return code;
+}
+
+void clear_error() { g_err[0] = 0; }
+
+int cuda_check(cudaError_t e, const char* what) {
+  if (e == cudaSuccess) return FATHOM_OK;
+  return set_error(FATHOM_ECUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+int device_view(const void* p, const char* name, const void** dev, bool nullable, int* is_host) {
+  if (is_host) *is_host = 0;
+  if (p == nullptr) {
+    *dev = nullptr;
+    if (nullable) return FATHOM_OK;
+    return set_error(FATHOM_EINVAL, "%s is NULL", name);
+  }
+  cudaPointerAttributes a;
+  cudaError_t e = cudaPointerGetAttributes(&a, p);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return set_error(FATHOM_EINVAL, "%s: not a CUDA-visible pointer (%s)", name, cudaGetErrorString(e));
+  }
+  switch (a.type) {
+    case cudaMemoryTypeDevice:
+    case cudaMemoryTypeManaged:
+      *dev = p;
+      return FATHOM_OK;
+    case cudaMemoryTypeHost:
+      if (a.devicePointer == nullptr)
+        return set_error(FATHOM_EINVAL, "%s: pinned host memory not mapped into the device address space", name);
+      *dev = a.devicePointer;
+      if (is_host) *is_host = 1;
+      return FATHOM_OK;
+    default:
+      return set_error(FATHOM_EINVAL, "%s: ordinary host memory; pass device or pinned (mapped) host memory", name);
+  }
+}
+
+int num_sms() {
+  static int sms = 0;
+  if (sms == 0) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+      cudaGetLastError();
+      sms = 148;
+    }
+  }
+  return sms;
+}
+
+int index_geom(const fathom_index_desc* d, IndexGeom* g) {
+  if (!d) return set_error(FATHOM_EINVAL, "index desc is NULL");
+  if (d->d != kD) return set_error(FATHOM_EINVAL, "d must be 128 (got %d)", d->d);
+  if (d->block != kBlock) return set_error(FATHOM_EINVAL, "block must be 128 (got %d)", d->block);
+  if (d->n < 1 || d->n > (int64_t(1) << 31) - 1) return set_error(FATHOM_EINVAL, "n must be in [1, 2^31-1]");
+  if (d->rows < 1) return set_error(FATHOM_EINVAL, "rows must be >= 1");
+  int S = d->superblock;
+  if (S < 128 || S > 65536 || (S & (S - 1)) != 0)
+    return set_error(FATHOM_EINVAL, "superblock must be a power of two in [128, 65536] (got %d)", S);
+  g->n = d->n;
+  g->rows = d->rows;
+  g->S = S;
+  g->nsb = (d->n + S - 1) / S;
+  g->nblk = (d->n + kBlock - 1) / kBlock;
+  int l = 0;
+  while ((1 << l) < S) ++l;
+  g->log2S = l;
+  return FATHOM_OK;
+}
+
+}  // namespace fathom
+
+using namespace fathom;
+
+extern "C" {
+
+const char* fathom_last_error(void) { return g_err; }
+
+int fathom_abi_version(void) { return 1; }
+
+int fathom_index_bytes(const fathom_index_desc* desc, size_t* plane_bytes, size_t* meta_bytes) {
+  IndexGeom g;
+  FATHOM_TRY(index_geom(desc, &g));
+  if (!plane_bytes || !meta_bytes) return set_error(FATHOM_EINVAL, "output pointers are NULL");
+  *plane_bytes = size_t(g.rows) * g.nsb * kD * kPlanes * (g.S / 32) * sizeof(uint32_t);
+  *meta_bytes = size_t(g.rows) * kD * g.nblk * 2 * sizeof(uint16_t);
+  return FATHOM_OK;
+}
+
+}  // extern "C"

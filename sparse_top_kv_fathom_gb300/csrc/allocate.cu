@@ -1,0 +1,120 @@
+// fathom_allocate: per-query reverse water-filling of a bits-per-token budget.
+//
+// Fathom article, "How each query picks its own depth": a channel's importance
+// is the share of score variance it carries; one more bit on a channel removes
+// error in proportion to that importance divided by four to the power of the
+// bits already spent; the budget goes to the largest such marginal gains (the
+// page finds the cut by binary-searching a threshold; selecting the B largest
+// gains with a fixed tie order is the same allocation).  Importance of channel c
+// is w_c = qbar_c^2 * var_c (Glonce summary: variance-weighted importance).
+//
+// GPU form: one CTA per row, one thread per candidate (channel c, plane j).
+// Each thread ranks its gain against all 512 candidates (gain descending, then
+// j ascending, then c ascending) and is taken if its rank is below the budget;
+// the rank is a total order, so exactly min(B, 512) candidates are taken.
+#include "common.cuh"
+
+namespace fathom {
+namespace {
+
+constexpr int kCand = kD * kPlanes;  // 512 candidates per row
+
+__global__ void __launch_bounds__(kCand) allocate_kernel(int group, const void* __restrict__ q, int q_dtype,
+                                                         const float* __restrict__ var,
+                                                         const uint16_t* __restrict__ budgets, int budget,
+                                                         uint8_t* __restrict__ bits, float* __restrict__ qbar,
+                                                         int32_t* __restrict__ status) {
+  __shared__ float s_gain[kCand];
+  __shared__ int s_count[kD];
+  __shared__ int s_bad;
+  const int r = blockIdx.x;
+  const int i = threadIdx.x;  // candidate index = j * 128 + c
+  const int c = i & (kD - 1), j = i >> 7;
+  if (i == 0) s_bad = 0;
+  if (i < kD) s_count[i] = 0;
+  __syncthreads();
+  float w = 0.0f;
+  if (j == 0) {
+    const int64_t q0 = int64_t(r) * group * kD + c;
+    float s = load_as_float(q, q0, q_dtype);
+    for (int h = 1; h < group; ++h) s = __fadd_rn(s, load_as_float(q, q0 + int64_t(h) * kD, q_dtype));
+    const float v = var[int64_t(r) * kD + c];
+    if (!isfinite(s) || !isfinite(v)) s_bad = 1;
+    qbar[int64_t(r) * kD + c] = s;
+    w = __fmul_rn(__fmul_rn(s, s), v);
+    s_gain[c] = w;
+  }
+  __syncthreads();
+  if (s_bad) {
+    if (i < kD) bits[int64_t(r) * kD + i] = 0;
+    if (i == 0 && status) atomicOr(status, FATHOM_STATUS_NONFINITE);
+    return;
+  }
+  if (j > 0) {
+    w = s_gain[c];
+    for (int jj = 0; jj < j; ++jj) w = __fmul_rn(w, 0.25f);
+  }
+  __syncthreads();  // everyone has read s_gain[c] before it is overwritten below
+  s_gain[i] = w;
+  __syncthreads();
+  int B = budgets ? int(budgets[r]) : budget;
+  if (B > kCand) {
+    if (i == 0 && status) atomicOr(status, FATHOM_STATUS_BUDGET_CLAMPED);
+    B = kCand;
+  }
+  int rank = 0;
+#pragma unroll 8
+  for (int o = 0; o < kCand; ++o) {
+    const float g = s_gain[o];
+    rank += (g > w) || (g == w && o < i);
+  }
+  if (rank < B) atomicAdd(&s_count[c], 1);
+  __syncthreads();
+  if (i < kD) bits[int64_t(r) * kD + i] = uint8_t(s_count[i]);
+}
+
+__global__ void __launch_bounds__(kD) qbar_kernel(int group, const void* __restrict__ q, int q_dtype,
+                                                  float* __restrict__ qbar) {
+  const int r = blockIdx.x, c = threadIdx.x;
+  const int64_t q0 = int64_t(r) * group * kD + c;
+  float s = load_as_float(q, q0, q_dtype);
+  for (int h = 1; h < group; ++h) s = __fadd_rn(s, load_as_float(q, q0 + int64_t(h) * kD, q_dtype));
+  qbar[int64_t(r) * kD + c] = s;
+}
+
+}  // namespace
+
+cudaError_t launch_allocate(int rows, int group, const void* q, int q_dtype, const float* var, const uint16_t* budgets,
+                            int budget, uint8_t* bits, float* qbar, int32_t* status, cudaStream_t st) {
+  allocate_kernel<<<rows, kCand, 0, st>>>(group, q, q_dtype, var, budgets, budget, bits, qbar, status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_qbar(int rows, int group, const void* q, int q_dtype, float* qbar, cudaStream_t st) {
+  qbar_kernel<<<rows, kD, 0, st>>>(group, q, q_dtype, qbar);
+  return cudaGetLastError();
+}
+
+}  // namespace fathom
+
+using namespace fathom;
+
+extern "C" int fathom_allocate(int rows, int group, const void* q, int q_dtype, const float* var,
+                               const uint16_t* budgets, int budget, uint8_t* bits, float* qbar, int32_t* status,
+                               void* stream) {
+  clear_error();
+  if (rows < 1 || group < 1 || group > 64) return set_error(FATHOM_EINVAL, "rows >= 1 and 1 <= group <= 64 required");
+  if (!valid_dtype(q_dtype)) return set_error(FATHOM_EINVAL, "q_dtype %d invalid", q_dtype);
+  if (!budgets && (budget < 0 || budget > kD * kPlanes))
+    return set_error(FATHOM_EINVAL, "budget %d outside [0, 512]", budget);
+  const void *dq, *dv, *db, *dbits, *dqb, *dst;
+  FATHOM_TRY(device_view(q, "q", &dq));
+  FATHOM_TRY(device_view(var, "var", &dv));
+  FATHOM_TRY(device_view(budgets, "budgets", &db, true));
+  FATHOM_TRY(device_view(bits, "bits", &dbits));
+  FATHOM_TRY(device_view(qbar, "qbar", &dqb));
+  FATHOM_TRY(device_view(status, "status", &dst, true));
+  FATHOM_TRY_CUDA(launch_allocate(rows, group, dq, q_dtype, (const float*)dv, (const uint16_t*)db, budget,
+                                  (uint8_t*)dbits, (float*)dqb, (int32_t*)dst, as_stream(stream)));
+  return FATHOM_OK;
+}

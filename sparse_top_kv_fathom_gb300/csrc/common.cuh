@@ -1,0 +1,115 @@
+// Internal helpers shared by the CUDA sources of libfathom (not part of the ABI).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <string>
+
+#include "../../include/fathom.h"
+
+namespace fathom {
+
+constexpr int kD = 128;      // channels per KV head
+constexpr int kBlock = 128;  // tokens per quantisation block
+constexpr int kPlanes = 4;   // 4-bit codes
+
+// ---------------------------------------------------------------- errors ---
+int set_error(int code, const char* fmt, ...);
+void clear_error();
+int cuda_check(cudaError_t e, const char* what);
+#define FATHOM_TRY_CUDA(call)                          \
+  do {                                                 \
+    cudaError_t e_ = (call);                           \
+    if (e_ != cudaSuccess) return cuda_check(e_, #call); \
+  } while (0)
+#define FATHOM_TRY(call)       \
+  do {                         \
+    int r_ = (call);           \
+    if (r_ != FATHOM_OK) return r_; \
+  } while (0)
+
+// Resolve a pointer the GPU will dereference.  Accepts device memory, managed
+// memory, and pinned host memory that is mapped into the device's address
+// space (returned through *dev).  NULL is rejected unless `nullable`.
+int device_view(const void* p, const char* name, const void** dev, bool nullable = false, int* is_host = nullptr);
+
+inline cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
+
+int num_sms();
+
+// --------------------------------------------------------------- dtypes ---
+__device__ __forceinline__ float load_as_float(const void* p, int64_t i, int dtype) {
+  if (dtype == FATHOM_F32) return reinterpret_cast<const float*>(p)[i];
+  if (dtype == FATHOM_F16) return __half2float(reinterpret_cast<const __half*>(p)[i]);
+  return __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(p)[i]);
+}
+
+inline bool valid_dtype(int d) { return d == FATHOM_F32 || d == FATHOM_F16 || d == FATHOM_BF16; }
+inline size_t dtype_size(int d) { return d == FATHOM_F32 ? 4 : 2; }
+
+// Order-preserving map of an fp32 score to uint32 (larger score -> larger key),
+// with -0.0 mapped like +0.0.
+__device__ __forceinline__ uint32_t score_key(float s) {
+  uint32_t u = __float_as_uint(s);
+  if (u == 0x80000000u) u = 0u;
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float key_score(uint32_t k) {
+  uint32_t u = (k & 0x80000000u) ? (k & 0x7fffffffu) : ~k;
+  return __uint_as_float(u);
+}
+
+// Workspace carving: 256-byte aligned slices of one caller buffer.
+struct Carve {
+  char* base;
+  size_t off;
+  size_t cap;
+  explicit Carve(void* b, size_t c) : base(static_cast<char*>(b)), off(0), cap(c) {}
+  template <class T>
+  T* take(size_t count) {
+    off = (off + 255) & ~size_t(255);
+    T* p = reinterpret_cast<T*>(reinterpret_cast<uintptr_t>(base) + off);  // base 0: offsets only
+    off += count * sizeof(T);
+    return p;
+  }
+  bool fits() const { return off <= cap; }
+};
+
+// --------------------------------------------------- internal launchers ---
+struct IndexGeom {
+  int64_t n;
+  int rows;
+  int S;
+  int64_t nsb;   // superblocks per row
+  int64_t nblk;  // 128-token blocks per row
+  int log2S;
+};
+int index_geom(const fathom_index_desc* d, IndexGeom* g);
+
+// workspace layout queries (bytes for a null base)
+size_t topk_ws_bytes(int rows, int64_t n, int64_t k);
+size_t attn_ws_bytes(int rows, int group, int64_t k);
+
+// launchers used by the step functions (arguments already validated)
+cudaError_t launch_allocate(int rows, int group, const void* q, int q_dtype, const float* var, const uint16_t* budgets,
+                            int budget, uint8_t* bits, float* qbar, int32_t* status, cudaStream_t st);
+cudaError_t launch_qbar(int rows, int group, const void* q, int q_dtype, float* qbar, cudaStream_t st);
+cudaError_t launch_scan(const IndexGeom& g, const uint32_t* planes, const __half2* meta, const uint8_t* bits,
+                        const float* qbar, float* scores, uint32_t* hist, cudaStream_t st);
+cudaError_t launch_topk(int rows, int64_t n, int64_t k, const float* scores, int32_t* idx, float* vals, void* ws,
+                        bool hist_ready, cudaStream_t st);
+cudaError_t launch_attn(int rows, int group, int64_t n, int64_t k, const void* q, int q_dtype, const void* K,
+                        const void* V, int kv_dtype, const int32_t* idx, float* out, uint16_t* out_bf16, void* ws,
+                        cudaStream_t st);
+cudaError_t launch_fixed136_scan(int rows, int64_t n, const int32_t* chans, const uint8_t* codes, const uint8_t* exps,
+                                 const float* qbar, float* scores, uint32_t* hist, cudaStream_t st);
+
+// top-k histogram geometry (12-bit first digit of the score key)
+constexpr int kHistBits = 12;
+constexpr int kHistBins = 1 << kHistBits;
+uint32_t* topk_hist_ptr(void* ws, int rows, int64_t n, int64_t k);
+
+}  // namespace fathom

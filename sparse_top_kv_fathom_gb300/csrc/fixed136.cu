@@ -1,0 +1,183 @@
+// The fixed-depth 136-bit comparator index: 32 channels chosen offline, read at
+// 4 bits for every key, plus an 8-bit power-of-two scale (Fathom article,
+// "The catch": Double Sparsity keeps 32 channels chosen offline; Loki, Double
+// Sparsity and SparQ land near 136 bits per token).  Channels: the 32 of
+// largest variance (ties to the lower channel).  Per token: scale 2^e with e
+// the smallest integer such that 7*2^e >= max|x| over those channels, codes
+// clamp(rint(x / 2^e), -7, 7) as signed nibbles; 16 B + 1 B = 136 bits.
+#include "common.cuh"
+
+namespace fathom {
+namespace {
+
+constexpr int kSel = 32;
+constexpr int kThreads = 256;
+constexpr int kErrRange = 1;
+
+__global__ void __launch_bounds__(kD) chans_kernel(const float* __restrict__ var, int32_t* __restrict__ chans) {
+  __shared__ float s_v[kD];
+  __shared__ int s_cnt[kD / 32];
+  const int r = blockIdx.x, c = threadIdx.x, lane = c & 31, warp = c >> 5;
+  s_v[c] = var[int64_t(r) * kD + c];
+  __syncthreads();
+  const float v = s_v[c];
+  int rank = 0;
+  for (int o = 0; o < kD; ++o) rank += (s_v[o] > v) || (s_v[o] == v && o < c);
+  const bool sel = rank < kSel;
+  const unsigned b = __ballot_sync(0xffffffffu, sel);
+  if (lane == 0) s_cnt[warp] = __popc(b);
+  __syncthreads();
+  int off = 0;
+  for (int w = 0; w < warp; ++w) off += s_cnt[w];
+  if (sel) chans[int64_t(r) * kSel + off + __popc(b & ((1u << lane) - 1u))] = c;
+}
+
+__global__ void __launch_bounds__(kThreads) pack136_kernel(int64_t n, const void* __restrict__ K, int k_dtype,
+                                                           const int32_t* __restrict__ chans,
+                                                           uint8_t* __restrict__ codes, uint8_t* __restrict__ exps,
+                                                           int* __restrict__ err) {
+  __shared__ int s_ch[kSel];
+  const int r = blockIdx.y;
+  if (threadIdx.x < kSel) s_ch[threadIdx.x] = chans[int64_t(r) * kSel + threadIdx.x];
+  __syncthreads();
+  const int64_t t = int64_t(blockIdx.x) * kThreads + threadIdx.x;
+  if (t >= n) return;
+  const int64_t base = (int64_t(r) * n + t) * kD;
+  float x[kSel];
+  float mx = 0.0f;
+  bool bad = false;
+#pragma unroll
+  for (int i = 0; i < kSel; ++i) {
+    x[i] = load_as_float(K, base + s_ch[i], k_dtype);
+    const float a = fabsf(x[i]);
+    bad |= !(a <= 65504.0f);
+    mx = a > mx ? a : mx;
+  }
+  if (bad) atomicOr(err, kErrRange);
+  int e = -127;
+  if (mx > 0.0f) {
+    int E;
+    frexpf(mx, &E);
+    e = (7.0f * ldexpf(1.0f, E - 3) >= mx) ? E - 3 : E - 2;
+  }
+  exps[int64_t(r) * n + t] = uint8_t(e + 127);
+  uint32_t wv[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+  for (int i = 0; i < kSel; ++i) {
+    int code = 0;
+    if (mx > 0.0f) {
+      const float qv = rintf(ldexpf(x[i], -e));
+      code = qv < -7.0f ? -7 : (qv > 7.0f ? 7 : int(qv));
+    }
+    wv[i / 8] |= uint32_t(code & 0xF) << (4 * (i % 8));
+  }
+  *reinterpret_cast<uint4*>(codes + (int64_t(r) * n + t) * 16) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+}
+
+template <bool kHist>
+__global__ void __launch_bounds__(kThreads) scan136_kernel(int64_t n, const int32_t* __restrict__ chans,
+                                                           const uint8_t* __restrict__ codes,
+                                                           const uint8_t* __restrict__ exps,
+                                                           const float* __restrict__ qbar, float* __restrict__ scores,
+                                                           uint32_t* __restrict__ hist) {
+  __shared__ float s_q[kSel];
+  __shared__ uint32_t s_hist[kHist ? kHistBins : 1];
+  const int r = blockIdx.y;
+  if (threadIdx.x < kSel) s_q[threadIdx.x] = qbar[int64_t(r) * kD + chans[int64_t(r) * kSel + threadIdx.x]];
+  if constexpr (kHist)
+    for (int i = threadIdx.x; i < kHistBins; i += kThreads) s_hist[i] = 0u;
+  __syncthreads();
+  const int64_t t = int64_t(blockIdx.x) * kThreads + threadIdx.x;
+  if (t < n) {
+    const uint4 cw = __ldg(reinterpret_cast<const uint4*>(codes + (int64_t(r) * n + t) * 16));
+    const int e = int(__ldg(exps + int64_t(r) * n + t)) - 127;
+    const uint32_t w[4] = {cw.x, cw.y, cw.z, cw.w};
+    float s = 0.0f;
+#pragma unroll
+    for (int i = 0; i < kSel; ++i) {
+      const int code = int(w[i / 8] << (28 - 4 * (i % 8))) >> 28;  // sign-extended nibble
+      s = fmaf(s_q[i], float(code), s);
+    }
+    s = ldexpf(s, e);
+    scores[int64_t(r) * n + t] = s;
+    if constexpr (kHist) atomicAdd(&s_hist[score_key(s) >> (32 - kHistBits)], 1u);
+  }
+  if constexpr (kHist) {
+    __syncthreads();
+    for (int i = threadIdx.x; i < kHistBins; i += kThreads)
+      if (s_hist[i]) atomicAdd(hist + int64_t(r) * kHistBins + i, s_hist[i]);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_fixed136_scan(int rows, int64_t n, const int32_t* chans, const uint8_t* codes, const uint8_t* exps,
+                                 const float* qbar, float* scores, uint32_t* hist, cudaStream_t st) {
+  dim3 grid(unsigned((n + kThreads - 1) / kThreads), unsigned(rows));
+  if (hist)
+    scan136_kernel<true><<<grid, kThreads, 0, st>>>(n, chans, codes, exps, qbar, scores, hist);
+  else
+    scan136_kernel<false><<<grid, kThreads, 0, st>>>(n, chans, codes, exps, qbar, scores, nullptr);
+  return cudaGetLastError();
+}
+
+}  // namespace fathom
+
+using namespace fathom;
+
+extern "C" {
+
+int fathom_fixed136_pack_workspace_bytes(int rows, int64_t n, size_t* bytes) {
+  clear_error();
+  if (rows < 1 || n < 1) return set_error(FATHOM_EINVAL, "rows or n out of range");
+  if (!bytes) return set_error(FATHOM_EINVAL, "bytes is NULL");
+  *bytes = 256;
+  return FATHOM_OK;
+}
+
+int fathom_fixed136_pack(int rows, int64_t n, const void* K, int k_dtype, const float* var, int32_t* chans,
+                         uint8_t* codes, uint8_t* exps, void* workspace, size_t ws_bytes, void* stream) {
+  clear_error();
+  if (rows < 1 || rows > 65535 || n < 1 || n > 0x7fffffff) return set_error(FATHOM_EINVAL, "rows or n out of range");
+  if (!valid_dtype(k_dtype)) return set_error(FATHOM_EINVAL, "k_dtype %d invalid", k_dtype);
+  const void *dK, *dV, *dC, *dX, *dE, *dW;
+  FATHOM_TRY(device_view(workspace, "workspace", &dW));
+  if (ws_bytes < 256) return set_error(FATHOM_ENOMEM, "workspace %zu < 256 bytes", ws_bytes);
+  FATHOM_TRY(device_view(K, "K", &dK));
+  FATHOM_TRY(device_view(var, "var", &dV));
+  FATHOM_TRY(device_view(chans, "chans", &dC));
+  FATHOM_TRY(device_view(codes, "codes", &dX));
+  FATHOM_TRY(device_view(exps, "exps", &dE));
+  if (reinterpret_cast<uintptr_t>(dX) & 15) return set_error(FATHOM_EINVAL, "codes must be 16-byte aligned");
+  cudaStream_t st = as_stream(stream);
+  int* err = static_cast<int*>(const_cast<void*>(dW));
+  FATHOM_TRY_CUDA(cudaMemsetAsync(err, 0, sizeof(int), st));
+  chans_kernel<<<rows, kD, 0, st>>>((const float*)dV, (int32_t*)dC);
+  FATHOM_TRY_CUDA(cudaGetLastError());
+  pack136_kernel<<<dim3(unsigned((n + kThreads - 1) / kThreads), unsigned(rows)), kThreads, 0, st>>>(
+      n, dK, k_dtype, (const int32_t*)dC, (uint8_t*)dX, (uint8_t*)dE, err);
+  FATHOM_TRY_CUDA(cudaGetLastError());
+  int herr = 0;
+  FATHOM_TRY_CUDA(cudaMemcpyAsync(&herr, err, sizeof(int), cudaMemcpyDeviceToHost, st));
+  FATHOM_TRY_CUDA(cudaStreamSynchronize(st));
+  if (herr & kErrRange) return set_error(FATHOM_EDATA, "K holds a non-finite value or one outside the fp16 range");
+  return FATHOM_OK;
+}
+
+int fathom_fixed136_scan(int rows, int64_t n, const int32_t* chans, const uint8_t* codes, const uint8_t* exps,
+                         const float* qbar, float* scores, void* stream) {
+  clear_error();
+  if (rows < 1 || rows > 65535 || n < 1 || n > 0x7fffffff) return set_error(FATHOM_EINVAL, "rows or n out of range");
+  const void *dC, *dX, *dE, *dQ, *dS;
+  FATHOM_TRY(device_view(chans, "chans", &dC));
+  FATHOM_TRY(device_view(codes, "codes", &dX));
+  FATHOM_TRY(device_view(exps, "exps", &dE));
+  FATHOM_TRY(device_view(qbar, "qbar", &dQ));
+  FATHOM_TRY(device_view(scores, "scores", &dS));
+  if (reinterpret_cast<uintptr_t>(dX) & 15) return set_error(FATHOM_EINVAL, "codes must be 16-byte aligned");
+  FATHOM_TRY_CUDA(launch_fixed136_scan(rows, n, (const int32_t*)dC, (const uint8_t*)dX, (const uint8_t*)dE,
+                                       (const float*)dQ, (float*)dS, nullptr, as_stream(stream)));
+  return FATHOM_OK;
+}
+
+}  // extern "C"

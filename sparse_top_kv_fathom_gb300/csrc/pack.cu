@@ -1,0 +1,198 @@
+// fathom_pack: K cache -> 4-bit bit-plane index (MSB-first planes, channel-major)
+// plus per-(channel, 128-token block) fp16 (lo, delta) and per-channel variance.
+//
+// Follows the Fathom article, "Bit planes: how a partial read becomes a valid
+// read" (store the first bits of a block of tokens together, then the second
+// bits...; plane 0 is the most significant bit) and the Glonce summary
+// (the 4-bit K cache is stored channel-major as bit planes).  Quantiser:
+// per channel per 128-token block, min/max with 15 steps, scale and offset
+// rounded to fp16 (128 ch x 4 bits + 128 x 4 B / 128 tokens = 68 B per token,
+// the article's storage figure in "Where this does not work").
+//
+// Every floating-point step uses explicitly rounded IEEE operations so the
+// result is reproducible bit for bit: fp32 for the quantiser, fp64 for the
+// variance (block sums in token order, then block sums in block order).
+#include "common.cuh"
+
+namespace fathom {
+namespace {
+
+constexpr int kErrRange = 1;
+
+// One CTA per (row, 128-token block), one thread per channel.
+// Blocks past n (padding inside the last superblock) write zero plane words.
+__global__ void __launch_bounds__(kD) pack_quant_kernel(const void* __restrict__ K, int k_dtype, int64_t n, int64_t nblk,
+                                                        int64_t nsb, int log2S, uint32_t* __restrict__ planes,
+                                                        __half2* __restrict__ meta, double* __restrict__ part,
+                                                        int* __restrict__ err) {
+  const int c = threadIdx.x;
+  const int64_t b = blockIdx.x;  // block index inside the row, < nsb * S / 128
+  const int r = blockIdx.y;
+  const int64_t S = int64_t(1) << log2S;
+  const int64_t t0 = b * kBlock;
+  const int64_t sb = t0 >> log2S;
+  const int64_t w0 = (t0 & (S - 1)) >> 5;  // first word of this block inside the (c, j) run
+  const int64_t run = S >> 5;
+  uint32_t* pw = planes + (((int64_t(r) * nsb + sb) * kD + c) * kPlanes) * run + w0;
+
+  if (t0 >= n) {  // padding block: zero words only
+    const uint4 z = make_uint4(0, 0, 0, 0);
+#pragma unroll
+    for (int j = 0; j < kPlanes; ++j) *reinterpret_cast<uint4*>(pw + j * run) = z;
+    return;
+  }
+  const int64_t t1 = (t0 + kBlock < n) ? t0 + kBlock : n;
+  const int64_t base = int64_t(r) * n * kD + c;
+
+  float lo = load_as_float(K, base + t0 * kD, k_dtype), hi = lo;
+  bool bad = !(fabsf(lo) <= 65504.0f);
+  for (int64_t t = t0 + 1; t < t1; ++t) {
+    float x = load_as_float(K, base + t * kD, k_dtype);
+    bad |= !(fabsf(x) <= 65504.0f);
+    if (x < lo) lo = x;
+    if (x > hi) hi = x;
+  }
+  if (bad) atomicOr(err, kErrRange);
+  const float delta = __fdiv_rn(__fsub_rn(hi, lo), 15.0f);
+  const __half lo16 = __float2half_rn(lo), d16 = __float2half_rn(delta);
+  meta[(int64_t(r) * kD + c) * nblk + b] = __halves2half2(lo16, d16);
+  const float lof = __half2float(lo16), df = __half2float(d16);
+
+  double psum = 0.0;
+  uint4 words[kPlanes];
+#pragma unroll
+  for (int wi = 0; wi < 4; ++wi) {
+    uint32_t a[kPlanes] = {0u, 0u, 0u, 0u};
+#pragma unroll 4
+    for (int bi = 0; bi < 32; ++bi) {
+      const int64_t t = t0 + wi * 32 + bi;
+      if (t < t1) {
+        const float x = load_as_float(K, base + t * kD, k_dtype);
+        psum = __dadd_rn(psum, double(x));
+        int code = 0;
+        if (df != 0.0f) {
+          const float qv = rintf(__fdiv_rn(__fsub_rn(x, lof), df));
+          code = qv < 0.0f ? 0 : (qv > 15.0f ? 15 : int(qv));
+        }
+#pragma unroll
+        for (int j = 0; j < kPlanes; ++j) a[j] |= uint32_t((code >> (3 - j)) & 1) << bi;
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < kPlanes; ++j) {
+      if (wi == 0) words[j].x = a[j];
+      else if (wi == 1) words[j].y = a[j];
+      else if (wi == 2) words[j].z = a[j];
+      else words[j].w = a[j];
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < kPlanes; ++j) *reinterpret_cast<uint4*>(pw + j * run) = words[j];
+  part[(int64_t(r) * kD + c) * nblk + b] = psum;
+}
+
+// One thread per (row, channel): sum block partials in block order.
+__global__ void pack_mean_kernel(const double* __restrict__ part, int rows, int64_t nblk, int64_t n,
+                                 double* __restrict__ mean) {
+  const int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= int64_t(rows) * kD) return;
+  const double* p = part + i * nblk;
+  double tot = 0.0;
+  for (int64_t b = 0; b < nblk; ++b) tot = __dadd_rn(tot, p[b]);
+  mean[i] = __ddiv_rn(tot, double(n));
+}
+
+// One CTA per (row, block), one thread per channel: sum of squared deviations.
+__global__ void __launch_bounds__(kD) pack_m2_kernel(const void* __restrict__ K, int k_dtype, int64_t n, int64_t nblk,
+                                                     const double* __restrict__ mean, double* __restrict__ part) {
+  const int c = threadIdx.x;
+  const int64_t b = blockIdx.x;
+  const int r = blockIdx.y;
+  const int64_t t0 = b * kBlock, t1 = (t0 + kBlock < n) ? t0 + kBlock : n;
+  const double mu = mean[int64_t(r) * kD + c];
+  const int64_t base = int64_t(r) * n * kD + c;
+  double s = 0.0;
+  for (int64_t t = t0; t < t1; ++t) {
+    const double dv = __dsub_rn(double(load_as_float(K, base + t * kD, k_dtype)), mu);
+    s = __dadd_rn(s, __dmul_rn(dv, dv));
+  }
+  part[(int64_t(r) * kD + c) * nblk + b] = s;
+}
+
+__global__ void pack_var_kernel(const double* __restrict__ part, int rows, int64_t nblk, int64_t n,
+                                float* __restrict__ var) {
+  const int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= int64_t(rows) * kD) return;
+  const double* p = part + i * nblk;
+  double m2 = 0.0;
+  for (int64_t b = 0; b < nblk; ++b) m2 = __dadd_rn(m2, p[b]);
+  var[i] = __double2float_rn(__ddiv_rn(m2, double(n)));
+}
+
+size_t pack_ws(const IndexGeom& g) {
+  Carve c(nullptr, 0);
+  c.take<double>(size_t(g.rows) * kD * g.nblk);
+  c.take<double>(size_t(g.rows) * kD);
+  c.take<int>(1);
+  return c.off + 256;
+}
+
+}  // namespace
+}  // namespace fathom
+
+using namespace fathom;
+
+extern "C" {
+
+int fathom_pack_workspace_bytes(const fathom_index_desc* desc, size_t* bytes) {
+  clear_error();
+  IndexGeom g;
+  FATHOM_TRY(index_geom(desc, &g));
+  if (!bytes) return set_error(FATHOM_EINVAL, "bytes is NULL");
+  *bytes = pack_ws(g);
+  return FATHOM_OK;
+}
+
+int fathom_pack(const fathom_index_desc* desc, const void* K, int k_dtype, uint32_t* planes, uint16_t* meta,
+                float* var, void* workspace, size_t ws_bytes, void* stream) {
+  clear_error();
+  IndexGeom g;
+  FATHOM_TRY(index_geom(desc, &g));
+  if (!valid_dtype(k_dtype)) return set_error(FATHOM_EINVAL, "k_dtype %d invalid", k_dtype);
+  const void *dK, *dP, *dM, *dV, *dW;
+  FATHOM_TRY(device_view(K, "K", &dK));
+  FATHOM_TRY(device_view(planes, "planes", &dP));
+  FATHOM_TRY(device_view(meta, "meta", &dM));
+  FATHOM_TRY(device_view(var, "var", &dV));
+  FATHOM_TRY(device_view(workspace, "workspace", &dW));
+  if (reinterpret_cast<uintptr_t>(dW) & 255) return set_error(FATHOM_EINVAL, "workspace must be 256-byte aligned");
+  if (ws_bytes < pack_ws(g)) return set_error(FATHOM_ENOMEM, "workspace %zu < %zu bytes", ws_bytes, pack_ws(g));
+  if ((reinterpret_cast<uintptr_t>(dP) & 15) != 0 || (reinterpret_cast<uintptr_t>(dM) & 3) != 0)
+    return set_error(FATHOM_EINVAL, "planes must be 16-byte aligned and meta 4-byte aligned");
+  cudaStream_t st = as_stream(stream);
+  Carve cv(const_cast<void*>(dW), ws_bytes);
+  double* part = cv.take<double>(size_t(g.rows) * kD * g.nblk);
+  double* mean = cv.take<double>(size_t(g.rows) * kD);
+  int* err = cv.take<int>(1);
+  FATHOM_TRY_CUDA(cudaMemsetAsync(err, 0, sizeof(int), st));
+  const int64_t blocks_all = g.nsb * (int64_t(g.S) / kBlock);
+  if (blocks_all > 0x7fffffff || g.rows > 65535) return set_error(FATHOM_EINVAL, "index too large for one launch");
+  dim3 gq(unsigned(blocks_all), unsigned(g.rows));
+  pack_quant_kernel<<<gq, kD, 0, st>>>(dK, k_dtype, g.n, g.nblk, g.nsb, g.log2S, (uint32_t*)dP, (__half2*)dM, part,
+                                       err);
+  FATHOM_TRY_CUDA(cudaGetLastError());
+  const int rc = g.rows * kD;
+  pack_mean_kernel<<<(rc + 127) / 128, 128, 0, st>>>(part, g.rows, g.nblk, g.n, mean);
+  FATHOM_TRY_CUDA(cudaGetLastError());
+  pack_m2_kernel<<<dim3(unsigned(g.nblk), unsigned(g.rows)), kD, 0, st>>>(dK, k_dtype, g.n, g.nblk, mean, part);
+  FATHOM_TRY_CUDA(cudaGetLastError());
+  pack_var_kernel<<<(rc + 127) / 128, 128, 0, st>>>(part, g.rows, g.nblk, g.n, (float*)dV);
+  FATHOM_TRY_CUDA(cudaGetLastError());
+  int herr = 0;
+  FATHOM_TRY_CUDA(cudaMemcpyAsync(&herr, err, sizeof(int), cudaMemcpyDeviceToHost, st));
+  FATHOM_TRY_CUDA(cudaStreamSynchronize(st));
+  if (herr & kErrRange) return set_error(FATHOM_EDATA, "K holds a non-finite value or one outside the fp16 range");
+  return FATHOM_OK;
+}
+
+}  // extern "C"

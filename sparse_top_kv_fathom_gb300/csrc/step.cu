@@ -1,0 +1,145 @@
+// fathom_decode_step and fathom_fixed136_decode_step: one decode step over a
+// set of independent rows (Rootconf proposal, summary: the index scan ranks
+// all n keys to pick the top k, then attention runs over the selected rows).
+// The steps are enqueued back to back on the caller's stream; scores, depths,
+// the top-k state and the attention partials live in the caller's workspace.
+// The scan also builds the first radix digit's histogram for the top-k, so
+// the scores are read only twice more (candidate pass, then the small final
+// select) before attention.
+#include "common.cuh"
+
+namespace fathom {
+namespace {
+
+struct StepWs {
+  uint8_t* bits;
+  float* qbar;
+  float* scores;
+  void* topk;
+  void* attn;
+  size_t end;
+};
+
+StepWs carve_step(void* base, int rows, int group, int64_t n, int64_t k) {
+  Carve cv(base, ~size_t(0));
+  StepWs w;
+  w.bits = cv.take<uint8_t>(size_t(rows) * kD);
+  w.qbar = cv.take<float>(size_t(rows) * kD);
+  w.scores = cv.take<float>(size_t(rows) * n);
+  w.topk = cv.take<char>(topk_ws_bytes(rows, n, k));
+  w.attn = cv.take<char>(attn_ws_bytes(rows, group, k));
+  w.end = cv.off;
+  return w;
+}
+
+}  // namespace
+}  // namespace fathom
+
+using namespace fathom;
+
+extern "C" {
+
+int fathom_decode_step_workspace_bytes(const fathom_step_desc* s, size_t* bytes) {
+  clear_error();
+  if (!s || !bytes) return set_error(FATHOM_EINVAL, "NULL argument");
+  IndexGeom g;
+  FATHOM_TRY(index_geom(&s->index, &g));
+  if (s->group < 1 || s->group > 8 || s->k < 1) return set_error(FATHOM_EINVAL, "group (1..8) or k out of range");
+  *bytes = carve_step(nullptr, g.rows, s->group, g.n, s->k).end + 256;
+  return FATHOM_OK;
+}
+
+int fathom_decode_step(const fathom_step_desc* s, void* workspace, size_t ws_bytes, void* stream) {
+  clear_error();
+  if (!s) return set_error(FATHOM_EINVAL, "step desc is NULL");
+  IndexGeom g;
+  FATHOM_TRY(index_geom(&s->index, &g));
+  if (g.rows > 65535) return set_error(FATHOM_EINVAL, "rows > 65535");
+  if (s->group < 1 || s->group > 8) return set_error(FATHOM_EINVAL, "group must be 1..8");
+  if (s->k < 1 || s->k > 0x7fffffff) return set_error(FATHOM_EINVAL, "k out of range");
+  if (!valid_dtype(s->q_dtype) || !valid_dtype(s->kv_dtype)) return set_error(FATHOM_EINVAL, "invalid dtype");
+  if (!s->budgets && (s->budget < 0 || s->budget > kD * kPlanes))
+    return set_error(FATHOM_EINVAL, "budget %d outside [0, 512]", s->budget);
+  const void *dP, *dM, *dVar, *dBud, *dq, *dK, *dV, *dI, *dO, *dB, *dSt, *dW;
+  FATHOM_TRY(device_view(s->planes, "planes", &dP));
+  FATHOM_TRY(device_view(s->meta, "meta", &dM));
+  FATHOM_TRY(device_view(s->var, "var", &dVar));
+  FATHOM_TRY(device_view(s->budgets, "budgets", &dBud, true));
+  FATHOM_TRY(device_view(s->q, "q", &dq));
+  FATHOM_TRY(device_view(s->K, "K", &dK));
+  FATHOM_TRY(device_view(s->V, "V", &dV));
+  FATHOM_TRY(device_view(s->idx, "idx", &dI));
+  FATHOM_TRY(device_view(s->out, "out", &dO, true));
+  FATHOM_TRY(device_view(s->out_bf16, "out_bf16", &dB, true));
+  FATHOM_TRY(device_view(s->status, "status", &dSt, true));
+  FATHOM_TRY(device_view(workspace, "workspace", &dW));
+  if (!dO && !dB) return set_error(FATHOM_EINVAL, "out and out_bf16 are both NULL");
+  StepWs w = carve_step(const_cast<void*>(dW), g.rows, s->group, g.n, s->k);
+  if (reinterpret_cast<uintptr_t>(dW) & 255) return set_error(FATHOM_EINVAL, "workspace must be 256-byte aligned");
+  if (ws_bytes < w.end + 256) return set_error(FATHOM_ENOMEM, "workspace %zu < %zu bytes", ws_bytes, w.end + 256);
+  const size_t al = s->kv_dtype == FATHOM_F32 ? 16 : 8;
+  if ((reinterpret_cast<uintptr_t>(dK) % al) || (reinterpret_cast<uintptr_t>(dV) % al) ||
+      (reinterpret_cast<uintptr_t>(dP) & 3) || (reinterpret_cast<uintptr_t>(dM) & 3))
+    return set_error(FATHOM_EINVAL, "misaligned planes, meta, K or V");
+  cudaStream_t st = as_stream(stream);
+  const bool use_hist = s->k < g.n;
+  uint32_t* hist = use_hist ? topk_hist_ptr(w.topk, g.rows, g.n, s->k) : nullptr;
+  if (hist) FATHOM_TRY_CUDA(cudaMemsetAsync(hist, 0, size_t(g.rows) * kHistBins * sizeof(uint32_t), st));
+  FATHOM_TRY_CUDA(launch_allocate(g.rows, s->group, dq, s->q_dtype, (const float*)dVar, (const uint16_t*)dBud,
+                                  s->budget, w.bits, w.qbar, (int32_t*)dSt, st));
+  FATHOM_TRY_CUDA(launch_scan(g, (const uint32_t*)dP, (const __half2*)dM, w.bits, w.qbar, w.scores, hist, st));
+  FATHOM_TRY_CUDA(launch_topk(g.rows, g.n, s->k, w.scores, (int32_t*)dI, nullptr, w.topk, use_hist, st));
+  FATHOM_TRY_CUDA(launch_attn(g.rows, s->group, g.n, s->k, dq, s->q_dtype, dK, dV, s->kv_dtype, (const int32_t*)dI,
+                              (float*)dO, (uint16_t*)dB, w.attn, st));
+  return FATHOM_OK;
+}
+
+int fathom_fixed136_step_workspace_bytes(const fathom_fixed136_step_desc* s, size_t* bytes) {
+  clear_error();
+  if (!s || !bytes) return set_error(FATHOM_EINVAL, "NULL argument");
+  if (s->rows < 1 || s->n < 1 || s->k < 1 || s->group < 1 || s->group > 8)
+    return set_error(FATHOM_EINVAL, "rows, n, k or group out of range");
+  *bytes = carve_step(nullptr, s->rows, s->group, s->n, s->k).end + 256;
+  return FATHOM_OK;
+}
+
+int fathom_fixed136_decode_step(const fathom_fixed136_step_desc* s, void* workspace, size_t ws_bytes, void* stream) {
+  clear_error();
+  if (!s) return set_error(FATHOM_EINVAL, "step desc is NULL");
+  if (s->rows < 1 || s->rows > 65535 || s->n < 1 || s->n > 0x7fffffff || s->k < 1 || s->k > 0x7fffffff ||
+      s->group < 1 || s->group > 8)
+    return set_error(FATHOM_EINVAL, "rows, n, k or group out of range");
+  if (!valid_dtype(s->q_dtype) || !valid_dtype(s->kv_dtype)) return set_error(FATHOM_EINVAL, "invalid dtype");
+  const void *dC, *dX, *dE, *dq, *dK, *dV, *dI, *dO, *dB, *dW;
+  FATHOM_TRY(device_view(s->chans, "chans", &dC));
+  FATHOM_TRY(device_view(s->codes, "codes", &dX));
+  FATHOM_TRY(device_view(s->exps, "exps", &dE));
+  FATHOM_TRY(device_view(s->q, "q", &dq));
+  FATHOM_TRY(device_view(s->K, "K", &dK));
+  FATHOM_TRY(device_view(s->V, "V", &dV));
+  FATHOM_TRY(device_view(s->idx, "idx", &dI));
+  FATHOM_TRY(device_view(s->out, "out", &dO, true));
+  FATHOM_TRY(device_view(s->out_bf16, "out_bf16", &dB, true));
+  FATHOM_TRY(device_view(workspace, "workspace", &dW));
+  if (!dO && !dB) return set_error(FATHOM_EINVAL, "out and out_bf16 are both NULL");
+  StepWs w = carve_step(const_cast<void*>(dW), s->rows, s->group, s->n, s->k);
+  if (reinterpret_cast<uintptr_t>(dW) & 255) return set_error(FATHOM_EINVAL, "workspace must be 256-byte aligned");
+  if (ws_bytes < w.end + 256) return set_error(FATHOM_ENOMEM, "workspace %zu < %zu bytes", ws_bytes, w.end + 256);
+  const size_t al = s->kv_dtype == FATHOM_F32 ? 16 : 8;
+  if ((reinterpret_cast<uintptr_t>(dK) % al) || (reinterpret_cast<uintptr_t>(dV) % al) ||
+      (reinterpret_cast<uintptr_t>(dX) & 15))
+    return set_error(FATHOM_EINVAL, "misaligned codes, K or V");
+  cudaStream_t st = as_stream(stream);
+  const bool use_hist = s->k < s->n;
+  uint32_t* hist = use_hist ? topk_hist_ptr(w.topk, s->rows, s->n, s->k) : nullptr;
+  if (hist) FATHOM_TRY_CUDA(cudaMemsetAsync(hist, 0, size_t(s->rows) * kHistBins * sizeof(uint32_t), st));
+  FATHOM_TRY_CUDA(launch_qbar(s->rows, s->group, dq, s->q_dtype, w.qbar, st));
+  FATHOM_TRY_CUDA(launch_fixed136_scan(s->rows, s->n, (const int32_t*)dC, (const uint8_t*)dX, (const uint8_t*)dE,
+                                       w.qbar, w.scores, hist, st));
+  FATHOM_TRY_CUDA(launch_topk(s->rows, s->n, s->k, w.scores, (int32_t*)dI, nullptr, w.topk, use_hist, st));
+  FATHOM_TRY_CUDA(launch_attn(s->rows, s->group, s->n, s->k, dq, s->q_dtype, dK, dV, s->kv_dtype, (const int32_t*)dI,
+                              (float*)dO, (uint16_t*)dB, w.attn, st));
+  return FATHOM_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,517 @@
+// fathom_topk: the k largest scores of each row, ties to the lower index,
+// written in ascending index order (Fathom article, "The first fix: stop
+// attending to everything": score every key and take the top k).
+//
+// Scores are mapped to order-preserving 32-bit keys (-0.0 as +0.0).  The
+// selection is an exact radix select:
+//   1. a 4096-bin histogram of each row's top 12 key bits (fused into the scan
+//      inside the decode step, or a separate pass here);
+//   2. per row, the bin b1 holding the k-th largest key;
+//   3. one pass over the scores: keys in bins above b1 are certainly selected
+//      (appended to a "sure" list of fewer than k entries), keys in b1 are
+//      candidates (appended to a bounded candidate list);
+//   4. per row, one CTA finishes the select on the candidates (two more 10-bit
+//      digits give the exact threshold key T), hands out the keys equal to T
+//      to the lowest indices (a radix select on the index), and sorts the k
+//      chosen indices.
+// If the candidate list overflows, or k is larger than the sort buffer, step 4
+// instead runs the same definition directly over the row's scores (3 digit
+// passes, an ordered count of the keys equal to T, then an ordered compaction);
+// both routes produce the identical result.
+#include "common.cuh"
+
+namespace fathom {
+namespace {
+
+constexpr int kFinThreads = 1024;
+constexpr int kSortMax = 8192;  // largest k sorted in shared memory
+constexpr int kPassThreads = 256;
+constexpr int kPassItems = 16;  // items per thread in the histogram / compaction passes
+
+struct RowState {
+  uint32_t b1;      // bin (top 12 key bits) holding the k-th largest key
+  int32_t above;    // keys in bins above b1
+  int32_t sure_cnt;
+  int32_t cand_cnt;
+  int32_t pad[4];
+};
+
+struct TopkWs {
+  uint32_t* hist;
+  RowState* state;
+  int32_t* sure;
+  uint32_t* cand_key;
+  int32_t* cand_idx;
+  int64_t cap;
+};
+
+int64_t cand_cap(int64_t n, int64_t k) {
+  int64_t c = 4 * k > 32768 ? 4 * k : 32768;
+  return c < n ? c : n;
+}
+
+TopkWs carve_topk(void* base, int rows, int64_t n, int64_t k) {
+  Carve cv(base, ~size_t(0));
+  TopkWs w;
+  w.cap = cand_cap(n, k);
+  w.hist = cv.take<uint32_t>(size_t(rows) * kHistBins);
+  w.state = cv.take<RowState>(size_t(rows));
+  w.sure = cv.take<int32_t>(size_t(rows) * k);
+  w.cand_key = cv.take<uint32_t>(size_t(rows) * w.cap);
+  w.cand_idx = cv.take<int32_t>(size_t(rows) * w.cap);
+  return w;
+}
+
+// ---------------------------------------------------------------- helpers ---
+// Exclusive prefix sum over the CTA (blockDim.x a multiple of 32, <= 1024).
+__device__ int block_exclusive_scan(int v, int* total) {
+  __shared__ int s_w[32];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  __syncthreads();
+  if (lane == 31) s_w[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int w = lane < nw ? s_w[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += y;
+    }
+    s_w[lane] = w;
+  }
+  __syncthreads();
+  const int base = warp ? s_w[warp - 1] : 0;
+  if (total) *total = s_w[nw - 1];
+  __syncthreads();
+  return base + x - v;
+}
+
+// Given a shared histogram h[nbins] (nbins == blockDim.x), find the bin where the
+// count taken from the top (from_top) or from the bottom reaches `need` (1 <= need
+// <= total).  Returns the bin; *before = count strictly beyond it on the taken side.
+__device__ void find_digit(const uint32_t* h, int need, bool from_top, int* s_out) {
+  const int nb = blockDim.x;
+  const int b = from_top ? nb - 1 - int(threadIdx.x) : int(threadIdx.x);
+  const int cnt = int(h[b]);
+  int tot;
+  const int before = block_exclusive_scan(cnt, &tot);
+  if (before < need && before + cnt >= need) {
+    s_out[0] = b;
+    s_out[1] = before;
+  }
+  __syncthreads();
+}
+
+__device__ __forceinline__ void warp_append(bool pred, int32_t* counter, int* slot) {
+  const unsigned m = __ballot_sync(0xffffffffu, pred);
+  const int lane = threadIdx.x & 31;
+  int base = 0;
+  if (m) {
+    const int leader = __ffs(m) - 1;
+    if (lane == leader) base = atomicAdd(counter, __popc(m));
+    base = __shfl_sync(0xffffffffu, base, leader);
+  }
+  *slot = base + __popc(m & ((1u << lane) - 1u));
+}
+
+// ----------------------------------------------------------------- kernels ---
+__global__ void topk_all_kernel(int64_t n, int64_t k, const float* __restrict__ scores, int32_t* __restrict__ idx,
+                                float* __restrict__ vals) {
+  const int r = blockIdx.y;
+  for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < k; i += int64_t(gridDim.x) * blockDim.x) {
+    idx[int64_t(r) * k + i] = i < n ? int32_t(i) : -1;
+    if (vals) vals[int64_t(r) * k + i] = i < n ? scores[int64_t(r) * n + i] : -INFINITY;
+  }
+}
+
+__global__ void __launch_bounds__(kPassThreads) topk_hist_kernel(int64_t n, const float* __restrict__ scores,
+                                                                 uint32_t* __restrict__ hist) {
+  __shared__ uint32_t h[kHistBins];
+  const int r = blockIdx.y;
+  for (int i = threadIdx.x; i < kHistBins; i += kPassThreads) h[i] = 0u;
+  __syncthreads();
+  const int64_t t0 = int64_t(blockIdx.x) * kPassThreads * kPassItems;
+  const float* s = scores + int64_t(r) * n;
+  for (int i = 0; i < kPassItems; ++i) {
+    const int64_t t = t0 + int64_t(i) * kPassThreads + threadIdx.x;
+    if (t < n) atomicAdd(&h[score_key(s[t]) >> (32 - kHistBits)], 1u);
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < kHistBins; i += kPassThreads)
+    if (h[i]) atomicAdd(hist + int64_t(r) * kHistBins + i, h[i]);
+}
+
+// One CTA (1024 threads) per row: locate the bin of the k-th largest key.
+__global__ void __launch_bounds__(kFinThreads) topk_bin_kernel(int64_t k, const uint32_t* __restrict__ hist,
+                                                               RowState* __restrict__ state) {
+  __shared__ uint32_t h[kFinThreads];
+  __shared__ int s_out[2];
+  const int r = blockIdx.x;
+  // fold the 4096 bins into 1024 groups of 4 (from the top), then refine inside the group
+  const uint32_t* hr = hist + int64_t(r) * kHistBins;
+  const int g = threadIdx.x;
+  h[g] = hr[4 * g] + hr[4 * g + 1] + hr[4 * g + 2] + hr[4 * g + 3];
+  __syncthreads();
+  find_digit(h, int(k), true, s_out);
+  if (threadIdx.x == 0) {
+    const int grp = s_out[0];
+    int before = s_out[1];
+    int b = 4 * grp + 3;
+    for (; b > 4 * grp; --b) {
+      const int c = int(hr[b]);
+      if (before + c >= int(k)) break;
+      before += c;
+    }
+    RowState st;
+    st.b1 = uint32_t(b);
+    st.above = before;
+    st.sure_cnt = 0;
+    st.cand_cnt = 0;
+    st.pad[0] = st.pad[1] = st.pad[2] = st.pad[3] = 0;
+    state[r] = st;
+  }
+}
+
+__global__ void __launch_bounds__(kPassThreads) topk_compact_kernel(int64_t n, int64_t k, int64_t cap,
+                                                                    const float* __restrict__ scores,
+                                                                    RowState* __restrict__ state,
+                                                                    int32_t* __restrict__ sure,
+                                                                    uint32_t* __restrict__ cand_key,
+                                                                    int32_t* __restrict__ cand_idx) {
+  const int r = blockIdx.y;
+  const uint32_t b1 = state[r].b1;
+  const int64_t t0 = int64_t(blockIdx.x) * kPassThreads * kPassItems;
+  const float* s = scores + int64_t(r) * n;
+  for (int i = 0; i < kPassItems; ++i) {
+    const int64_t t = t0 + int64_t(i) * kPassThreads + threadIdx.x;
+    uint32_t key = 0u;
+    if (t < n) key = score_key(s[t]);
+    const uint32_t bin = key >> (32 - kHistBits);
+    const bool is_sure = (t < n) && bin > b1;
+    const bool is_cand = (t < n) && bin == b1;
+    int slot;
+    warp_append(is_sure, &state[r].sure_cnt, &slot);
+    if (is_sure && slot < k) sure[int64_t(r) * k + slot] = int32_t(t);
+    warp_append(is_cand, &state[r].cand_cnt, &slot);
+    if (is_cand && slot < cap) {
+      cand_key[int64_t(r) * cap + slot] = key;
+      cand_idx[int64_t(r) * cap + slot] = int32_t(t);
+    }
+  }
+}
+
+// Bitonic sort (ascending) of s[0..m) in shared memory, m a power of two.
+__device__ void bitonic_sort(int32_t* s, int m) {
+  for (int size = 2; size <= m; size <<= 1) {
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      for (int i = threadIdx.x; i < (m >> 1); i += blockDim.x) {
+        const int lo = 2 * i - (i & (stride - 1));
+        const int hi = lo + stride;
+        const bool up = ((lo & size) == 0);
+        const int32_t a = s[lo], b = s[hi];
+        if ((a > b) == up) {
+          s[lo] = b;
+          s[hi] = a;
+        }
+      }
+      __syncthreads();
+    }
+  }
+}
+
+// Exact select directly over the row's n scores (one CTA): threshold key T, the
+// index cut among keys equal to T, then ordered output.
+__device__ void select_row_direct(int64_t n, int64_t k, const float* s, int32_t* out_idx, float* out_vals,
+                                  uint32_t* h, int* s_out) {
+  const int tid = threadIdx.x;
+  // --- threshold key by three digits: 12 bits (in 4 folds of 1024), 10, 10
+  uint32_t prefix = 0u, pmask = 0u;
+  int need = int(k);
+  const int shifts[3] = {20, 10, 0};
+  const int widths[3] = {12, 10, 10};
+  for (int p = 0; p < 3; ++p) {
+    const int sh = shifts[p], wd = widths[p];
+    // histogram over 1024 bins of the top (wd - 2) or wd bits
+    const int fold = wd - 10;  // bins folded (12-bit digit -> 1024 groups of 4)
+    for (int i = tid; i < kFinThreads; i += blockDim.x) h[i] = 0u;
+    __syncthreads();
+    for (int64_t t = tid; t < n; t += blockDim.x) {
+      const uint32_t key = score_key(s[t]);
+      if ((key & pmask) == prefix) atomicAdd(&h[((key >> sh) & ((1u << wd) - 1u)) >> fold], 1u);
+    }
+    __syncthreads();
+    find_digit(h, need, true, s_out);
+    int grp = s_out[0], before = s_out[1];
+    uint32_t digit = uint32_t(grp);
+    if (fold) {
+      // refine inside the group of 4: recount those 4 bins
+      __syncthreads();
+      if (tid < 4) h[tid] = 0u;
+      __syncthreads();
+      for (int64_t t = tid; t < n; t += blockDim.x) {
+        const uint32_t key = score_key(s[t]);
+        if ((key & pmask) == prefix) {
+          const uint32_t d = (key >> sh) & ((1u << wd) - 1u);
+          if ((d >> fold) == uint32_t(grp)) atomicAdd(&h[d & 3u], 1u);
+        }
+      }
+      __syncthreads();
+      int b = 3;
+      for (; b > 0; --b) {
+        if (before + int(h[b]) >= need) break;
+        before += int(h[b]);
+      }
+      digit = (uint32_t(grp) << fold) | uint32_t(b);
+      __syncthreads();
+    }
+    need -= before;
+    prefix |= digit << sh;
+    pmask |= ((1u << wd) - 1u) << sh;
+    __syncthreads();
+  }
+  const uint32_t T = prefix;  // keys > T all taken; `need` keys equal to T taken, lowest indices first
+  // --- index cut: the need-th key equal to T in index order
+  const int64_t chunk = (n + blockDim.x - 1) / blockDim.x;
+  const int64_t c0 = int64_t(tid) * chunk, c1 = (c0 + chunk < n) ? c0 + chunk : n;
+  int eq = 0, gt = 0;
+  for (int64_t t = c0; t < c1; ++t) {
+    const uint32_t key = score_key(s[t]);
+    eq += key == T;
+    gt += key > T;
+  }
+  int tot;
+  const int eq_before = block_exclusive_scan(eq, &tot);
+  __shared__ int64_t s_cut;
+  if (eq_before < need && eq_before + eq >= need) {
+    int c = eq_before;
+    for (int64_t t = c0; t < c1; ++t) {
+      if (score_key(s[t]) == T && ++c == need) {
+        s_cut = t;
+        break;
+      }
+    }
+  }
+  __syncthreads();
+  const int64_t cut = s_cut;
+  // --- ordered compaction
+  int sel = 0;
+  for (int64_t t = c0; t < c1; ++t) {
+    const uint32_t key = score_key(s[t]);
+    sel += (key > T) || (key == T && t <= cut);
+  }
+  int pos = block_exclusive_scan(sel, &tot);
+  for (int64_t t = c0; t < c1; ++t) {
+    const uint32_t key = score_key(s[t]);
+    if ((key > T) || (key == T && t <= cut)) {
+      out_idx[pos] = int32_t(t);
+      if (out_vals) out_vals[pos] = s[t];
+      ++pos;
+    }
+  }
+  (void)gt;
+}
+
+__global__ void __launch_bounds__(kFinThreads) topk_final_kernel(int64_t n, int64_t k, int64_t cap,
+                                                                 const float* __restrict__ scores,
+                                                                 const RowState* __restrict__ state,
+                                                                 const int32_t* __restrict__ sure,
+                                                                 const uint32_t* __restrict__ cand_key,
+                                                                 const int32_t* __restrict__ cand_idx,
+                                                                 int32_t* __restrict__ idx, float* __restrict__ vals) {
+  extern __shared__ int32_t s_sel[];  // kSortMax entries
+  __shared__ uint32_t h[kFinThreads];
+  __shared__ int s_out[2];
+  __shared__ int s_fill;
+  const int r = blockIdx.x;
+  const int tid = threadIdx.x;
+  const RowState st = state[r];
+  const float* s = scores + int64_t(r) * n;
+  int32_t* oi = idx + int64_t(r) * k;
+  float* ov = vals ? vals + int64_t(r) * k : nullptr;
+  const int m = st.cand_cnt;
+  if (m > cap || k > kSortMax) {
+    select_row_direct(n, k, s, oi, ov, h, s_out);
+    return;
+  }
+  const uint32_t* ck = cand_key + int64_t(r) * cap;
+  const int32_t* ci = cand_idx + int64_t(r) * cap;
+  int need = int(k) - st.above;  // >= 1
+  // --- digits 2 and 3 (bits 19..10 and 9..0) among the candidates
+  uint32_t prefix = st.b1 << 20, pmask = 0xFFF00000u;
+  for (int sh = 10; sh >= 0; sh -= 10) {
+    h[tid] = 0u;
+    __syncthreads();
+    for (int i = tid; i < m; i += kFinThreads) {
+      const uint32_t key = ck[i];
+      if ((key & pmask) == prefix) atomicAdd(&h[(key >> sh) & 0x3FFu], 1u);
+    }
+    __syncthreads();
+    find_digit(h, need, true, s_out);
+    need -= s_out[1];
+    prefix |= uint32_t(s_out[0]) << sh;
+    pmask |= 0x3FFu << sh;
+    __syncthreads();
+  }
+  const uint32_t T = prefix;
+  // --- among candidates equal to T, the `need` lowest indices: radix select on the index
+  int32_t cut = 0x7fffffff;
+  {
+    uint32_t ip = 0u, im = 0u;
+    int ineed = need;
+    int eq_total = 0;
+    for (int i = tid; i < m; i += kFinThreads) eq_total += ck[i] == T;
+    int tot;
+    block_exclusive_scan(eq_total, &tot);
+    if (tot > need) {
+      const int ishift[3] = {21, 10, 0};
+      const int iwidth[3] = {10, 11, 10};
+      for (int p = 0; p < 3; ++p) {
+        const int sh = ishift[p], wd = iwidth[p];
+        h[tid] = 0u;
+        __syncthreads();
+        for (int i = tid; i < m; i += kFinThreads) {
+          const uint32_t ix = uint32_t(ci[i]);
+          if (ck[i] == T && (ix & im) == ip) {
+            const uint32_t d = (ix >> sh) & ((1u << wd) - 1u);
+            atomicAdd(&h[d >> (wd - 10)], 1u);
+          }
+        }
+        __syncthreads();
+        find_digit(h, ineed, false, s_out);
+        int grp = s_out[0], before = s_out[1];
+        uint32_t digit = uint32_t(grp);
+        if (wd > 10) {  // refine the pair of 11-bit digits folded into one bin
+          __syncthreads();
+          if (tid < 2) h[tid] = 0u;
+          __syncthreads();
+          for (int i = tid; i < m; i += kFinThreads) {
+            const uint32_t ix = uint32_t(ci[i]);
+            if (ck[i] == T && (ix & im) == ip) {
+              const uint32_t d = (ix >> sh) & ((1u << wd) - 1u);
+              if ((d >> 1) == uint32_t(grp)) atomicAdd(&h[d & 1u], 1u);
+            }
+          }
+          __syncthreads();
+          int b = 0;
+          if (before + int(h[0]) < ineed) {
+            before += int(h[0]);
+            b = 1;
+          }
+          digit = (uint32_t(grp) << 1) | uint32_t(b);
+          __syncthreads();
+        }
+        ineed -= before;
+        ip |= digit << sh;
+        im |= ((1u << wd) - 1u) << sh;
+        __syncthreads();
+      }
+      cut = int32_t(ip);
+    }
+  }
+  // --- gather the k chosen indices and sort them
+  int pow2 = 1;
+  while (pow2 < k) pow2 <<= 1;
+  for (int i = tid; i < pow2; i += kFinThreads) s_sel[i] = 0x7fffffff;
+  if (tid == 0) s_fill = 0;
+  __syncthreads();
+  for (int i = tid; i < st.above; i += kFinThreads) s_sel[i] = sure[int64_t(r) * k + i];
+  if (tid == 0) s_fill = st.above;
+  __syncthreads();
+  for (int i = tid; i < m; i += kFinThreads) {
+    const uint32_t key = ck[i];
+    if (key > T || (key == T && ci[i] <= cut)) {
+      const int p = atomicAdd(&s_fill, 1);
+      s_sel[p] = ci[i];
+    }
+  }
+  __syncthreads();
+  bitonic_sort(s_sel, pow2);
+  for (int i = tid; i < k; i += kFinThreads) {
+    const int32_t t = s_sel[i];
+    oi[i] = t;
+    if (ov) ov[i] = s[t];
+  }
+}
+
+}  // namespace
+
+size_t topk_ws_bytes(int rows, int64_t n, int64_t k) {
+  TopkWs w = carve_topk(nullptr, rows, n, k);
+  return reinterpret_cast<size_t>(w.cand_idx) + size_t(rows) * w.cap * sizeof(int32_t) + 256;
+}
+
+uint32_t* topk_hist_ptr(void* ws, int rows, int64_t n, int64_t k) { return carve_topk(ws, rows, n, k).hist; }
+
+cudaError_t launch_topk(int rows, int64_t n, int64_t k, const float* scores, int32_t* idx, float* vals, void* ws,
+                        bool hist_ready, cudaStream_t st) {
+  if (k >= n) {
+    dim3 grid(unsigned((k + 255) / 256 < 1024 ? (k + 255) / 256 : 1024), unsigned(rows));
+    topk_all_kernel<<<grid, 256, 0, st>>>(n, k, scores, idx, vals);
+    return cudaGetLastError();
+  }
+  TopkWs w = carve_topk(ws, rows, n, k);
+  const int64_t tiles = (n + kPassThreads * kPassItems - 1) / (kPassThreads * kPassItems);
+  const dim3 pgrid{unsigned(tiles), unsigned(rows), 1u};
+  cudaError_t e;
+  if (!hist_ready) {
+    e = cudaMemsetAsync(w.hist, 0, size_t(rows) * kHistBins * sizeof(uint32_t), st);
+    if (e != cudaSuccess) return e;
+    topk_hist_kernel<<<pgrid, kPassThreads, 0, st>>>(n, scores, w.hist);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  topk_bin_kernel<<<rows, kFinThreads, 0, st>>>(k, w.hist, w.state);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  topk_compact_kernel<<<pgrid, kPassThreads, 0, st>>>(n, k, w.cap, scores, w.state, w.sure, w.cand_key, w.cand_idx);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  const size_t smem = kSortMax * sizeof(int32_t);
+  static bool attr_set = false;
+  if (!attr_set) {
+    e = cudaFuncSetAttribute(topk_final_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  topk_final_kernel<<<rows, kFinThreads, smem, st>>>(n, k, w.cap, scores, w.state, w.sure, w.cand_key, w.cand_idx,
+                                                     idx, vals);
+  return cudaGetLastError();
+}
+
+}  // namespace fathom
+
+using namespace fathom;
+
+extern "C" {
+
+int fathom_topk_workspace_bytes(int rows, int64_t n, int64_t k, size_t* bytes) {
+  clear_error();
+  if (rows < 1 || n < 1 || k < 1 || n > 0x7fffffff) return set_error(FATHOM_EINVAL, "rows, n, k out of range");
+  if (!bytes) return set_error(FATHOM_EINVAL, "bytes is NULL");
+  *bytes = topk_ws_bytes(rows, n, k);
+  return FATHOM_OK;
+}
+
+int fathom_topk(int rows, int64_t n, int64_t k, const float* scores, int32_t* idx, float* vals, void* workspace,
+                size_t ws_bytes, void* stream) {
+  clear_error();
+  if (rows < 1 || rows > 65535 || n < 1 || k < 1 || n > 0x7fffffff || k > 0x7fffffff)
+    return set_error(FATHOM_EINVAL, "rows, n, k out of range");
+  const void *dS, *dI, *dV, *dW;
+  FATHOM_TRY(device_view(scores, "scores", &dS));
+  FATHOM_TRY(device_view(idx, "idx", &dI));
+  FATHOM_TRY(device_view(vals, "vals", &dV, true));
+  const bool need_ws = k < n;
+  FATHOM_TRY(device_view(workspace, "workspace", &dW, !need_ws));
+  if (reinterpret_cast<uintptr_t>(dW) & 255) return set_error(FATHOM_EINVAL, "workspace must be 256-byte aligned");
+  if (need_ws && ws_bytes < topk_ws_bytes(rows, n, k))
+    return set_error(FATHOM_ENOMEM, "workspace %zu < %zu bytes", ws_bytes, topk_ws_bytes(rows, n, k));
+  FATHOM_TRY_CUDA(launch_topk(rows, n, k, (const float*)dS, (int32_t*)dI, (float*)dV, const_cast<void*>(dW), false,
+                              as_stream(stream)));
+  return FATHOM_OK;
+}
+
+}  // extern "C"

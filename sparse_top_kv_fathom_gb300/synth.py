@@ -109,11 +109,11 @@ def _rope(x: torch.Tensor, pos0: int, base: float):
     """Rotate channel pairs (i, i+64) by angle pos * base^(-2i/128) (fp64 angles)."""
     n = x.shape[0]
     half = D // 2
-    inv = base ** (-torch.arange(half, dtype=torch.float64) * 2.0 / D)
-    pos = torch.arange(pos0, pos0 + n, dtype=torch.float64)
+    inv = (base ** (-torch.arange(half, dtype=torch.float64) * 2.0 / D)).to(x.device)
+    pos = torch.arange(pos0, pos0 + n, dtype=torch.float64, device=x.device)
     ang = pos[:, None] * inv[None, :]
-    cos = torch.cos(ang).to(device=x.device, dtype=torch.float32)
-    sin = torch.sin(ang).to(device=x.device, dtype=torch.float32)
+    cos = torch.cos(ang).to(torch.float32)
+    sin = torch.sin(ang).to(torch.float32)
     a, b = x[:, :half], x[:, half:]
     return torch.cat([a * cos - b * sin, a * sin + b * cos], dim=1)
 

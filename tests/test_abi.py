@@ -1,0 +1,108 @@
+"""The C-ABI library builds, loads and exports every declared entry point;
+host-only calls (size queries, argument validation) behave as documented.
+No GPU: nothing here launches a kernel."""
+import ctypes
+import json
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+INCLUDE = os.path.join(ROOT, "include")
+
+
+@pytest.fixture(scope="module")
+def F():
+    from sparse_top_kv_fathom_gb300 import build
+    build.build()
+    import sparse_top_kv_fathom_gb300 as F
+    F.load()
+    return F
+
+
+def declared_functions():
+    names = []
+    for h in sorted(os.listdir(INCLUDE)):
+        if not h.endswith(".h"):
+            continue
+        text = open(os.path.join(INCLUDE, h)).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        names += re.findall(r"^\s*(?:const\s+)?\w[\w\s\*]*?\b(fathom_\w+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_every_declared_symbol_is_exported(F):
+    from sparse_top_kv_fathom_gb300 import _native
+    names = declared_functions()
+    assert len(names) >= 18, names
+    lib = ctypes.CDLL(_native.LIB_PATH)
+    for name in names:
+        assert hasattr(lib, name), name
+        assert name in _native.SIGNATURES, "binding lacks " + name
+
+
+def test_index_sizes_match_the_pages(F):
+    g = json.load(open(os.path.join(ROOT, "tests", "golden", "sizes.json")))
+    # 68 bytes per token per KV head for the bit-plane index (codes + fp16 scale/offset)
+    for n in [128, 4096, 1 << 20]:
+        pb, mb = F.index_bytes(n, 1, 4096 if n >= 4096 else 128)
+        assert (pb + mb) / n == g["fathom_index_bytes_per_token_per_kv_head"]
+    # ... 4x the 17-byte (136-bit) fixed index
+    assert g["fathom_index_bytes_per_token_per_kv_head"] == g["fathom_vs_double_sparsity_label_cache"] * 136 // 8
+    q = g["qwen3_8b"]
+    kv = q["layers"] * q["kv_heads"] * q["head_dim"] * 2 * q["bits"] // 8
+    assert abs(kv - g["kv_bytes_per_token_about"]) / g["kv_bytes_per_token_about"] < 0.03
+    assert abs(kv * 32000 / 1e9 - g["cache_at_32000_tokens_GB_about"]) < 0.1
+    assert abs(kv * 1e6 / 1e9 - g["cache_at_1000000_tokens_GB_about"]) / 150 < 0.03
+    pairs = q["layers"] * q["kv_heads"]
+    assert pairs == g["layer_head_pairs"]
+    fixed = g["fixed_index_bits_per_token"] / 8 * pairs
+    assert abs(fixed * 32768 / 1e6 - g["fixed_index_MB_per_step_at_32000_about"]) < 2
+    assert abs(fixed * (1 << 20) / 1e9 - g["fixed_index_GB_per_step_at_1000000_about"]) < 0.1
+
+
+def test_invalid_arguments_are_rejected_on_the_host(F):
+    from sparse_top_kv_fathom_gb300 import _native as N
+    L = F.load()
+    pb, mb = ctypes.c_size_t(), ctypes.c_size_t()
+    for bad in [N.IndexDesc(0, 1, 128, 128, 4096), N.IndexDesc(10, 1, 64, 128, 4096),
+                N.IndexDesc(10, 1, 128, 64, 4096), N.IndexDesc(10, 1, 128, 128, 3000),
+                N.IndexDesc(10, 0, 128, 128, 4096), N.IndexDesc(10, 1, 128, 128, 64)]:
+        assert L.fathom_index_bytes(ctypes.byref(bad), ctypes.byref(pb), ctypes.byref(mb)) == 1
+        assert L.fathom_last_error()
+    ok = N.IndexDesc(10, 1, 128, 128, 4096)
+    assert L.fathom_index_bytes(ctypes.byref(ok), ctypes.byref(pb), ctypes.byref(mb)) == 0
+    assert L.fathom_index_bytes(ctypes.byref(ok), None, ctypes.byref(mb)) == 1
+    # validation that fails before any device pointer is inspected
+    assert L.fathom_scan(ctypes.byref(N.IndexDesc(10, 1, 64, 128, 4096)), None, None, None, None, None, None) == 1
+    assert L.fathom_allocate(1, 4, None, 2, None, None, 513, None, None, None, None) == 1
+    assert L.fathom_allocate(1, 0, None, 2, None, None, 92, None, None, None, None) == 1
+    assert L.fathom_allocate(1, 4, None, 9, None, None, 92, None, None, None, None) == 1
+    assert L.fathom_topk(1, 10, 0, None, None, None, None, 0, None) == 1
+    assert L.fathom_sparse_attn(1, 9, 10, 1, None, 2, None, None, 2, None, None, None, None, 0, None) == 1
+    assert L.fathom_probe_stream_read(None, 17, 1, 256, None, None) == 1
+    b = ctypes.c_size_t()
+    assert L.fathom_topk_workspace_bytes(8, 1 << 20, 2048, ctypes.byref(b)) == 0 and b.value > 0
+    assert L.fathom_sparse_attn_workspace_bytes(8, 4, 2048, ctypes.byref(b)) == 0 and b.value > 0
+    sd = N.StepDesc()
+    sd.index = N.IndexDesc(1 << 20, 8, 128, 128, 4096)
+    sd.group, sd.k, sd.budget = 4, 2048, 92
+    assert L.fathom_decode_step_workspace_bytes(ctypes.byref(sd), ctypes.byref(b)) == 0
+    assert b.value >= 8 * (1 << 20) * 4  # holds the scores
+    sd.group = 9
+    assert L.fathom_decode_step_workspace_bytes(ctypes.byref(sd), ctypes.byref(b)) == 1
+
+
+def test_no_oracle_in_product_path():
+    """The product package never imports the oracle; the oracle never imports the product."""
+    pkg = os.path.join(ROOT, "sparse_top_kv_fathom_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert "import oracle" not in text and "from oracle" not in text and "fathom_oracle" not in text, f
+    for f in os.listdir(os.path.join(ROOT, "oracle")):
+        if f.endswith((".py", ".c")):
+            text = open(os.path.join(ROOT, "oracle", f)).read()
+            assert "sparse_top_kv_fathom_gb300" not in text and "fathom.h" not in text, f

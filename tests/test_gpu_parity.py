@@ -1,0 +1,212 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle.
+
+Bars: packing, allocations and top-k index sets bit-exact; scores within
+1e-5 of the per-key L1 norm sum_c |qbar_c x_c| (fp32 accumulation vs the fp64
+oracle); attention within 2e-3 absolute on the fp32 output, the bf16 output
+within one bf16 ulp of the fp32 output rounded to nearest even.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from sparse_top_kv_fathom_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+SCORE_RTOL = 1e-5
+ATTN_ATOL = 2e-3
+
+
+def small(name, **kw):
+    return synth.scaled(synth.WORKLOADS[name], **kw)
+
+
+def gen(w, rows=None, device="cpu"):
+    rows = w.rows if rows is None else rows
+    K = torch.stack([synth.keys(w, r, device) for r in range(rows)])
+    V = torch.stack([synth.values(w, r, device) for r in range(rows)])
+    q = torch.cat([synth.queries(w, l, device) for l in range(max(1, rows // w.kv_heads))])[: rows * w.group]
+    return K, V, q
+
+
+def f32(t):
+    return t.detach().float().cpu().numpy()
+
+
+def check_scores(gpu, ref, l1):
+    err = np.abs(gpu.astype(np.float64) - ref)
+    bad = err > SCORE_RTOL * l1
+    assert not bad.any(), "max rel err %g" % (err / np.maximum(l1, 1e-300)).max()
+
+
+def check_attn(out, outb, ref):
+    assert np.abs(out - ref).max() <= ATTN_ATOL, np.abs(out - ref).max()
+    rne = torch.from_numpy(out).to(torch.bfloat16).float().numpy()
+    b = outb.float().cpu().numpy()
+    ulp = np.abs(rne) * 2.0 ** -7 + 1e-38
+    assert (np.abs(b - rne) <= ulp).all()
+
+
+CASES = [
+    ("tiny", dict(), 1024),
+    ("tiny", dict(n=10000), 4096),
+    ("qwen_layer", dict(n=9000), 1024),
+    ("qwen_layer", dict(n=5000, k_dtype=torch.float16, kv_dtype=torch.float16), 128),
+    ("sessions", dict(n=4500, layers=2), 2048),
+    ("decode36", dict(n=3000, layers=2), 32768),
+]
+
+
+@pytest.fixture(scope="module", params=range(len(CASES)), ids=["%s-%s-S%d" % (c[0], c[1].get("n", "full"), c[2])
+                                                               for c in CASES])
+def case(request, gpu_lib):
+    name, kw, S = CASES[request.param]
+    w = small(name, **kw)
+    K, V, q = gen(w)
+    F = gpu_lib
+    Kd, Vd, qd = K.cuda(), V.cuda(), q.cuda()
+    index = F.pack(Kd, S)
+    torch.cuda.synchronize()
+    planes, meta, var = oracle.pack(f32(K), S)
+    return dict(w=w, S=S, K=K, V=V, q=q, Kd=Kd, Vd=Vd, qd=qd, index=index, planes=planes, meta=meta, var=var)
+
+
+def test_pack_bit_exact(case):
+    ix = case["index"]
+    assert np.array_equal(ix.planes.cpu().numpy().view(np.uint32), case["planes"])
+    assert np.array_equal(ix.meta.cpu().numpy().view(np.uint16), case["meta"])
+    assert np.array_equal(ix.var.cpu().numpy().view(np.uint32), case["var"].view(np.uint32))
+
+
+@pytest.mark.parametrize("budget", [0, 1, 48, 68, 92, 136, 256, 511, 512, "rows"])
+def test_allocate_bit_exact(case, gpu_lib, budget):
+    F, w = gpu_lib, case["w"]
+    rows = w.rows
+    if budget == "rows":
+        b = np.array([[0, 1, 68, 92, 136, 256, 511, 512][r % 8] for r in range(rows)], np.int32)
+        bt = torch.from_numpy(b.astype(np.int16)).cuda()
+    else:
+        b, bt = budget, budget
+    bits, qbar = F.allocate(case["qd"], case["index"].var, bt, w.group)
+    ob, oq = oracle.allocate(f32(case["q"]), case["var"], b, w.group)
+    assert np.array_equal(bits.cpu().numpy(), ob)
+    assert np.array_equal(qbar.cpu().numpy().view(np.uint32), oq.view(np.uint32))
+
+
+@pytest.mark.parametrize("budget", [0, 1, 68, 92, 136, 512])
+def test_scan_within_tolerance(case, gpu_lib, budget):
+    F, w = gpu_lib, case["w"]
+    bits, qbar = F.allocate(case["qd"], case["index"].var, budget, w.group)
+    s = F.scan(case["index"], bits, qbar)
+    ref, l1 = oracle.scan(case["planes"], case["meta"], bits.cpu().numpy(), qbar.cpu().numpy(), w.n, case["S"])
+    check_scores(s.cpu().numpy(), ref, l1)
+    if budget == 0:
+        assert (s.cpu().numpy() == 0).all()
+
+
+def test_host_resident_index_gives_identical_scores(case, gpu_lib):
+    F, w = gpu_lib, case["w"]
+    bits, qbar = F.allocate(case["qd"], case["index"].var, 92, w.group)
+    s_dev = F.scan(case["index"], bits, qbar)
+    s_host = F.scan(case["index"].to_host(), bits, qbar)
+    assert torch.equal(s_dev, s_host)
+
+
+def test_decode_step_parity(case, gpu_lib):
+    F, w = gpu_lib, case["w"]
+    B, k = w.budgets[len(w.budgets) // 2], min(w.k, w.n)
+    idx, out, outb = F.decode_step(case["index"], case["qd"], case["Kd"], case["Vd"], k, w.group, B)
+    # components: the step's winners are the exact top-k of the scan's own fp32 scores
+    bits, qbar = F.allocate(case["qd"], case["index"].var, B, w.group)
+    s = F.scan(case["index"], bits, qbar)
+    assert np.array_equal(idx.cpu().numpy(), oracle.topk_f32(s.cpu().numpy(), k))
+    # against the oracle's own fp64 step: winners differ only inside the score tolerance band
+    oi, oo = oracle.decode_step(case["planes"], case["meta"], case["var"], f32(case["q"]), B, f32(case["K"]),
+                                f32(case["V"]), k, w.group, case["S"])
+    ref, l1 = oracle.scan(case["planes"], case["meta"], bits.cpu().numpy(), qbar.cpu().numpy(), w.n, case["S"])
+    gi = idx.cpu().numpy()
+    for r in range(w.rows):
+        kth = np.sort(ref[r])[::-1][k - 1]
+        tol = SCORE_RTOL * l1[r].max() * 2
+        only_gpu = np.setdiff1d(gi[r], oi[r])
+        only_ref = np.setdiff1d(oi[r], gi[r])
+        assert (np.abs(ref[r][only_gpu] - kth) <= tol).all()
+        assert (np.abs(ref[r][only_ref] - kth) <= tol).all()
+    # attention on the GPU's winners
+    oatt = oracle.sparse_attn(f32(case["q"]), f32(case["K"]), f32(case["V"]), gi, w.group)
+    check_attn(out.cpu().numpy(), outb, oatt)
+
+
+def test_decode_step_host_resident_kv_and_index(case, gpu_lib):
+    F, w = gpu_lib, case["w"]
+    B, k = 92, min(w.k, w.n)
+    a = F.decode_step(case["index"], case["qd"], case["Kd"], case["Vd"], k, w.group, B)
+    Kh, Vh = case["Kd"].cpu().pin_memory(), case["Vd"].cpu().pin_memory()
+    b = F.decode_step(case["index"].to_host(), case["qd"], Kh, Vh, k, w.group, B)
+    assert torch.equal(a[0], b[0])
+    assert torch.equal(a[1], b[1])
+
+
+def test_fixed136_parity(case, gpu_lib):
+    F, w = gpu_lib, case["w"]
+    fx = F.fixed136_pack(case["Kd"], case["index"].var)
+    chans, codes, exps = oracle.fixed136_pack(f32(case["K"]), case["var"])
+    assert np.array_equal(fx.chans.cpu().numpy(), chans)
+    assert np.array_equal(fx.codes.cpu().numpy(), codes)
+    assert np.array_equal(fx.exps.cpu().numpy(), exps)
+    _, qbar = F.allocate(case["qd"], case["index"].var, 92, w.group)
+    s = F.fixed136_scan(fx, qbar)
+    ref, l1 = oracle.fixed136_scan(chans, codes, exps, qbar.cpu().numpy())
+    check_scores(s.cpu().numpy(), ref, l1)
+    k = min(w.k, w.n)
+    st = F.Fixed136Step(fx, case["Kd"], case["Vd"], case["qd"], k, w.group)
+    idx, out, outb = st()
+    oi = oracle.topk_f32(s.cpu().numpy(), k)
+    assert np.array_equal(idx.cpu().numpy(), oi)
+    check_attn(out.cpu().numpy(), outb, oracle.sparse_attn(f32(case["q"]), f32(case["K"]), f32(case["V"]), oi,
+                                                            w.group))
+
+
+# ------------------------------------------------------------------ top-k ---
+def _score_sets(rng, rows, n):
+    yield "normal", rng.standard_normal((rows, n)).astype(np.float32)
+    yield "ties8", rng.choice(np.linspace(-2, 2, 8).astype(np.float32), (rows, n))
+    yield "allequal", np.full((rows, n), 1.5, np.float32)
+    yield "zeros_signed", rng.choice(np.array([0.0, -0.0], np.float32), (rows, n))
+    yield "narrow", (1000.0 + rng.standard_normal((rows, n)) * 1e-3).astype(np.float32)  # one top bin
+    yield "wide", (rng.standard_normal((rows, n)) * np.exp(rng.normal(0, 20, (rows, n)))).astype(np.float32)
+
+
+@pytest.mark.parametrize("n", [1, 33, 4096, 70001])
+def test_topk_bit_exact(gpu_lib, n):
+    F = gpu_lib
+    rng = np.random.default_rng(n)
+    rows = 3
+    for name, s in _score_sets(rng, rows, n):
+        sd = torch.from_numpy(s).cuda()
+        for k in sorted({1, 7, 64, max(1, n // 3), max(1, n - 1), n, n + 5, 9000}):
+            idx, vals = F.topk(sd, k, with_values=True)
+            want = oracle.topk_f32(s, k)
+            assert np.array_equal(idx.cpu().numpy(), want), (name, n, k)
+            v = vals.cpu().numpy()
+            for r in range(rows):
+                sel = want[r] >= 0
+                assert np.array_equal(v[r][sel].view(np.uint32), s[r][want[r][sel]].view(np.uint32))
+
+
+# ------------------------------------------------------------ attention ---
+@pytest.mark.parametrize("dtype", [torch.float32, torch.float16, torch.bfloat16])
+@pytest.mark.parametrize("group", [1, 3, 4, 8])
+def test_sparse_attention_parity(gpu_lib, dtype, group):
+    F = gpu_lib
+    rng = np.random.default_rng(group)
+    rows, n, k = 3, 3000, 700
+    K = torch.from_numpy(rng.standard_normal((rows, n, 128)).astype(np.float32)).to(dtype)
+    V = torch.from_numpy(rng.standard_normal((rows, n, 128)).astype(np.float32)).to(dtype)
+    q = torch.from_numpy(rng.standard_normal((rows * group, 128)).astype(np.float32) * 2).to(dtype)
+    idx = np.sort(np.stack([rng.choice(n, k, replace=False) for _ in range(rows)]), 1).astype(np.int32)
+    idx[1, -5:] = -1  # padding entries are skipped
+    out, outb = F.sparse_attn(q.cuda(), K.cuda(), V.cuda(), torch.from_numpy(idx).cuda(), group)
+    ref = oracle.sparse_attn(f32(q), f32(K), f32(V), idx, group)
+    check_attn(out.cpu().numpy(), outb, ref)
