@@ -133,20 +133,21 @@ class Model:
         host = residency in ("host", "both")
         devr = residency in ("device", "both")
         t0 = time.time()
-        pin = dict(pin_memory=True)
         self.h = {}
         self.d = {}
         kvrows = KL * H
-        for store, kw in ((self.h, pin), (self.d, dict(device=dev))):
+        for store, empty in ((self.h, F.host_empty),
+                             (self.d, lambda shape, dtype: torch.empty(shape, dtype=dtype, device=dev))):
             if (store is self.h and not host) or (store is self.d and not devr):
                 continue
-            store["planes"] = torch.empty(ps, dtype=torch.int32, **kw)
-            store["meta"] = torch.empty(ms, dtype=torch.float16, **kw)
-            store["K"] = torch.empty((kvrows, n, D), dtype=w.kv_dtype, **kw)
-            store["V"] = torch.empty((kvrows, n, D), dtype=w.kv_dtype, **kw)
+            store["planes"] = empty(ps, torch.int32)
+            store["meta"] = empty(ms, torch.float16)
+            # K and V of a token side by side: one 512-byte row per winner
+            store["KV"] = empty((kvrows, n, 2, D), w.kv_dtype)
+            store["K"], store["V"] = store["KV"][:, :, 0, :], store["KV"][:, :, 1, :]
             if comparator:
-                store["codes"] = torch.empty((rows, n, 16), dtype=torch.uint8, **kw)
-                store["exps"] = torch.empty((rows, n), dtype=torch.uint8, **kw)
+                store["codes"] = empty((rows, n, 16), torch.uint8)
+                store["exps"] = empty((rows, n), torch.uint8)
         log("allocated buffers in %.1f s" % (time.time() - t0))
         self.var = torch.empty((rows, D), dtype=torch.float32, device=dev)
         self.chans = torch.empty((rows, 32), dtype=torch.int32, device=dev)
@@ -158,10 +159,11 @@ class Model:
             V = torch.stack([synth.values(w, r, dev) for r in range(s0, s1)])
             ix = F.pack(K, S)
             fx = F.fixed136_pack(K, ix.var) if comparator else None
+            KV = torch.stack([K, V], dim=2)  # [H][n][2][128], contiguous
             for store in (self.h, self.d):
                 if store:
-                    store["K"][s0:s1].copy_(K)
-                    store["V"][s0:s1].copy_(V)
+                    store["KV"][s0:s1].copy_(KV)
+            del KV
             for l in range(src, L, KL):
                 r0, r1 = l * H, (l + 1) * H
                 self.var[r0:r1] = ix.var
@@ -353,8 +355,8 @@ def cpu_baseline(model, store, log, seconds=(10.0, 30.0)):
     meta = store["meta"][:rows].numpy().view(np.uint16)
     var = model.var[:rows].cpu().numpy()
     q = model.q[: rows * G].float().cpu().numpy()
-    K = store["K"][:rows].float().numpy() if store["K"].device.type == "cpu" else store["K"][:rows].float().cpu().numpy()
-    V = store["V"][:rows].float().numpy() if store["V"].device.type == "cpu" else store["V"][:rows].float().cpu().numpy()
+    K = store["K"][:rows].float().cpu().numpy()
+    V = store["V"][:rows].float().cpu().numpy()
     reps, t = 0, 0.0
     t0 = time.time()
     while t < seconds[0] and reps < 50:
@@ -448,6 +450,7 @@ def main():
         g = capture(steps, stream)
         clocks = Clocks(local) if res == primary else None
         total, per, ck = time_graph(g, args.steps, args.warmup, stream, clocks)
+        log("%s-resident step ms: %s" % (res, " ".join("%.2f" % x for x in per)))
         total = max_over_ranks(total)
         ms = total / args.steps
         scan_ms, scan_bytes, _ = scan_timing(model, store, max(3, args.steps // 4), stream)

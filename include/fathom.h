@@ -159,15 +159,22 @@ int fathom_sparse_attn_workspace_bytes(int rows, int group, int64_t k, size_t* b
 /* Exact attention over the selected keys, each query head with its own q
  * ([A] "What the model keeps in memory"; "The first fix").
  *   q        device [rows*group][128] of q_dtype.
- *   K, V     device or mapped host, [rows][n][128] of kv_dtype (original
- *            16-bit or fp32 rows, not the 4-bit index).
+ *   K, V     device or mapped host: the key and value of token t of row r
+ *            are the 128 contiguous elements of kv_dtype at
+ *            K + (r*n + t)*kv_stride and V + (r*n + t)*kv_stride (original
+ *            16-bit or fp32 rows, not the 4-bit index).  kv_stride = 128 is
+ *            the dense [rows][n][128] layout; kv_stride = 256 with V = K + 128
+ *            interleaves K and V per token, so a winner is one contiguous
+ *            512-byte (16-bit) row: half the address translations when the
+ *            rows sit in host memory.
+ *   kv_stride  elements, >= 128 and a multiple of 4 (8-byte aligned rows).
  *   idx      device int32 [rows][k]; entries < 0 are skipped.
  *   out      device float [rows*group][128] out, softmax(q.K/sqrt(128)).V.
  *   out_bf16 device uint16 (bf16 bits) [rows*group][128] out, or NULL: the
  *            round-to-nearest-even bf16 of out. */
 int fathom_sparse_attn(int rows, int group, int64_t n, int64_t k, const void* q, int q_dtype, const void* K,
-                       const void* V, int kv_dtype, const int32_t* idx, float* out, uint16_t* out_bf16,
-                       void* workspace, size_t ws_bytes, void* stream);
+                       const void* V, int kv_dtype, int64_t kv_stride, const int32_t* idx, float* out,
+                       uint16_t* out_bf16, void* workspace, size_t ws_bytes, void* stream);
 
 /* One decode step over `index.rows` rows: allocate -> scan -> top-k ->
  * sparse attention ([R] summary: the index scan ranks all n keys to choose
@@ -180,13 +187,14 @@ typedef struct fathom_step_desc {
   int64_t k;                /* winners per row, >= 1 */
   int32_t q_dtype;          /* dtype of q */
   int32_t kv_dtype;         /* dtype of K and V */
+  int64_t kv_stride;        /* elements between consecutive tokens' K (and V) rows, see fathom_sparse_attn */
   const uint32_t* planes;   /* index (device or mapped host) */
   const uint16_t* meta;     /* index (device or mapped host) */
   const float* var;         /* device [rows][128] */
   const uint16_t* budgets;  /* device [rows] or NULL */
   const void* q;            /* device [rows*group][128] */
-  const void* K;            /* device or mapped host [rows][n][128] */
-  const void* V;            /* device or mapped host [rows][n][128] */
+  const void* K;            /* device or mapped host, rows of kv_stride elements */
+  const void* V;            /* device or mapped host, rows of kv_stride elements */
   int32_t* idx;             /* device [rows][k] out */
   float* out;               /* device [rows*group][128] out */
   uint16_t* out_bf16;       /* device [rows*group][128] out or NULL */
@@ -225,6 +233,7 @@ typedef struct fathom_fixed136_step_desc {
   int64_t k;
   int32_t q_dtype;
   int32_t kv_dtype;
+  int64_t kv_stride;     /* as in fathom_step_desc */
   const int32_t* chans;
   const uint8_t* codes;  /* device or mapped host */
   const uint8_t* exps;   /* device or mapped host */
@@ -239,6 +248,24 @@ typedef struct fathom_fixed136_step_desc {
 int fathom_fixed136_step_workspace_bytes(const fathom_fixed136_step_desc* step, size_t* bytes);
 int fathom_fixed136_decode_step(const fathom_fixed136_step_desc* step, void* workspace, size_t ws_bytes,
                                 void* stream);
+
+/* ---------------- host residency ------------------------------------------
+ * With the cache in host memory, the index scan and the winner gathers cross
+ * the host link ([A] "Where the memory lives changes the answer"; [R] "What
+ * made it difficult": gathers of 4 KB runs reach the link rate).  The scan
+ * streams at the link rate from any pinned memory, but the winner gathers are
+ * random rows, and their rate is bounded by address translation: memory
+ * backed by transparent huge pages translates several times fewer pages per
+ * gathered row than 64 KB-page pinned memory.
+ *
+ * fathom_host_alloc: `bytes` (> 0) of page-aligned host memory, anonymous,
+ * advised for transparent huge pages, touched, and registered with CUDA
+ * (mapped, portable) so that kernels read it over the host link.  *ptr is
+ * both the host and the device address.  The library keeps no record of it;
+ * release it with fathom_host_free(ptr, bytes) (same size).  ENOMEM if the
+ * mapping or the registration fails.  Host-only work plus one CUDA call. */
+int fathom_host_alloc(size_t bytes, void** ptr);
+int fathom_host_free(void* ptr, size_t bytes);
 
 #ifdef __cplusplus
 }

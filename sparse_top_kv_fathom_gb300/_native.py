@@ -20,14 +20,14 @@ class IndexDesc(ctypes.Structure):
 class StepDesc(ctypes.Structure):
     _fields_ = [("index", IndexDesc), ("group", ctypes.c_int32), ("budget", ctypes.c_int32),
                 ("k", ctypes.c_int64), ("q_dtype", ctypes.c_int32), ("kv_dtype", ctypes.c_int32),
-                ("planes", P), ("meta", P), ("var", P), ("budgets", P), ("q", P), ("K", P), ("V", P),
+                ("kv_stride", ctypes.c_int64), ("planes", P), ("meta", P), ("var", P), ("budgets", P), ("q", P), ("K", P), ("V", P),
                 ("idx", P), ("out", P), ("out_bf16", P), ("status", P)]
 
 
 class Fixed136StepDesc(ctypes.Structure):
     _fields_ = [("n", ctypes.c_int64), ("rows", ctypes.c_int32), ("group", ctypes.c_int32),
                 ("k", ctypes.c_int64), ("q_dtype", ctypes.c_int32), ("kv_dtype", ctypes.c_int32),
-                ("chans", P), ("codes", P), ("exps", P), ("q", P), ("K", P), ("V", P),
+                ("kv_stride", ctypes.c_int64), ("chans", P), ("codes", P), ("exps", P), ("q", P), ("K", P), ("V", P),
                 ("idx", P), ("out", P), ("out_bf16", P)]
 
 
@@ -45,7 +45,7 @@ SIGNATURES = {
     "fathom_topk_workspace_bytes": ([I32, I64, I64, SZP], I32),
     "fathom_topk": ([I32, I64, I64, P, P, P, P, SZ, P], I32),
     "fathom_sparse_attn_workspace_bytes": ([I32, I32, I64, SZP], I32),
-    "fathom_sparse_attn": ([I32, I32, I64, I64, P, I32, P, P, I32, P, P, P, P, SZ, P], I32),
+    "fathom_sparse_attn": ([I32, I32, I64, I64, P, I32, P, P, I32, I64, P, P, P, P, SZ, P], I32),
     "fathom_decode_step_workspace_bytes": ([ctypes.POINTER(StepDesc), SZP], I32),
     "fathom_decode_step": ([ctypes.POINTER(StepDesc), P, SZ, P], I32),
     "fathom_fixed136_pack_workspace_bytes": ([I32, I64, SZP], I32),
@@ -54,6 +54,8 @@ SIGNATURES = {
     "fathom_fixed136_step_workspace_bytes": ([ctypes.POINTER(Fixed136StepDesc), SZP], I32),
     "fathom_fixed136_decode_step": ([ctypes.POINTER(Fixed136StepDesc), P, SZ, P], I32),
     "fathom_probe_stream_read": ([P, SZ, I32, I32, P, P], I32),
+    "fathom_host_alloc": ([SZ, ctypes.POINTER(ctypes.c_void_p)], I32),
+    "fathom_host_free": ([P, SZ], I32),
 }
 
 _lib = None

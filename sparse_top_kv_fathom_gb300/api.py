@@ -136,6 +136,18 @@ def topk(scores, k, with_values=False, stream=None):
     return (idx, vals) if with_values else idx
 
 
+def kv_stride(K, V):
+    """Elements between consecutive tokens' rows of K and V ([rows][n][128] views,
+    dense or interleaved); rows of a KV head follow each other."""
+    rows, n, d = K.shape
+    if V.shape != K.shape or K.stride() != V.stride() or K.stride(2) != 1 or d != D:
+        raise ValueError("K and V must be [rows][n][128] views with equal strides and contiguous rows")
+    s = K.stride(1)
+    if rows > 1 and K.stride(0) != n * s:
+        raise ValueError("consecutive KV heads must follow each other (stride(0) == n * stride(1))")
+    return s
+
+
 def sparse_attn(q, K, V, idx, group, stream=None):
     """Attention over the selected rows -> (out fp32 [rows*group][128], out bf16)."""
     L = lib()
@@ -147,7 +159,8 @@ def sparse_attn(q, K, V, idx, group, stream=None):
     wsb = ctypes.c_size_t()
     N.check(L.fathom_sparse_attn_workspace_bytes(rows, group, k, ctypes.byref(wsb)))
     ws = _ws(wsb.value, dev)
-    N.check(L.fathom_sparse_attn(rows, group, n, k, _ptr(q), _dt(q), _ptr(K), _ptr(V), _dt(K), _ptr(idx), _ptr(out),
+    N.check(L.fathom_sparse_attn(rows, group, n, k, _ptr(q), _dt(q), _ptr(K), _ptr(V), _dt(K), kv_stride(K, V),
+                                 _ptr(idx), _ptr(out),
                                  _ptr(outb), _ptr(ws), wsb.value, _stream(stream)))
     return out, outb
 
@@ -178,6 +191,7 @@ class DecodeStep:
         self.desc.k = k
         self.desc.q_dtype = _dt(q)
         self.desc.kv_dtype = _dt(K)
+        self.desc.kv_stride = kv_stride(K, V)
         self._bind()
         wsb = ctypes.c_size_t()
         N.check(self.L.fathom_decode_step_workspace_bytes(ctypes.byref(self.desc), ctypes.byref(wsb)))
@@ -260,7 +274,7 @@ class Fixed136Step:
                          torch.empty((index.rows * group, D), dtype=torch.bfloat16, device=dev))
         d = self.desc = N.Fixed136StepDesc()
         d.n, d.rows, d.group, d.k = index.n, index.rows, group, k
-        d.q_dtype, d.kv_dtype = _dt(q), _dt(K)
+        d.q_dtype, d.kv_dtype, d.kv_stride = _dt(q), _dt(K), kv_stride(K, V)
         d.chans, d.codes, d.exps = index.chans.data_ptr(), index.codes.data_ptr(), index.exps.data_ptr()
         d.q, d.K, d.V = q.data_ptr(), K.data_ptr(), V.data_ptr()
         d.idx, d.out, d.out_bf16 = self.idx.data_ptr(), self.out.data_ptr(), self.out_bf16.data_ptr()
@@ -278,6 +292,43 @@ class Fixed136Step:
         N.check(self.L.fathom_fixed136_decode_step(ctypes.byref(self.desc), _ptr(self.ws), self.ws_bytes,
                                                    _stream(stream)))
         return self.idx, self.out, self.out_bf16
+
+
+class _HostBlock:
+    """Owner of one fathom_host_alloc block; frees it when the last tensor view dies."""
+
+    def __init__(self, nbytes):
+        self.L = lib()
+        p = ctypes.c_void_p()
+        N.check(self.L.fathom_host_alloc(nbytes, ctypes.byref(p)))
+        self.ptr, self.nbytes = p.value, nbytes
+        self.buf = (ctypes.c_char * nbytes).from_address(self.ptr)
+
+    def __del__(self):
+        if getattr(self, "ptr", None):
+            self.L.fathom_host_free(ctypes.c_void_p(self.ptr), self.nbytes)
+            self.ptr = None
+
+
+def host_empty(shape, dtype):
+    """A CPU tensor in pinned, transparent-huge-page host memory (fathom_host_alloc),
+    readable by the kernels over the host link.  Contents are zero."""
+    numel = 1
+    for x in shape:
+        numel *= int(x)
+    esize = torch.empty((), dtype=dtype).element_size()
+    blk = _HostBlock(max(numel * esize, 1))
+    t = torch.frombuffer(blk.buf, dtype=torch.uint8, count=numel * esize).view(dtype).view(*shape)
+    _HOST_BLOCKS[t.data_ptr()] = blk  # kept alive with the tensor (see host_release)
+    return t
+
+
+_HOST_BLOCKS = {}
+
+
+def host_release(t):
+    """Free the fathom_host_alloc block behind a tensor made by host_empty (views die with it)."""
+    _HOST_BLOCKS.pop(t.data_ptr(), None)
 
 
 def probe_stream_read(buf, blocks_per_sm=4, threads=512, sink=None, stream=None):

@@ -9,9 +9,11 @@
 // is w_c = qbar_c^2 * var_c (Glonce summary: variance-weighted importance).
 //
 // GPU form: one CTA per row, one thread per candidate (channel c, plane j).
-// Each thread ranks its gain against all 512 candidates (gain descending, then
-// j ascending, then c ascending) and is taken if its rank is below the budget;
-// the rank is a total order, so exactly min(B, 512) candidates are taken.
+// As on the page, the threshold tau is found by binary search: over the bit
+// patterns of non-negative fp32 gains (which order like integers), the largest
+// tau with at least B gains >= tau, each count taken by one __syncthreads_count.
+// Gains above tau are taken; gains equal to tau are handed out in (j, c) order
+// (j ascending, then c ascending) until exactly B are taken.
 #include "common.cuh"
 
 namespace fathom {
@@ -24,8 +26,9 @@ __global__ void __launch_bounds__(kCand) allocate_kernel(int group, const void* 
                                                          const uint16_t* __restrict__ budgets, int budget,
                                                          uint8_t* __restrict__ bits, float* __restrict__ qbar,
                                                          int32_t* __restrict__ status) {
-  __shared__ float s_gain[kCand];
+  __shared__ float s_gain[kD];
   __shared__ int s_count[kD];
+  __shared__ int s_weq[kCand / 32];
   __shared__ int s_bad;
   const int r = blockIdx.x;
   const int i = threadIdx.x;  // candidate index = j * 128 + c
@@ -54,21 +57,30 @@ __global__ void __launch_bounds__(kCand) allocate_kernel(int group, const void* 
     w = s_gain[c];
     for (int jj = 0; jj < j; ++jj) w = __fmul_rn(w, 0.25f);
   }
-  __syncthreads();  // everyone has read s_gain[c] before it is overwritten below
-  s_gain[i] = w;
-  __syncthreads();
+  const uint32_t gb = __float_as_uint(w);  // w >= +0: bit patterns order like the values
   int B = budgets ? int(budgets[r]) : budget;
   if (B > kCand) {
     if (i == 0 && status) atomicOr(status, FATHOM_STATUS_BUDGET_CLAMPED);
     B = kCand;
   }
-  int rank = 0;
-#pragma unroll 8
-  for (int o = 0; o < kCand; ++o) {
-    const float g = s_gain[o];
-    rank += (g > w) || (g == w && o < i);
+  bool take = false;
+  if (B > 0) {
+    uint32_t lo = 0u, hi = 0x7f800000u;  // count(gain >= lo) = 512 >= B
+    while (lo < hi) {                    // uniform: every thread holds the same lo, hi
+      const uint32_t mid = lo + (hi - lo + 1u) / 2u;
+      if (__syncthreads_count(gb >= mid) >= B) lo = mid;
+      else hi = mid - 1u;
+    }
+    const int above = __syncthreads_count(gb > lo);
+    // rank of this candidate among those equal to tau, in (j, c) order = thread order
+    const unsigned eqb = __ballot_sync(0xffffffffu, gb == lo);
+    if ((i & 31) == 0) s_weq[i >> 5] = __popc(eqb);
+    __syncthreads();
+    int eq_before = __popc(eqb & ((1u << (i & 31)) - 1u));
+    for (int wp = 0; wp < (i >> 5); ++wp) eq_before += s_weq[wp];
+    take = gb > lo || (gb == lo && eq_before < B - above);
   }
-  if (rank < B) atomicAdd(&s_count[c], 1);
+  if (take) atomicAdd(&s_count[c], 1);
   __syncthreads();
   if (i < kD) bits[int64_t(r) * kD + i] = uint8_t(s_count[i]);
 }

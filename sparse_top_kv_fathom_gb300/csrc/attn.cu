@@ -27,15 +27,15 @@ struct Row4;
 template <>
 struct Row4<float> {
   using raw = float4;
-  __device__ static float4 get(const float* p, int64_t row, int lane) {
-    const float4 v = __ldg(reinterpret_cast<const float4*>(p + row * kD) + lane);
+  __device__ static float4 get(const float* p, int64_t row, int64_t stride, int lane) {
+    const float4 v = __ldg(reinterpret_cast<const float4*>(p + row * stride) + lane);
     return v;
   }
 };
 template <>
 struct Row4<__half> {
-  __device__ static float4 get(const __half* p, int64_t row, int lane) {
-    const uint2 u = __ldg(reinterpret_cast<const uint2*>(p + row * kD) + lane);
+  __device__ static float4 get(const __half* p, int64_t row, int64_t stride, int lane) {
+    const uint2 u = __ldg(reinterpret_cast<const uint2*>(p + row * stride) + lane);
     const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&u.x));
     const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&u.y));
     return make_float4(a.x, a.y, b.x, b.y);
@@ -43,8 +43,8 @@ struct Row4<__half> {
 };
 template <>
 struct Row4<__nv_bfloat16> {
-  __device__ static float4 get(const __nv_bfloat16* p, int64_t row, int lane) {
-    const uint2 u = __ldg(reinterpret_cast<const uint2*>(p + row * kD) + lane);
+  __device__ static float4 get(const __nv_bfloat16* p, int64_t row, int64_t stride, int lane) {
+    const uint2 u = __ldg(reinterpret_cast<const uint2*>(p + row * stride) + lane);
     const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
     const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
     return make_float4(a.x, a.y, b.x, b.y);
@@ -52,7 +52,7 @@ struct Row4<__nv_bfloat16> {
 };
 
 template <int G, typename KV>
-__global__ void __launch_bounds__(kAttnThreads) attn_partial_kernel(int64_t n, int64_t k, int splits,
+__global__ void __launch_bounds__(kAttnThreads) attn_partial_kernel(int64_t n, int64_t k, int64_t stride, int splits,
                                                                     const void* __restrict__ q, int q_dtype,
                                                                     const KV* __restrict__ K, const KV* __restrict__ V,
                                                                     const int32_t* __restrict__ idx,
@@ -73,8 +73,8 @@ __global__ void __launch_bounds__(kAttnThreads) attn_partial_kernel(int64_t n, i
   const int64_t per = (k + splits - 1) / splits;
   const int64_t i0 = int64_t(sp) * per, i1 = (i0 + per < k) ? i0 + per : k;
   const int32_t* ir = idx + int64_t(r) * k;
-  const KV* Kr = K + int64_t(r) * n * kD;
-  const KV* Vr = V + int64_t(r) * n * kD;
+  const KV* Kr = K + int64_t(r) * n * stride;
+  const KV* Vr = V + int64_t(r) * n * stride;
 
   float m[G], l[G];
   float4 o[G];
@@ -96,8 +96,8 @@ __global__ void __launch_bounds__(kAttnThreads) attn_partial_kernel(int64_t n, i
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
       if (t[u] >= 0) {
-        kr[u] = Row4<KV>::get(Kr, t[u], lane);
-        vr[u] = Row4<KV>::get(Vr, t[u], lane);
+        kr[u] = Row4<KV>::get(Kr, t[u], stride, lane);
+        vr[u] = Row4<KV>::get(Vr, t[u], stride, lane);
       } else {
         kr[u] = vr[u] = make_float4(0.f, 0.f, 0.f, 0.f);
       }
@@ -199,10 +199,11 @@ int attn_splits(int rows, int64_t k) {
 
 template <int G, typename KV>
 cudaError_t launch_attn_t(int rows, int64_t n, int64_t k, const void* q, int q_dtype, const void* K, const void* V,
+                          int64_t stride,
                           const int32_t* idx, float* out, uint16_t* out_bf16, float* part, cudaStream_t st) {
   const int splits = attn_splits(rows, k);
   attn_partial_kernel<G, KV><<<dim3(splits, rows), kAttnThreads, 0, st>>>(
-      n, k, splits, q, q_dtype, reinterpret_cast<const KV*>(K), reinterpret_cast<const KV*>(V), idx, part);
+      n, k, stride, splits, q, q_dtype, reinterpret_cast<const KV*>(K), reinterpret_cast<const KV*>(V), idx, part);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   attn_combine_kernel<G><<<rows * G, kD, 0, st>>>(splits, part, out, out_bf16);
@@ -211,13 +212,13 @@ cudaError_t launch_attn_t(int rows, int64_t n, int64_t k, const void* q, int q_d
 
 template <int G>
 cudaError_t launch_attn_g(int rows, int64_t n, int64_t k, const void* q, int q_dtype, const void* K, const void* V,
-                          int kv_dtype, const int32_t* idx, float* out, uint16_t* out_bf16, float* part,
+                          int kv_dtype, int64_t stride, const int32_t* idx, float* out, uint16_t* out_bf16, float* part,
                           cudaStream_t st) {
   if (kv_dtype == FATHOM_F32)
-    return launch_attn_t<G, float>(rows, n, k, q, q_dtype, K, V, idx, out, out_bf16, part, st);
+    return launch_attn_t<G, float>(rows, n, k, q, q_dtype, K, V, stride, idx, out, out_bf16, part, st);
   if (kv_dtype == FATHOM_F16)
-    return launch_attn_t<G, __half>(rows, n, k, q, q_dtype, K, V, idx, out, out_bf16, part, st);
-  return launch_attn_t<G, __nv_bfloat16>(rows, n, k, q, q_dtype, K, V, idx, out, out_bf16, part, st);
+    return launch_attn_t<G, __half>(rows, n, k, q, q_dtype, K, V, stride, idx, out, out_bf16, part, st);
+  return launch_attn_t<G, __nv_bfloat16>(rows, n, k, q, q_dtype, K, V, stride, idx, out, out_bf16, part, st);
 }
 
 }  // namespace
@@ -228,18 +229,18 @@ size_t attn_ws_bytes(int rows, int group, int64_t k) {
 }
 
 cudaError_t launch_attn(int rows, int group, int64_t n, int64_t k, const void* q, int q_dtype, const void* K,
-                        const void* V, int kv_dtype, const int32_t* idx, float* out, uint16_t* out_bf16, void* ws,
+                        const void* V, int kv_dtype, int64_t kv_stride, const int32_t* idx, float* out, uint16_t* out_bf16, void* ws,
                         cudaStream_t st) {
   float* part = reinterpret_cast<float*>(ws);
   switch (group) {
-    case 1: return launch_attn_g<1>(rows, n, k, q, q_dtype, K, V, kv_dtype, idx, out, out_bf16, part, st);
-    case 2: return launch_attn_g<2>(rows, n, k, q, q_dtype, K, V, kv_dtype, idx, out, out_bf16, part, st);
-    case 3: return launch_attn_g<3>(rows, n, k, q, q_dtype, K, V, kv_dtype, idx, out, out_bf16, part, st);
-    case 4: return launch_attn_g<4>(rows, n, k, q, q_dtype, K, V, kv_dtype, idx, out, out_bf16, part, st);
-    case 5: return launch_attn_g<5>(rows, n, k, q, q_dtype, K, V, kv_dtype, idx, out, out_bf16, part, st);
-    case 6: return launch_attn_g<6>(rows, n, k, q, q_dtype, K, V, kv_dtype, idx, out, out_bf16, part, st);
-    case 7: return launch_attn_g<7>(rows, n, k, q, q_dtype, K, V, kv_dtype, idx, out, out_bf16, part, st);
-    case 8: return launch_attn_g<8>(rows, n, k, q, q_dtype, K, V, kv_dtype, idx, out, out_bf16, part, st);
+    case 1: return launch_attn_g<1>(rows, n, k, q, q_dtype, K, V, kv_dtype, kv_stride, idx, out, out_bf16, part, st);
+    case 2: return launch_attn_g<2>(rows, n, k, q, q_dtype, K, V, kv_dtype, kv_stride, idx, out, out_bf16, part, st);
+    case 3: return launch_attn_g<3>(rows, n, k, q, q_dtype, K, V, kv_dtype, kv_stride, idx, out, out_bf16, part, st);
+    case 4: return launch_attn_g<4>(rows, n, k, q, q_dtype, K, V, kv_dtype, kv_stride, idx, out, out_bf16, part, st);
+    case 5: return launch_attn_g<5>(rows, n, k, q, q_dtype, K, V, kv_dtype, kv_stride, idx, out, out_bf16, part, st);
+    case 6: return launch_attn_g<6>(rows, n, k, q, q_dtype, K, V, kv_dtype, kv_stride, idx, out, out_bf16, part, st);
+    case 7: return launch_attn_g<7>(rows, n, k, q, q_dtype, K, V, kv_dtype, kv_stride, idx, out, out_bf16, part, st);
+    case 8: return launch_attn_g<8>(rows, n, k, q, q_dtype, K, V, kv_dtype, kv_stride, idx, out, out_bf16, part, st);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -259,11 +260,12 @@ int fathom_sparse_attn_workspace_bytes(int rows, int group, int64_t k, size_t* b
 }
 
 int fathom_sparse_attn(int rows, int group, int64_t n, int64_t k, const void* q, int q_dtype, const void* K,
-                       const void* V, int kv_dtype, const int32_t* idx, float* out, uint16_t* out_bf16,
-                       void* workspace, size_t ws_bytes, void* stream) {
+                       const void* V, int kv_dtype, int64_t kv_stride, const int32_t* idx, float* out,
+                       uint16_t* out_bf16, void* workspace, size_t ws_bytes, void* stream) {
   clear_error();
   if (rows < 1 || rows > 65535 || group < 1 || group > 8 || n < 1 || k < 1 || n > 0x7fffffff)
     return set_error(FATHOM_EINVAL, "rows, group (1..8), n, k out of range");
+  if (kv_stride < kD || (kv_stride & 3)) return set_error(FATHOM_EINVAL, "kv_stride must be >= 128, a multiple of 4");
   if (!valid_dtype(q_dtype) || !valid_dtype(kv_dtype)) return set_error(FATHOM_EINVAL, "invalid dtype");
   const void *dq, *dK, *dV, *dI, *dO, *dB, *dW;
   FATHOM_TRY(device_view(q, "q", &dq));
@@ -280,7 +282,8 @@ int fathom_sparse_attn(int rows, int group, int64_t n, int64_t k, const void* q,
   const size_t al = kv_dtype == FATHOM_F32 ? 16 : 8;
   if ((reinterpret_cast<uintptr_t>(dK) % al) || (reinterpret_cast<uintptr_t>(dV) % al))
     return set_error(FATHOM_EINVAL, "K and V must be %zu-byte aligned", al);
-  FATHOM_TRY_CUDA(launch_attn(rows, group, n, k, dq, q_dtype, dK, dV, kv_dtype, (const int32_t*)dI, (float*)dO,
+  FATHOM_TRY_CUDA(launch_attn(rows, group, n, k, dq, q_dtype, dK, dV, kv_dtype, kv_stride, (const int32_t*)dI,
+                              (float*)dO,
                               (uint16_t*)dB, const_cast<void*>(dW), as_stream(stream)));
   return FATHOM_OK;
 }

@@ -102,7 +102,7 @@ cudaError_t launch_scan(const IndexGeom& g, const uint32_t* planes, const __half
 cudaError_t launch_topk(int rows, int64_t n, int64_t k, const float* scores, int32_t* idx, float* vals, void* ws,
                         bool hist_ready, cudaStream_t st);
 cudaError_t launch_attn(int rows, int group, int64_t n, int64_t k, const void* q, int q_dtype, const void* K,
-                        const void* V, int kv_dtype, const int32_t* idx, float* out, uint16_t* out_bf16, void* ws,
+                        const void* V, int kv_dtype, int64_t kv_stride, const int32_t* idx, float* out, uint16_t* out_bf16, void* ws,
                         cudaStream_t st);
 cudaError_t launch_fixed136_scan(int rows, int64_t n, const int32_t* chans, const uint8_t* codes, const uint8_t* exps,
                                  const float* qbar, float* scores, uint32_t* hist, cudaStream_t st);

@@ -8,24 +8,34 @@
 //     s(t) = sum_{c: b_c>=1} qbar_c * (lo + delta*(m*p_c(t) + (m-1)/2)),
 // m = 2^(4-b_c), p_c(t) the b_c-bit prefix, (lo, delta) of t's 128-token block.
 //
-// GPU form (integer work per bit is what bounds this scan when the index sits
-// in HBM, per the article's "Where this does not work" and the Rootconf
-// proposal): one thread owns 32 consecutive tokens, i.e. exactly one 32-bit
-// word of every plane.  For each active channel it loads b_c words (coalesced:
-// a warp reads 128 contiguous bytes per plane), merges them into four
-// "nibble words" of 8 tokens each with shifts and masks (~1/4 integer op per
-// plane bit), then turns each 4-bit prefix into a float by OR-ing it under the
-// mantissa of 1.0 (1 + u/16, exact) and accumulates with one FMA per token and
-// channel.  The constant part of every term (lo, the bucket centre and the
-// -16*delta offset of the 1 + u/16 form) is folded into one per-thread value.
+// GPU form.  With the index in HBM the integer work per bit bounds this scan
+// (the article's "Where this does not work"; the Rootconf proposal's "What
+// made it difficult"), so the kernel is organised around it:
+//   * one thread owns 32 consecutive tokens = exactly one 32-bit word of every
+//     plane, so a warp reads 128 contiguous bytes per (channel, plane) and
+//     never extracts a bit it does not use;
+//   * a 4-stage cp.async ring stages each thread's plane words and block
+//     (lo, delta) a few channels ahead, hiding memory latency without
+//     registers (each thread reads back only what it copied, so no barrier);
+//   * per channel, the b_c planes are merged into four "nibble words" (8 tokens
+//     x 4 bits) with b_c shifts and b_c-1 bit-select ops each; the prefix of a
+//     token becomes the float 1 + u/16 by one shift and one mask-or under the
+//     mantissa of 1.0 (exact, mask depends on b_c);
+//   * x = fma(16*delta, 1 + u/16, lo + delta*((m-1)/2 - 16)) = lo + delta*(u +
+//     (m-1)/2) with a single rounding, then acc += qbar * x; both FMAs run on
+//     two tokens at a time (packed f32x2), so each term carries only a few ulps
+//     of |qbar_c * x_c| of error.
+// Inside the decode step the kernel also builds the 12-bit first-digit
+// histogram of its scores for the top-k.
 #include "common.cuh"
 
 namespace fathom {
 namespace {
 
-constexpr int kScanThreads = 128;                  // one warp group: 4096 tokens per CTA
+constexpr int kScanThreads = 256;  // 8192 tokens per CTA
 constexpr int kTokPerThread = 32;
 constexpr int kTile = kScanThreads * kTokPerThread;
+constexpr int kStages = 4;
 
 template <int SH>
 __device__ __forceinline__ uint32_t shift_signed(uint32_t x) {
@@ -35,67 +45,112 @@ __device__ __forceinline__ uint32_t shift_signed(uint32_t x) {
   else return x;
 }
 
-// o_k: nibble m holds the 4-bit prefix of token 4m+k (plane 0 in bit 3).
-template <int K>
+// bit select: bits of a where mask is set, of b elsewhere
+__device__ __forceinline__ uint32_t bitsel(uint32_t mask, uint32_t a, uint32_t b) { return (a & mask) | (b & ~mask); }
+
+// o_k for depth DEP: nibble m holds the prefix of token 4m+k in its top DEP bits
+// (plane 0 in bit 3); bits below the prefix are left unspecified (masked later).
+template <int DEP, int K>
 __device__ __forceinline__ uint32_t nibble_word(uint32_t w0, uint32_t w1, uint32_t w2, uint32_t w3) {
-  return (shift_signed<K - 3>(w0) & 0x88888888u) | (shift_signed<K - 2>(w1) & 0x44444444u) |
-         (shift_signed<K - 1>(w2) & 0x22222222u) | (shift_signed<K>(w3) & 0x11111111u);
+  const uint32_t s0 = shift_signed<K - 3>(w0);
+  if constexpr (DEP == 1) return s0;
+  const uint32_t s1 = shift_signed<K - 2>(w1);
+  if constexpr (DEP == 2) return bitsel(0x88888888u, s0, s1);
+  const uint32_t s2 = shift_signed<K - 1>(w2);
+  if constexpr (DEP == 3) return bitsel(0x88888888u, s0, bitsel(0x44444444u, s1, s2));
+  const uint32_t s3 = shift_signed<K>(w3);
+  return bitsel(0x88888888u, s0, bitsel(0x44444444u, s1, bitsel(0x22222222u, s2, s3)));
 }
 
-// float 1 + u/16 for the nibble M of o (u in 0..15), exact.
-template <int M>
-__device__ __forceinline__ float nibble_float(uint32_t o) {
-  return __uint_as_float((shift_signed<4 * M - 19>(o) & 0x00780000u) | 0x3F800000u);
+// Mixed-precision FMA (sm_100+): fp16 multiplicands, fp32 addend and result,
+// one rounding.
+__device__ __forceinline__ float fma_f16_f32(uint16_t a, uint16_t b, float c) {
+  float d;
+  asm("fma.rn.f32.f16 %0, %1, %2, %3;" : "=f"(d) : "h"(a), "h"(b), "f"(c));
+  return d;
 }
 
+// The prefixes of tokens 4M+K (nibble M of o_K) and 4M+16+K (nibble M+4) as two
+// fp16 values 16 + u in one register: nibble M -> bits 6..9, nibble M+4 -> bits
+// 22..25 (16 apart), under the fp16 exponent of 16 (0x4C00), keeping only the
+// prefix bits `mask6` (exact).
 template <int M>
-__device__ __forceinline__ float2 nibble_pair(uint32_t oa, uint32_t ob) {
-  return make_float2(nibble_float<M>(oa), nibble_float<M>(ob));
+__device__ __forceinline__ uint32_t prefix_halves(uint32_t o, uint32_t mask6) {
+  return (shift_signed<4 * M - 6>(o) & mask6) | 0x4C004C00u;
 }
 
-// Tokens 4m+k0 and 4m+k0+1 (nibble m of oa and ob): x = lo' + 16*delta*(1 + u/16)
-// = lo + delta*(u + (m_c - 1)/2) with one rounding, then acc += qbar * x; two
-// tokens per packed f32x2 instruction.
-template <int M>
-__device__ __forceinline__ void accumulate_pair(float2& acc, uint32_t oa, uint32_t ob, float2 d16, float2 lo2,
-                                                float2 q2) {
-  const float2 x = __ffma2_rn(d16, nibble_pair<M>(oa, ob), lo2);
+// x = delta*(16 + u) + lo' = lo + delta*(u + (m-1)/2) in one rounding per token,
+// then acc += qbar * x for the two tokens at once (packed f32x2 FMA).
+__device__ __forceinline__ void accumulate_halves(float2& acc, uint32_t h2, uint16_t dl16, float lop, float2 q2) {
+  const float2 x = make_float2(fma_f16_f32(dl16, uint16_t(h2 & 0xFFFFu), lop), fma_f16_f32(dl16, uint16_t(h2 >> 16), lop));
   acc = __ffma2_rn(q2, x, acc);
 }
 
+// acc[4m + k] holds tokens (4m + k, 4m + 16 + k).
+template <int DEP>
+__device__ __forceinline__ void channel_terms(float2 (&acc)[kTokPerThread / 2], uint32_t w0, uint32_t w1, uint32_t w2,
+                                              uint32_t w3, uint16_t dl16, float lop, float2 q2) {
+  constexpr uint32_t mnib = (0xF0u >> DEP) & 0xFu;  // top DEP bits of a nibble
+  constexpr uint32_t mask6 = (mnib << 6) | (mnib << 22);
+  const uint32_t o[4] = {nibble_word<DEP, 0>(w0, w1, w2, w3), nibble_word<DEP, 1>(w0, w1, w2, w3),
+                         nibble_word<DEP, 2>(w0, w1, w2, w3), nibble_word<DEP, 3>(w0, w1, w2, w3)};
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    accumulate_halves(acc[0 + k], prefix_halves<0>(o[k], mask6), dl16, lop, q2);
+    accumulate_halves(acc[4 + k], prefix_halves<1>(o[k], mask6), dl16, lop, q2);
+    accumulate_halves(acc[8 + k], prefix_halves<2>(o[k], mask6), dl16, lop, q2);
+    accumulate_halves(acc[12 + k], prefix_halves<3>(o[k], mask6), dl16, lop, q2);
+  }
+}
+
+__device__ __forceinline__ void cp_async4(void* smem, const void* gmem) {
+  const unsigned s = static_cast<unsigned>(__cvta_generic_to_shared(smem));
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(s), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
+}
+
 template <bool kHist>
-__global__ void __launch_bounds__(kScanThreads) scan_kernel(const uint32_t* __restrict__ planes,
-                                                            const __half2* __restrict__ meta,
-                                                            const uint8_t* __restrict__ bits,
-                                                            const float* __restrict__ qbar, float* __restrict__ scores,
-                                                            uint32_t* __restrict__ hist, int64_t n, int64_t nsb,
-                                                            int log2S, int64_t nblk) {
+__global__ void __launch_bounds__(kScanThreads, 4) scan_kernel(const uint32_t* __restrict__ planes,
+                                                               const __half2* __restrict__ meta,
+                                                               const uint8_t* __restrict__ bits,
+                                                               const float* __restrict__ qbar,
+                                                               float* __restrict__ scores, uint32_t* __restrict__ hist,
+                                                               int64_t n, int64_t nsb, int log2S, int64_t nblk) {
   __shared__ int s_ch[kD];
   __shared__ int s_dep[kD];
   __shared__ float s_q[kD];
-  __shared__ int s_wcnt[kScanThreads / 32];
-  __shared__ float s_tr[kScanThreads / 32][32][33];
+  __shared__ int s_wcnt[kD / 32];
+  __shared__ uint32_t s_w[kStages][kPlanes][kScanThreads];
+  __shared__ __half2 s_m[kStages][kScanThreads];
   __shared__ uint32_t s_hist[kHist ? kHistBins : 1];
 
   const int r = blockIdx.y;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
-  // Active channels of this row, in channel order.
-  const int dep = min(int(bits[int64_t(r) * kD + tid]), kPlanes);
-  const float qv = qbar[int64_t(r) * kD + tid];
-  const unsigned ball = __ballot_sync(0xffffffffu, dep > 0);
-  if (lane == 0) s_wcnt[warp] = __popc(ball);
+  // Active channels of this row, in channel order (warps 0..3, whole warps, cover the 128 channels).
+  int dep = 0;
+  float qv = 0.0f;
+  unsigned ball = 0u;
+  if (tid < kD) {
+    dep = min(int(bits[int64_t(r) * kD + tid]), kPlanes);
+    qv = qbar[int64_t(r) * kD + tid];
+    ball = __ballot_sync(0xffffffffu, dep > 0);
+    if (lane == 0) s_wcnt[warp] = __popc(ball);
+  }
   if constexpr (kHist) {
     for (int i = tid; i < kHistBins; i += kScanThreads) s_hist[i] = 0u;
   }
   __syncthreads();
-  int off = 0, nact = 0;
+  int nact = 0;
 #pragma unroll
-  for (int w = 0; w < kScanThreads / 32; ++w) {
-    off += (w < warp) ? s_wcnt[w] : 0;
-    nact += s_wcnt[w];
-  }
-  if (dep > 0) {
+  for (int w = 0; w < kD / 32; ++w) nact += s_wcnt[w];
+  if (tid < kD && dep > 0) {
+    int off = 0;
+    for (int w = 0; w < warp; ++w) off += s_wcnt[w];
     const int pos = off + __popc(ball & ((1u << lane) - 1u));
     s_ch[pos] = tid;
     s_dep[pos] = dep;
@@ -111,68 +166,75 @@ __global__ void __launch_bounds__(kScanThreads) scan_kernel(const uint32_t* __re
   const uint32_t* pb = planes + (int64_t(r) * nsb + (tt >> log2S)) * (kD * kPlanes) * run + ((tt & (S - 1)) >> 5);
   const __half2* mb = meta + int64_t(r) * kD * nblk + (tt >> 7);
 
-  float2 acc[kTokPerThread / 2];  // acc[i] = tokens (2i, 2i+1)
+  auto issue = [&](int a) {
+    if (a < nact && valid) {
+      const int st = a % kStages;
+      const int c = s_ch[a], d = s_dep[a];
+      const uint32_t* p = pb + int64_t(c) * kPlanes * run;
+      cp_async4(&s_w[st][0][tid], p);
+      if (d > 1) cp_async4(&s_w[st][1][tid], p + run);
+      if (d > 2) cp_async4(&s_w[st][2][tid], p + 2 * run);
+      if (d > 3) cp_async4(&s_w[st][3][tid], p + 3 * run);
+      cp_async4(&s_m[st][tid], mb + int64_t(c) * nblk);
+    }
+    cp_async_commit();  // one group per channel, possibly empty
+  };
+
+  float2 acc[kTokPerThread / 2];  // acc[i] = tokens (i, i + 16) of this thread's 32
 #pragma unroll
   for (int i = 0; i < kTokPerThread / 2; ++i) acc[i] = make_float2(0.0f, 0.0f);
 
+#pragma unroll
+  for (int a = 0; a < kStages - 1; ++a) issue(a);
   for (int a = 0; a < nact; ++a) {
-    const int c = s_ch[a];
+    issue(a + kStages - 1);
+    cp_async_wait<kStages - 1>();  // this thread's copies for channel a have landed
+    if (!valid) continue;
+    const int st = a % kStages;
     const int d = s_dep[a];
     const float q = s_q[a];
-    uint32_t w0 = 0u, w1 = 0u, w2 = 0u, w3 = 0u;
-    float lo = 0.0f, dl = 0.0f;
-    if (valid) {
-      const uint32_t* p = pb + int64_t(c) * kPlanes * run;
-      w0 = __ldg(p);
-      if (d > 1) w1 = __ldg(p + run);
-      if (d > 2) w2 = __ldg(p + 2 * run);
-      if (d > 3) w3 = __ldg(p + 3 * run);
-      const float2 m = __half22float2(__ldg(mb + int64_t(c) * nblk));
-      lo = m.x;
-      dl = m.y;
-    }
+    const __half2 mh = s_m[st][tid];
+    const float lo = __low2float(mh), dl = __high2float(mh);
+    const uint16_t dl16 = __half_as_ushort(__high2half(mh));
     const float half_m1 = float((1 << (4 - d)) - 1) * 0.5f;  // (m - 1) / 2
     // lo' = lo + delta*((m-1)/2 - 16): exact for fp16 lo, delta unless |lo| > 2^12 delta
     const float lop = fmaf(dl, half_m1 - 16.0f, lo);
-    const float2 lo2 = make_float2(lop, lop);
-    const float2 d16 = make_float2(16.0f * dl, 16.0f * dl);
     const float2 q2 = make_float2(q, q);
-    const uint32_t o0 = nibble_word<0>(w0, w1, w2, w3), o1 = nibble_word<1>(w0, w1, w2, w3);
-    const uint32_t o2 = nibble_word<2>(w0, w1, w2, w3), o3 = nibble_word<3>(w0, w1, w2, w3);
-    accumulate_pair<0>(acc[0], o0, o1, d16, lo2, q2);
-    accumulate_pair<0>(acc[1], o2, o3, d16, lo2, q2);
-    accumulate_pair<1>(acc[2], o0, o1, d16, lo2, q2);
-    accumulate_pair<1>(acc[3], o2, o3, d16, lo2, q2);
-    accumulate_pair<2>(acc[4], o0, o1, d16, lo2, q2);
-    accumulate_pair<2>(acc[5], o2, o3, d16, lo2, q2);
-    accumulate_pair<3>(acc[6], o0, o1, d16, lo2, q2);
-    accumulate_pair<3>(acc[7], o2, o3, d16, lo2, q2);
-    accumulate_pair<4>(acc[8], o0, o1, d16, lo2, q2);
-    accumulate_pair<4>(acc[9], o2, o3, d16, lo2, q2);
-    accumulate_pair<5>(acc[10], o0, o1, d16, lo2, q2);
-    accumulate_pair<5>(acc[11], o2, o3, d16, lo2, q2);
-    accumulate_pair<6>(acc[12], o0, o1, d16, lo2, q2);
-    accumulate_pair<6>(acc[13], o2, o3, d16, lo2, q2);
-    accumulate_pair<7>(acc[14], o0, o1, d16, lo2, q2);
-    accumulate_pair<7>(acc[15], o2, o3, d16, lo2, q2);
+    const uint32_t w0 = s_w[st][0][tid];
+    switch (d) {  // uniform across the CTA
+      case 1: channel_terms<1>(acc, w0, 0u, 0u, 0u, dl16, lop, q2); break;
+      case 2: channel_terms<2>(acc, w0, s_w[st][1][tid], 0u, 0u, dl16, lop, q2); break;
+      case 3: channel_terms<3>(acc, w0, s_w[st][1][tid], s_w[st][2][tid], 0u, dl16, lop, q2); break;
+      default:
+        channel_terms<4>(acc, w0, s_w[st][1][tid], s_w[st][2][tid], s_w[st][3][tid], dl16, lop, q2);
+        break;
+    }
   }
+  cp_async_wait<0>();
 
-  // Transpose through shared memory so that the stores are coalesced.
+  if (valid) {
+    float* out = scores + int64_t(r) * n + t0;
+    if (t0 + kTokPerThread <= n && (reinterpret_cast<uintptr_t>(out) & 15) == 0) {
 #pragma unroll
-  for (int i = 0; i < kTokPerThread / 2; ++i) {
-    s_tr[warp][lane][2 * i] = acc[i].x;
-    s_tr[warp][lane][2 * i + 1] = acc[i].y;
-  }
-  __syncwarp();
-  const int64_t tw = (int64_t(blockIdx.x) * kScanThreads + warp * 32) * kTokPerThread;  // warp's first token
-  float* out = scores + int64_t(r) * n;
-#pragma unroll 4
-  for (int i = 0; i < 32; ++i) {
-    const int64_t t = tw + int64_t(i) * 32 + lane;
-    const float s = s_tr[warp][i][lane];
-    if (t < n) {
-      out[t] = s;
-      if constexpr (kHist) atomicAdd(&s_hist[score_key(s) >> (32 - kHistBits)], 1u);
+      for (int i = 0; i < 4; ++i) {
+        reinterpret_cast<float4*>(out)[i] =
+            make_float4(acc[4 * i].x, acc[4 * i + 1].x, acc[4 * i + 2].x, acc[4 * i + 3].x);
+        reinterpret_cast<float4*>(out)[4 + i] =
+            make_float4(acc[4 * i].y, acc[4 * i + 1].y, acc[4 * i + 2].y, acc[4 * i + 3].y);
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < kTokPerThread / 2; ++i) {
+        if (t0 + i < n) out[i] = acc[i].x;
+        if (t0 + 16 + i < n) out[16 + i] = acc[i].y;
+      }
+    }
+    if constexpr (kHist) {
+#pragma unroll
+      for (int i = 0; i < kTokPerThread / 2; ++i) {
+        if (t0 + i < n) atomicAdd(&s_hist[score_key(acc[i].x) >> (32 - kHistBits)], 1u);
+        if (t0 + 16 + i < n) atomicAdd(&s_hist[score_key(acc[i].y) >> (32 - kHistBits)], 1u);
+      }
     }
   }
   if constexpr (kHist) {
@@ -190,7 +252,7 @@ __global__ void __launch_bounds__(kScanThreads) scan_kernel(const uint32_t* __re
 cudaError_t launch_scan(const IndexGeom& g, const uint32_t* planes, const __half2* meta, const uint8_t* bits,
                         const float* qbar, float* scores, uint32_t* hist, cudaStream_t st) {
   const int64_t tiles = (g.n + kTile - 1) / kTile;
-  dim3 grid(unsigned(tiles), unsigned(g.rows));
+  const dim3 grid{unsigned(tiles), unsigned(g.rows), 1u};
   if (hist)
     scan_kernel<true><<<grid, kScanThreads, 0, st>>>(planes, meta, bits, qbar, scores, hist, g.n, g.nsb, g.log2S,
                                                      g.nblk);

@@ -77,6 +77,7 @@ int fathom_decode_step(const fathom_step_desc* s, void* workspace, size_t ws_byt
   StepWs w = carve_step(const_cast<void*>(dW), g.rows, s->group, g.n, s->k);
   if (reinterpret_cast<uintptr_t>(dW) & 255) return set_error(FATHOM_EINVAL, "workspace must be 256-byte aligned");
   if (ws_bytes < w.end + 256) return set_error(FATHOM_ENOMEM, "workspace %zu < %zu bytes", ws_bytes, w.end + 256);
+  if (s->kv_stride < kD || (s->kv_stride & 3)) return set_error(FATHOM_EINVAL, "kv_stride must be >= 128, a multiple of 4");
   const size_t al = s->kv_dtype == FATHOM_F32 ? 16 : 8;
   if ((reinterpret_cast<uintptr_t>(dK) % al) || (reinterpret_cast<uintptr_t>(dV) % al) ||
       (reinterpret_cast<uintptr_t>(dP) & 3) || (reinterpret_cast<uintptr_t>(dM) & 3))
@@ -89,7 +90,7 @@ int fathom_decode_step(const fathom_step_desc* s, void* workspace, size_t ws_byt
                                   s->budget, w.bits, w.qbar, (int32_t*)dSt, st));
   FATHOM_TRY_CUDA(launch_scan(g, (const uint32_t*)dP, (const __half2*)dM, w.bits, w.qbar, w.scores, hist, st));
   FATHOM_TRY_CUDA(launch_topk(g.rows, g.n, s->k, w.scores, (int32_t*)dI, nullptr, w.topk, use_hist, st));
-  FATHOM_TRY_CUDA(launch_attn(g.rows, s->group, g.n, s->k, dq, s->q_dtype, dK, dV, s->kv_dtype, (const int32_t*)dI,
+  FATHOM_TRY_CUDA(launch_attn(g.rows, s->group, g.n, s->k, dq, s->q_dtype, dK, dV, s->kv_dtype, s->kv_stride, (const int32_t*)dI,
                               (float*)dO, (uint16_t*)dB, w.attn, st));
   return FATHOM_OK;
 }
@@ -125,6 +126,7 @@ int fathom_fixed136_decode_step(const fathom_fixed136_step_desc* s, void* worksp
   StepWs w = carve_step(const_cast<void*>(dW), s->rows, s->group, s->n, s->k);
   if (reinterpret_cast<uintptr_t>(dW) & 255) return set_error(FATHOM_EINVAL, "workspace must be 256-byte aligned");
   if (ws_bytes < w.end + 256) return set_error(FATHOM_ENOMEM, "workspace %zu < %zu bytes", ws_bytes, w.end + 256);
+  if (s->kv_stride < kD || (s->kv_stride & 3)) return set_error(FATHOM_EINVAL, "kv_stride must be >= 128, a multiple of 4");
   const size_t al = s->kv_dtype == FATHOM_F32 ? 16 : 8;
   if ((reinterpret_cast<uintptr_t>(dK) % al) || (reinterpret_cast<uintptr_t>(dV) % al) ||
       (reinterpret_cast<uintptr_t>(dX) & 15))
@@ -137,7 +139,7 @@ int fathom_fixed136_decode_step(const fathom_fixed136_step_desc* s, void* worksp
   FATHOM_TRY_CUDA(launch_fixed136_scan(s->rows, s->n, (const int32_t*)dC, (const uint8_t*)dX, (const uint8_t*)dE,
                                        w.qbar, w.scores, hist, st));
   FATHOM_TRY_CUDA(launch_topk(s->rows, s->n, s->k, w.scores, (int32_t*)dI, nullptr, w.topk, use_hist, st));
-  FATHOM_TRY_CUDA(launch_attn(s->rows, s->group, s->n, s->k, dq, s->q_dtype, dK, dV, s->kv_dtype, (const int32_t*)dI,
+  FATHOM_TRY_CUDA(launch_attn(s->rows, s->group, s->n, s->k, dq, s->q_dtype, dK, dV, s->kv_dtype, s->kv_stride, (const int32_t*)dI,
                               (float*)dO, (uint16_t*)dB, w.attn, st));
   return FATHOM_OK;
 }

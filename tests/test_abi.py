@@ -80,7 +80,10 @@ def test_invalid_arguments_are_rejected_on_the_host(F):
     assert L.fathom_allocate(1, 0, None, 2, None, None, 92, None, None, None, None) == 1
     assert L.fathom_allocate(1, 4, None, 9, None, None, 92, None, None, None, None) == 1
     assert L.fathom_topk(1, 10, 0, None, None, None, None, 0, None) == 1
-    assert L.fathom_sparse_attn(1, 9, 10, 1, None, 2, None, None, 2, None, None, None, None, 0, None) == 1
+    assert L.fathom_sparse_attn(1, 9, 10, 1, None, 2, None, None, 2, 128, None, None, None, None, 0, None) == 1
+    assert L.fathom_sparse_attn(1, 4, 10, 1, None, 2, None, None, 2, 130, None, None, None, None, 0, None) == 1
+    assert L.fathom_host_alloc(0, ctypes.byref(ctypes.c_void_p())) == 1
+    assert L.fathom_host_free(None, 16) == 1
     assert L.fathom_probe_stream_read(None, 17, 1, 256, None, None) == 1
     b = ctypes.c_size_t()
     assert L.fathom_topk_workspace_bytes(8, 1 << 20, 2048, ctypes.byref(b)) == 0 and b.value > 0

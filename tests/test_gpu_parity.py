@@ -148,6 +148,29 @@ def test_decode_step_host_resident_kv_and_index(case, gpu_lib):
     assert torch.equal(a[1], b[1])
 
 
+def test_interleaved_kv_in_huge_page_host_memory(case, gpu_lib):
+    """K and V interleaved per token (row stride 256) in fathom_host_alloc memory, index too:
+    same winners and outputs as the dense device-resident step."""
+    F, w = gpu_lib, case["w"]
+    k = min(w.k, w.n)
+    a = F.decode_step(case["index"], case["qd"], case["Kd"], case["Vd"], k, w.group, 92)
+    ix = case["index"]
+    KV = F.host_empty((w.rows, w.n, 2, 128), case["Kd"].dtype)
+    KV.copy_(torch.stack([case["Kd"], case["Vd"]], 2).cpu())
+    planes = F.host_empty(tuple(ix.planes.shape), torch.int32)
+    planes.copy_(ix.planes.cpu())
+    meta = F.host_empty(tuple(ix.meta.shape), torch.float16)
+    meta.copy_(ix.meta.cpu())
+    hix = F.BitPlaneIndex(planes, meta, ix.var, ix.n, ix.rows, ix.superblock)
+    assert F.kv_stride(KV[:, :, 0], KV[:, :, 1]) == 256
+    b = F.decode_step(hix, case["qd"], KV[:, :, 0], KV[:, :, 1], k, w.group, 92)
+    torch.cuda.synchronize()
+    assert torch.equal(a[0], b[0])
+    assert torch.equal(a[1], b[1])
+    for t in (KV, planes, meta):
+        F.host_release(t)
+
+
 def test_fixed136_parity(case, gpu_lib):
     F, w = gpu_lib, case["w"]
     fx = F.fixed136_pack(case["Kd"], case["index"].var)
