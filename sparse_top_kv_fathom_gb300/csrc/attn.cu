@@ -4,32 +4,35 @@
 // relevance; "The first fix": attend over just the k winners).  Every query
 // head of a KV head uses its own q with that KV head's winner set.
 //
-// GPU form: the winners of a row are split across CTAs (split count sized so
-// the grid covers the SMs); each warp gathers whole K and V rows (a lane holds
-// 4 channels: 8 contiguous bytes of a 16-bit row), reduces the G dot products
-// with shuffles and keeps an online softmax (running max, sum, weighted V);
-// the CTA merges its warps and writes one partial per (row, split, head).  A
-// second kernel merges the splits with the usual max-rescaled sums.  The rows
-// may sit in HBM or in pinned host memory (read over the host link).
+// GPU form: one thread-block cluster of kCluster CTAs per KV head.  Each CTA
+// takes a slice of the winners; each warp gathers whole K and V rows (a lane
+// holds 4 channels: 8 contiguous bytes of a 16-bit row), several winners in
+// flight per warp, reduces the group's dot products with shuffles and keeps an
+// online softmax (running max, sum and weighted V).  The CTA merges its warps
+// in shared memory; then CTA 0 of the cluster merges the kCluster partials by
+// reading the other CTAs' shared memory (distributed shared memory) and writes
+// the output: one launch, no partials in global memory.  The K/V rows may sit
+// in HBM or in pinned host memory.
+#include <cooperative_groups.h>
+
 #include "common.cuh"
+
+namespace cg = cooperative_groups;
 
 namespace fathom {
 namespace {
 
-constexpr int kAttnThreads = 128;
+constexpr int kAttnThreads = 256;
 constexpr int kAttnWarps = kAttnThreads / 32;
-constexpr int kUnroll = 4;      // winners in flight per warp
-constexpr int kPartStride = kD + 2;  // m, l, o[128]
-constexpr int kMinPerSplit = 32;
+constexpr int kCluster = 8;  // CTAs per KV head (portable cluster size)
+constexpr int kUnroll = 4;   // winners in flight per warp
 
 template <typename T>
 struct Row4;
 template <>
 struct Row4<float> {
-  using raw = float4;
   __device__ static float4 get(const float* p, int64_t row, int64_t stride, int lane) {
-    const float4 v = __ldg(reinterpret_cast<const float4*>(p + row * stride) + lane);
-    return v;
+    return __ldg(reinterpret_cast<const float4*>(p + row * stride) + lane);
   }
 };
 template <>
@@ -51,16 +54,24 @@ struct Row4<__nv_bfloat16> {
   }
 };
 
+// weight of a partial with running max mw when merged under the overall max M
+__device__ __forceinline__ float merge_weight(float mw, float M) { return mw == -INFINITY ? 0.0f : expf(mw - M); }
+
 template <int G, typename KV>
-__global__ void __launch_bounds__(kAttnThreads) attn_partial_kernel(int64_t n, int64_t k, int64_t stride, int splits,
+__global__ void __launch_bounds__(kAttnThreads) attn_cluster_kernel(int64_t n, int64_t k, int64_t stride,
                                                                     const void* __restrict__ q, int q_dtype,
                                                                     const KV* __restrict__ K, const KV* __restrict__ V,
                                                                     const int32_t* __restrict__ idx,
-                                                                    float* __restrict__ part) {
+                                                                    float* __restrict__ out,
+                                                                    uint16_t* __restrict__ out_bf16) {
   __shared__ float s_q[G][kD];
   __shared__ float s_m[kAttnWarps][G], s_l[kAttnWarps][G];
   __shared__ float s_o[kAttnWarps][G][kD];
-  const int r = blockIdx.y, sp = blockIdx.x;
+  __shared__ float c_m[G], c_l[G];  // this CTA's merged partial, read by CTA 0 of the cluster
+  __shared__ float c_o[G][kD];
+  cg::cluster_group cluster = cg::this_cluster();
+  const int crank = int(cluster.block_rank());
+  const int r = blockIdx.y;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const float scale = 0.08838834764831845f;  // 1/sqrt(128)
   for (int i = tid; i < G * kD; i += kAttnThreads)
@@ -68,10 +79,10 @@ __global__ void __launch_bounds__(kAttnThreads) attn_partial_kernel(int64_t n, i
   __syncthreads();
   float4 qv[G];
 #pragma unroll
-  for (int h = 0; h < G; ++h) qv[h] = make_float4(s_q[h][4 * lane], s_q[h][4 * lane + 1], s_q[h][4 * lane + 2],
-                                                 s_q[h][4 * lane + 3]);
-  const int64_t per = (k + splits - 1) / splits;
-  const int64_t i0 = int64_t(sp) * per, i1 = (i0 + per < k) ? i0 + per : k;
+  for (int h = 0; h < G; ++h)
+    qv[h] = make_float4(s_q[h][4 * lane], s_q[h][4 * lane + 1], s_q[h][4 * lane + 2], s_q[h][4 * lane + 3]);
+  const int64_t per = (k + kCluster - 1) / kCluster;
+  const int64_t i0 = int64_t(crank) * per, i1 = (i0 + per < k) ? i0 + per : k;
   const int32_t* ir = idx + int64_t(r) * k;
   const KV* Kr = K + int64_t(r) * n * stride;
   const KV* Vr = V + int64_t(r) * n * stride;
@@ -121,7 +132,7 @@ __global__ void __launch_bounds__(kAttnThreads) attn_partial_kernel(int64_t n, i
 #pragma unroll
       for (int h = 0; h < G; ++h) {
         const float mn = fmaxf(m[h], z[h]);
-        const float corr = expf(m[h] - mn);  // m = -inf first time: exp(-inf) = 0
+        const float corr = expf(m[h] - mn);  // m = -inf the first time: exp(-inf) = 0
         const float p = expf(z[h] - mn);
         l[h] = fmaf(l[h], corr, p);
         o[h].x = fmaf(o[h].x, corr, p * vr[u].x);
@@ -132,7 +143,7 @@ __global__ void __launch_bounds__(kAttnThreads) attn_partial_kernel(int64_t n, i
       }
     }
   }
-  // merge the warps
+  // merge the warps of this CTA
 #pragma unroll
   for (int h = 0; h < G; ++h) {
     if (lane == 0) {
@@ -145,102 +156,94 @@ __global__ void __launch_bounds__(kAttnThreads) attn_partial_kernel(int64_t n, i
     s_o[warp][h][4 * lane + 3] = o[h].w;
   }
   __syncthreads();
-  const int c = tid;  // kAttnThreads == kD
-  for (int h = 0; h < G; ++h) {
+  for (int e = tid; e < G * kD; e += kAttnThreads) {
+    const int h = e / kD, c = e % kD;
     float M = -INFINITY;
 #pragma unroll
     for (int w = 0; w < kAttnWarps; ++w) M = fmaxf(M, s_m[w][h]);
     float L = 0.0f, O = 0.0f;
 #pragma unroll
     for (int w = 0; w < kAttnWarps; ++w) {
-      const float e = (s_m[w][h] == -INFINITY) ? 0.0f : expf(s_m[w][h] - M);
-      L = fmaf(s_l[w][h], e, L);
-      O = fmaf(s_o[w][h][c], e, O);
+      const float wt = merge_weight(s_m[w][h], M);
+      L = fmaf(s_l[w][h], wt, L);
+      O = fmaf(s_o[w][h][c], wt, O);
     }
-    float* pp = part + ((int64_t(r) * splits + sp) * G + h) * kPartStride;
+    c_o[h][c] = O;
     if (c == 0) {
-      pp[0] = M;
-      pp[1] = L;
+      c_m[h] = M;
+      c_l[h] = L;
     }
-    pp[2 + c] = O;
   }
-}
-
-// One CTA per query head: merge the split partials.
-template <int G>
-__global__ void __launch_bounds__(kD) attn_combine_kernel(int splits, const float* __restrict__ part,
-                                                          float* __restrict__ out, uint16_t* __restrict__ out_bf16) {
-  const int qh = blockIdx.x;  // r * G + h
-  const int r = qh / G, h = qh % G;
-  const int c = threadIdx.x;
-  float M = -INFINITY;
-  for (int s = 0; s < splits; ++s) M = fmaxf(M, part[((int64_t(r) * splits + s) * G + h) * kPartStride]);
-  float L = 0.0f, O = 0.0f;
-  for (int s = 0; s < splits; ++s) {
-    const float* pp = part + ((int64_t(r) * splits + s) * G + h) * kPartStride;
-    const float e = (pp[0] == -INFINITY) ? 0.0f : expf(pp[0] - M);
-    L = fmaf(pp[1], e, L);
-    O = fmaf(pp[2 + c], e, O);
+  cluster.sync();  // every CTA's partial is visible to the cluster
+  if (crank == 0) {
+    for (int e = tid; e < G * kD; e += kAttnThreads) {
+      const int h = e / kD, c = e % kD;
+      float M = -INFINITY;
+      for (int rk = 0; rk < kCluster; ++rk) M = fmaxf(M, *cluster.map_shared_rank(&c_m[h], rk));
+      float L = 0.0f, O = 0.0f;
+      for (int rk = 0; rk < kCluster; ++rk) {
+        const float wt = merge_weight(*cluster.map_shared_rank(&c_m[h], rk), M);
+        L = fmaf(*cluster.map_shared_rank(&c_l[h], rk), wt, L);
+        O = fmaf(*cluster.map_shared_rank(&c_o[h][c], rk), wt, O);
+      }
+      const float v = L > 0.0f ? O / L : 0.0f;
+      const int64_t qh = int64_t(r) * G + h;
+      if (out) out[qh * kD + c] = v;
+      if (out_bf16) {
+        const __nv_bfloat16 b = __float2bfloat16_rn(v);
+        out_bf16[qh * kD + c] = *reinterpret_cast<const uint16_t*>(&b);
+      }
+    }
   }
-  const float v = L > 0.0f ? O / L : 0.0f;
-  if (out) out[int64_t(qh) * kD + c] = v;
-  if (out_bf16) {
-    const __nv_bfloat16 b = __float2bfloat16_rn(v);
-    out_bf16[int64_t(qh) * kD + c] = *reinterpret_cast<const uint16_t*>(&b);
-  }
-}
-
-int attn_splits(int rows, int64_t k) {
-  const int64_t want = (2 * int64_t(num_sms()) + rows - 1) / rows;
-  const int64_t maxs = (k + kMinPerSplit - 1) / kMinPerSplit;
-  int64_t s = want < maxs ? want : maxs;
-  return int(s < 1 ? 1 : s);
+  cluster.sync();  // keep this CTA's shared memory alive until CTA 0 has read it
 }
 
 template <int G, typename KV>
 cudaError_t launch_attn_t(int rows, int64_t n, int64_t k, const void* q, int q_dtype, const void* K, const void* V,
-                          int64_t stride,
-                          const int32_t* idx, float* out, uint16_t* out_bf16, float* part, cudaStream_t st) {
-  const int splits = attn_splits(rows, k);
-  attn_partial_kernel<G, KV><<<dim3(splits, rows), kAttnThreads, 0, st>>>(
-      n, k, stride, splits, q, q_dtype, reinterpret_cast<const KV*>(K), reinterpret_cast<const KV*>(V), idx, part);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  attn_combine_kernel<G><<<rows * G, kD, 0, st>>>(splits, part, out, out_bf16);
-  return cudaGetLastError();
+                          int64_t stride, const int32_t* idx, float* out, uint16_t* out_bf16, cudaStream_t st) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(kCluster, unsigned(rows), 1);
+  cfg.blockDim = dim3(kAttnThreads, 1, 1);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = kCluster;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, attn_cluster_kernel<G, KV>, n, k, stride, q, q_dtype,
+                            reinterpret_cast<const KV*>(K), reinterpret_cast<const KV*>(V), idx, out, out_bf16);
 }
 
 template <int G>
 cudaError_t launch_attn_g(int rows, int64_t n, int64_t k, const void* q, int q_dtype, const void* K, const void* V,
-                          int kv_dtype, int64_t stride, const int32_t* idx, float* out, uint16_t* out_bf16, float* part,
+                          int kv_dtype, int64_t stride, const int32_t* idx, float* out, uint16_t* out_bf16,
                           cudaStream_t st) {
   if (kv_dtype == FATHOM_F32)
-    return launch_attn_t<G, float>(rows, n, k, q, q_dtype, K, V, stride, idx, out, out_bf16, part, st);
+    return launch_attn_t<G, float>(rows, n, k, q, q_dtype, K, V, stride, idx, out, out_bf16, st);
   if (kv_dtype == FATHOM_F16)
-    return launch_attn_t<G, __half>(rows, n, k, q, q_dtype, K, V, stride, idx, out, out_bf16, part, st);
-  return launch_attn_t<G, __nv_bfloat16>(rows, n, k, q, q_dtype, K, V, stride, idx, out, out_bf16, part, st);
+    return launch_attn_t<G, __half>(rows, n, k, q, q_dtype, K, V, stride, idx, out, out_bf16, st);
+  return launch_attn_t<G, __nv_bfloat16>(rows, n, k, q, q_dtype, K, V, stride, idx, out, out_bf16, st);
 }
 
 }  // namespace
 
-size_t attn_ws_bytes(int rows, int group, int64_t k) {
-  const int64_t maxs = (k + kMinPerSplit - 1) / kMinPerSplit;
-  return size_t(rows) * size_t(maxs) * group * kPartStride * sizeof(float) + 256;
-}
+size_t attn_ws_bytes(int, int, int64_t) { return 256; }
 
 cudaError_t launch_attn(int rows, int group, int64_t n, int64_t k, const void* q, int q_dtype, const void* K,
-                        const void* V, int kv_dtype, int64_t kv_stride, const int32_t* idx, float* out, uint16_t* out_bf16, void* ws,
-                        cudaStream_t st) {
-  float* part = reinterpret_cast<float*>(ws);
+                        const void* V, int kv_dtype, int64_t kv_stride, const int32_t* idx, float* out,
+                        uint16_t* out_bf16, void* /*ws*/, cudaStream_t st) {
   switch (group) {
-    case 1: return launch_attn_g<1>(rows, n, k, q, q_dtype, K, V, kv_dtype, kv_stride, idx, out, out_bf16, part, st);
-    case 2: return launch_attn_g<2>(rows, n, k, q, q_dtype, K, V, kv_dtype, kv_stride, idx, out, out_bf16, part, st);
-    case 3: return launch_attn_g<3>(rows, n, k, q, q_dtype, K, V, kv_dtype, kv_stride, idx, out, out_bf16, part, st);
-    case 4: return launch_attn_g<4>(rows, n, k, q, q_dtype, K, V, kv_dtype, kv_stride, idx, out, out_bf16, part, st);
-    case 5: return launch_attn_g<5>(rows, n, k, q, q_dtype, K, V, kv_dtype, kv_stride, idx, out, out_bf16, part, st);
-    case 6: return launch_attn_g<6>(rows, n, k, q, q_dtype, K, V, kv_dtype, kv_stride, idx, out, out_bf16, part, st);
-    case 7: return launch_attn_g<7>(rows, n, k, q, q_dtype, K, V, kv_dtype, kv_stride, idx, out, out_bf16, part, st);
-    case 8: return launch_attn_g<8>(rows, n, k, q, q_dtype, K, V, kv_dtype, kv_stride, idx, out, out_bf16, part, st);
+    case 1: return launch_attn_g<1>(rows, n, k, q, q_dtype, K, V, kv_dtype, kv_stride, idx, out, out_bf16, st);
+    case 2: return launch_attn_g<2>(rows, n, k, q, q_dtype, K, V, kv_dtype, kv_stride, idx, out, out_bf16, st);
+    case 3: return launch_attn_g<3>(rows, n, k, q, q_dtype, K, V, kv_dtype, kv_stride, idx, out, out_bf16, st);
+    case 4: return launch_attn_g<4>(rows, n, k, q, q_dtype, K, V, kv_dtype, kv_stride, idx, out, out_bf16, st);
+    case 5: return launch_attn_g<5>(rows, n, k, q, q_dtype, K, V, kv_dtype, kv_stride, idx, out, out_bf16, st);
+    case 6: return launch_attn_g<6>(rows, n, k, q, q_dtype, K, V, kv_dtype, kv_stride, idx, out, out_bf16, st);
+    case 7: return launch_attn_g<7>(rows, n, k, q, q_dtype, K, V, kv_dtype, kv_stride, idx, out, out_bf16, st);
+    case 8: return launch_attn_g<8>(rows, n, k, q, q_dtype, K, V, kv_dtype, kv_stride, idx, out, out_bf16, st);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -274,17 +277,14 @@ int fathom_sparse_attn(int rows, int group, int64_t n, int64_t k, const void* q,
   FATHOM_TRY(device_view(idx, "idx", &dI));
   FATHOM_TRY(device_view(out, "out", &dO, true));
   FATHOM_TRY(device_view(out_bf16, "out_bf16", &dB, true));
-  FATHOM_TRY(device_view(workspace, "workspace", &dW));
-  if (reinterpret_cast<uintptr_t>(dW) & 255) return set_error(FATHOM_EINVAL, "workspace must be 256-byte aligned");
+  FATHOM_TRY(device_view(workspace, "workspace", &dW, true));
   if (!dO && !dB) return set_error(FATHOM_EINVAL, "out and out_bf16 are both NULL");
-  if (ws_bytes < attn_ws_bytes(rows, group, k))
-    return set_error(FATHOM_ENOMEM, "workspace %zu < %zu bytes", ws_bytes, attn_ws_bytes(rows, group, k));
+  (void)ws_bytes;  // the clustered kernel keeps its partials on chip
   const size_t al = kv_dtype == FATHOM_F32 ? 16 : 8;
   if ((reinterpret_cast<uintptr_t>(dK) % al) || (reinterpret_cast<uintptr_t>(dV) % al))
     return set_error(FATHOM_EINVAL, "K and V must be %zu-byte aligned", al);
   FATHOM_TRY_CUDA(launch_attn(rows, group, n, k, dq, q_dtype, dK, dV, kv_dtype, kv_stride, (const int32_t*)dI,
-                              (float*)dO,
-                              (uint16_t*)dB, const_cast<void*>(dW), as_stream(stream)));
+                              (float*)dO, (uint16_t*)dB, const_cast<void*>(dW), as_stream(stream)));
   return FATHOM_OK;
 }
 

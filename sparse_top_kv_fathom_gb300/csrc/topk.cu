@@ -24,7 +24,8 @@ namespace fathom {
 namespace {
 
 constexpr int kFinThreads = 1024;
-constexpr int kSortMax = 8192;  // largest k sorted in shared memory
+constexpr int kSortMax = 8192;    // largest k sorted in shared memory
+constexpr int kCandSmem = 16384;  // candidates staged in shared memory by the final select
 constexpr int kPassThreads = 256;
 constexpr int kPassItems = 16;  // items per thread in the histogram / compaction passes
 
@@ -184,30 +185,67 @@ __global__ void __launch_bounds__(kPassThreads) topk_compact_kernel(int64_t n, i
                                                                     int32_t* __restrict__ sure,
                                                                     uint32_t* __restrict__ cand_key,
                                                                     int32_t* __restrict__ cand_idx) {
+  // Gather this tile's sure winners and candidates in shared memory first, then
+  // reserve space in the row's global lists with one atomic per list per CTA.
+  constexpr int kTileItems = kPassThreads * kPassItems;
+  __shared__ int32_t s_si[kTileItems];
+  __shared__ uint32_t s_ck[kTileItems];
+  __shared__ int32_t s_ci[kTileItems];
+  __shared__ int32_t s_ns, s_nc, s_bs, s_bc;
   const int r = blockIdx.y;
   const uint32_t b1 = state[r].b1;
-  const int64_t t0 = int64_t(blockIdx.x) * kPassThreads * kPassItems;
+  if (threadIdx.x == 0) s_ns = s_nc = 0;
+  __syncthreads();
+  const int64_t t0 = int64_t(blockIdx.x) * kTileItems;
   const float* s = scores + int64_t(r) * n;
+  float sv[kPassItems];  // all loads in flight before any is used
+#pragma unroll
+  for (int i = 0; i < kPassItems; ++i) {
+    const int64_t t = t0 + int64_t(i) * kPassThreads + threadIdx.x;
+    sv[i] = t < n ? __ldg(s + t) : 0.0f;
+  }
+#pragma unroll
   for (int i = 0; i < kPassItems; ++i) {
     const int64_t t = t0 + int64_t(i) * kPassThreads + threadIdx.x;
     uint32_t key = 0u;
-    if (t < n) key = score_key(s[t]);
+    if (t < n) key = score_key(sv[i]);
     const uint32_t bin = key >> (32 - kHistBits);
     const bool is_sure = (t < n) && bin > b1;
     const bool is_cand = (t < n) && bin == b1;
     int slot;
-    warp_append(is_sure, &state[r].sure_cnt, &slot);
-    if (is_sure && slot < k) sure[int64_t(r) * k + slot] = int32_t(t);
-    warp_append(is_cand, &state[r].cand_cnt, &slot);
-    if (is_cand && slot < cap) {
-      cand_key[int64_t(r) * cap + slot] = key;
-      cand_idx[int64_t(r) * cap + slot] = int32_t(t);
+    warp_append(is_sure, &s_ns, &slot);
+    if (is_sure) s_si[slot] = int32_t(t);
+    warp_append(is_cand, &s_nc, &slot);
+    if (is_cand) {
+      s_ck[slot] = key;
+      s_ci[slot] = int32_t(t);
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    s_bs = s_ns ? atomicAdd(&state[r].sure_cnt, s_ns) : 0;
+    s_bc = s_nc ? atomicAdd(&state[r].cand_cnt, s_nc) : 0;
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < s_ns; i += kPassThreads) {
+    const int64_t slot = int64_t(s_bs) + i;
+    if (slot < k) sure[int64_t(r) * k + slot] = s_si[i];
+  }
+  for (int i = threadIdx.x; i < s_nc; i += kPassThreads) {
+    const int64_t slot = int64_t(s_bc) + i;
+    if (slot < cap) {
+      cand_key[int64_t(r) * cap + slot] = s_ck[i];
+      cand_idx[int64_t(r) * cap + slot] = s_ci[i];
     }
   }
 }
 
 // Bitonic sort (ascending) of s[0..m) in shared memory, m a power of two.
+// With one compare-exchange pair per thread (m/2 == blockDim.x), a stage of
+// stride <= 32 only touches the 64 elements owned by the thread's warp, so it
+// needs a warp barrier, not a block barrier.
 __device__ void bitonic_sort(int32_t* s, int m) {
+  const bool pair_per_thread = (m >> 1) == int(blockDim.x);
   for (int size = 2; size <= m; size <<= 1) {
     for (int stride = size >> 1; stride > 0; stride >>= 1) {
       for (int i = threadIdx.x; i < (m >> 1); i += blockDim.x) {
@@ -220,7 +258,9 @@ __device__ void bitonic_sort(int32_t* s, int m) {
           s[hi] = a;
         }
       }
-      __syncthreads();
+      const int next = stride > 1 ? stride >> 1 : size;  // stride of the next stage
+      if (pair_per_thread && stride <= 32 && next <= 32) __syncwarp();
+      else __syncthreads();
     }
   }
 }
@@ -324,7 +364,10 @@ __global__ void __launch_bounds__(kFinThreads) topk_final_kernel(int64_t n, int6
                                                                  const uint32_t* __restrict__ cand_key,
                                                                  const int32_t* __restrict__ cand_idx,
                                                                  int32_t* __restrict__ idx, float* __restrict__ vals) {
-  extern __shared__ int32_t s_sel[];  // kSortMax entries
+  extern __shared__ int32_t s_dyn[];  // kSortMax sort entries, then kCandSmem keys and indices
+  int32_t* s_sel = s_dyn;
+  uint32_t* s_ck = reinterpret_cast<uint32_t*>(s_dyn + kSortMax);
+  int32_t* s_ci = s_dyn + kSortMax + kCandSmem;
   __shared__ uint32_t h[kFinThreads];
   __shared__ int s_out[2];
   __shared__ int s_fill;
@@ -341,6 +384,30 @@ __global__ void __launch_bounds__(kFinThreads) topk_final_kernel(int64_t n, int6
   }
   const uint32_t* ck = cand_key + int64_t(r) * cap;
   const int32_t* ci = cand_idx + int64_t(r) * cap;
+  if (m <= kCandSmem) {  // stage the candidates once, many loads in flight per thread
+    constexpr int kBatch = 8;
+    for (int base = 0; base < m; base += kFinThreads * kBatch) {
+      uint32_t kk[kBatch];
+      int32_t ii[kBatch];
+#pragma unroll
+      for (int b = 0; b < kBatch; ++b) {
+        const int i = base + b * kFinThreads + tid;
+        kk[b] = i < m ? ck[i] : 0u;
+        ii[b] = i < m ? ci[i] : 0;
+      }
+#pragma unroll
+      for (int b = 0; b < kBatch; ++b) {
+        const int i = base + b * kFinThreads + tid;
+        if (i < m) {
+          s_ck[i] = kk[b];
+          s_ci[i] = ii[b];
+        }
+      }
+    }
+    __syncthreads();
+    ck = s_ck;
+    ci = s_ci;
+  }
   int need = int(k) - st.above;  // >= 1
   // --- digits 2 and 3 (bits 19..10 and 9..0) among the candidates
   uint32_t prefix = st.b1 << 20, pmask = 0xFFF00000u;
@@ -469,7 +536,7 @@ cudaError_t launch_topk(int rows, int64_t n, int64_t k, const float* scores, int
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   topk_compact_kernel<<<pgrid, kPassThreads, 0, st>>>(n, k, w.cap, scores, w.state, w.sure, w.cand_key, w.cand_idx);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  const size_t smem = kSortMax * sizeof(int32_t);
+  const size_t smem = (kSortMax + 2 * kCandSmem) * sizeof(int32_t);
   static bool attr_set = false;
   if (!attr_set) {
     e = cudaFuncSetAttribute(topk_final_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
