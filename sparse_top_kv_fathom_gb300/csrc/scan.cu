@@ -63,11 +63,14 @@ __device__ __forceinline__ uint32_t nibble_word(uint32_t w0, uint32_t w1, uint32
 }
 
 // Mixed-precision FMA (sm_100+): fp16 multiplicands, fp32 addend and result,
-// one rounding.
-__device__ __forceinline__ float fma_f16_f32(uint16_t a, uint16_t b, float c) {
-  float d;
-  asm("fma.rn.f32.f16 %0, %1, %2, %3;" : "=f"(d) : "h"(a), "h"(b), "f"(c));
-  return d;
+// one rounding.  Both fp16 halves of h2 against the same a and c.
+__device__ __forceinline__ float2 fma_f16x2_f32(uint16_t a, uint32_t h2, float c) {
+  float d0, d1;
+  asm("{\n\t.reg .f16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+      "fma.rn.f32.f16 %0, %3, lo, %4;\n\tfma.rn.f32.f16 %1, %3, hi, %4;\n\t}"
+      : "=f"(d0), "=f"(d1)
+      : "r"(h2), "h"(a), "f"(c));
+  return make_float2(d0, d1);
 }
 
 // The prefixes of tokens 4M+K (nibble M of o_K) and 4M+16+K (nibble M+4) as two
@@ -82,7 +85,7 @@ __device__ __forceinline__ uint32_t prefix_halves(uint32_t o, uint32_t mask6) {
 // x = delta*(16 + u) + lo' = lo + delta*(u + (m-1)/2) in one rounding per token,
 // then acc += qbar * x for the two tokens at once (packed f32x2 FMA).
 __device__ __forceinline__ void accumulate_halves(float2& acc, uint32_t h2, uint16_t dl16, float lop, float2 q2) {
-  const float2 x = make_float2(fma_f16_f32(dl16, uint16_t(h2 & 0xFFFFu), lop), fma_f16_f32(dl16, uint16_t(h2 >> 16), lop));
+  const float2 x = fma_f16x2_f32(dl16, h2, lop);
   acc = __ffma2_rn(q2, x, acc);
 }
 
