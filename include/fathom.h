@@ -153,6 +153,25 @@ int fathom_topk_workspace_bytes(int rows, int64_t n, int64_t k, size_t* bytes);
 int fathom_topk(int rows, int64_t n, int64_t k, const float* scores, int32_t* idx, float* vals, void* workspace,
                 size_t ws_bytes, void* stream);
 
+/* fathom_topk without a workspace, for callers that can neither pass device
+ * scratch nor let the library allocate any (a serving loop that must never
+ * call cudaMalloc, which can synchronise the device; a process whose device
+ * memory is reserved up front by another allocator; C code with no device
+ * allocator).  The pages have no counterpart: this is a deployment variant.
+ * Same arguments and results as fathom_topk.  Its scratch is one fixed array
+ * of FATHOM_TOPK_NOALLOC_SCRATCH_BYTES in device memory, present on every GPU
+ * that loads the library until the process exits:
+ *   - if (rows, n, k) needs more scratch than that (fathom_topk_workspace_bytes
+ *     tells how much), the call fails with EINVAL and launches nothing;
+ *   - the first call on a device looks up the array's address with that device
+ *     current; make it before any stream capture begins;
+ *   - all calls on a device share the array, so calls that can overlap on the
+ *     GPU (unordered streams) race; order them on one stream.
+ * Nothing is allocated or freed. */
+#define FATHOM_TOPK_NOALLOC_SCRATCH_BYTES (8u << 20)
+int fathom_topk_noalloc(int rows, int64_t n, int64_t k, const float* scores, int32_t* idx, float* vals,
+                        void* stream);
+
 /* Workspace bytes of fathom_sparse_attn (host-only). */
 int fathom_sparse_attn_workspace_bytes(int rows, int group, int64_t k, size_t* bytes);
 

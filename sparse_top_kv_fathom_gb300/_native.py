@@ -44,6 +44,7 @@ SIGNATURES = {
     "fathom_scan": ([IDP, P, P, P, P, P, P], I32),
     "fathom_topk_workspace_bytes": ([I32, I64, I64, SZP], I32),
     "fathom_topk": ([I32, I64, I64, P, P, P, P, SZ, P], I32),
+    "fathom_topk_noalloc": ([I32, I64, I64, P, P, P, P], I32),
     "fathom_sparse_attn_workspace_bytes": ([I32, I32, I64, SZP], I32),
     "fathom_sparse_attn": ([I32, I32, I64, I64, P, I32, P, P, I32, I64, P, P, P, P, SZ, P], I32),
     "fathom_decode_step_workspace_bytes": ([ctypes.POINTER(StepDesc), SZP], I32),

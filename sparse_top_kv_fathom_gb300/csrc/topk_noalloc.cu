@@ -1,0 +1,78 @@
+// fathom_topk_noalloc: the top-k selection of fathom_topk for callers that
+// cannot hand the library scratch memory and must not have it allocate any.
+//
+// Some callers have no way to provide device scratch: a serving loop that must
+// never call cudaMalloc (it can synchronise the whole device and stall every
+// stream at the worst moment), a process whose device memory is entirely
+// reserved up front by another allocator, or plain C code with no device
+// allocator of its own.  For them this entry point keeps its scratch in a
+// fixed, file-scope device array that exists from the moment the library is
+// loaded until the process exits, on every GPU that loads the library.
+//
+// Contract (also in include/fathom.h):
+//   - the caller still owns and passes scores, idx and vals;
+//   - the scratch needed by (rows, n, k) must fit FATHOM_TOPK_NOALLOC_SCRATCH_BYTES,
+//     otherwise the call fails with FATHOM_EINVAL before launching anything;
+//   - the first call on a device looks up the array's device address with that
+//     device current (cudaGetSymbolAddress) and caches it; make that first call
+//     before starting any stream capture;
+//   - every call on a device shares the one array: calls whose work overlaps on
+//     the GPU (different streams, no ordering between them) race on it.  The
+//     histogram that must start at zero is cleared by each call; the rest is
+//     fully rewritten before it is read.
+// No cudaMalloc, cudaFree or allocating library routine is called.
+#include <mutex>
+
+#include "common.cuh"
+
+namespace fathom {
+namespace {
+
+static __device__ __align__(256) unsigned char g_topk_scratch[FATHOM_TOPK_NOALLOC_SCRATCH_BYTES];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+void* g_scratch_ptr[kMaxDevices] = {};
+
+// Device address of g_topk_scratch on the current device (looked up once per device).
+int scratch_on_current_device(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_check(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return set_error(FATHOM_EINVAL, "device ordinal %d unsupported", dev);
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (!g_scratch_ptr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_topk_scratch);
+    if (e != cudaSuccess) return cuda_check(e, "cudaGetSymbolAddress(g_topk_scratch)");
+    g_scratch_ptr[dev] = p;
+  }
+  *out = g_scratch_ptr[dev];
+  return FATHOM_OK;
+}
+
+}  // namespace
+}  // namespace fathom
+
+using namespace fathom;
+
+extern "C" int fathom_topk_noalloc(int rows, int64_t n, int64_t k, const float* scores, int32_t* idx, float* vals,
+                                   void* stream) {
+  clear_error();
+  if (rows < 1 || rows > 65535 || n < 1 || k < 1 || n > 0x7fffffff || k > 0x7fffffff)
+    return set_error(FATHOM_EINVAL, "rows, n, k out of range");
+  const size_t need = k < n ? topk_ws_bytes(rows, n, k) : 0;
+  if (need > size_t(FATHOM_TOPK_NOALLOC_SCRATCH_BYTES))
+    return set_error(FATHOM_EINVAL,
+                     "fathom_topk_noalloc: rows=%d n=%lld k=%lld need %zu bytes of scratch, more than the fixed "
+                     "%zu; use fathom_topk with a workspace",
+                     rows, (long long)n, (long long)k, need, size_t(FATHOM_TOPK_NOALLOC_SCRATCH_BYTES));
+  const void *dS, *dI, *dV;
+  FATHOM_TRY(device_view(scores, "scores", &dS));
+  FATHOM_TRY(device_view(idx, "idx", &dI));
+  FATHOM_TRY(device_view(vals, "vals", &dV, true));
+  void* ws = nullptr;
+  FATHOM_TRY(scratch_on_current_device(&ws));
+  FATHOM_TRY_CUDA(launch_topk(rows, n, k, (const float*)dS, (int32_t*)dI, (float*)dV, ws, false, as_stream(stream)));
+  return FATHOM_OK;
+}
