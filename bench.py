@@ -337,6 +337,30 @@ def captured_traffic(residency, w, budget):
     return r["bytes_per_launch"]
 
 
+def captured_issue_rate(residency, w, budget, ms_per_launch):
+    """Instruction-issue roofline of the scan (the bound with the index in HBM): warp
+    instructions of one launch (committed ncu capture, same kernel source and workload) per
+    second of the live launch time, against 4 issues per clock per SM at the maximum SM clock."""
+    import hashlib
+    try:
+        rec = json.load(open(TRAFFIC_RECORD))
+        src = hashlib.sha256(open(SCAN_SOURCE, "rb").read()).hexdigest()
+    except (OSError, ValueError):
+        return None
+    r = rec.get(residency)
+    if rec.get("scan_source_sha256") != src or not r or "warp_instructions" not in r or r.get("n") != w.n \
+            or r.get("budget") != budget:
+        return None
+    props = torch.cuda.get_device_properties(0)
+    sm_mhz = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))).get("sm_max_mhz", 2070.0) \
+        if os.path.exists(os.path.join(ROOT, "MEASURED_PEAKS.json")) else 2070.0
+    peak = 4.0 * props.multi_processor_count * sm_mhz * 1e6
+    achieved = r["warp_instructions"] / (ms_per_launch * 1e-3)
+    return {"bound": "issue", "achieved": achieved, "peak": peak, "unit": "warp instructions/s",
+            "frac": achieved / peak, "kernel": "scan_kernel",
+            "source": "smsp__inst_executed.sum of one launch (ncu) / live launch time"}
+
+
 def link_peak(log):
     """Host-link streaming-read peak: zero-copy 16 B loads over pinned host memory, best of several shapes."""
     import sparse_top_kv_fathom_gb300 as F
@@ -554,7 +578,9 @@ def main():
                                              "traffic": captured_traffic("device", w, args.budget),
                                              "algorithmic_bytes_per_launch": d["scan_algo_bytes_per_layer"],
                                              "kernel": "scan_kernel",
-                                             "peak_source": "MEASURED_PEAKS.json hbm_gbs (copy)"}}
+                                             "peak_source": "MEASURED_PEAKS.json hbm_gbs (copy)"},
+                                "roofline_issue": captured_issue_rate("device", w, args.budget,
+                                                                      d["scan_ms_per_layer"])}
     if comparator:
         line["comparator"] = {"index": "fixed 136-bit (32 channels x 4 bit + 8-bit scale)",
                               "ms_per_step": p.get("comparator_ms_per_step"),

@@ -4,12 +4,12 @@
 // relevance; "The first fix": attend over just the k winners).  Every query
 // head of a KV head uses its own q with that KV head's winner set.
 //
-// GPU form: one thread-block cluster of kCluster CTAs per KV head.  Each CTA
+// GPU form: one thread-block cluster of 16 (or the portable 8) CTAs per KV head.  Each CTA
 // takes a slice of the winners; each warp gathers whole K and V rows (a lane
 // holds 4 channels: 8 contiguous bytes of a 16-bit row), several winners in
 // flight per warp, reduces the group's dot products with shuffles and keeps an
 // online softmax (running max, sum and weighted V).  The CTA merges its warps
-// in shared memory; then CTA 0 of the cluster merges the kCluster partials by
+// in shared memory; then CTA 0 of the cluster merges the cluster's partials by
 // reading the other CTAs' shared memory (distributed shared memory) and writes
 // the output: one launch, no partials in global memory.  The K/V rows may sit
 // in HBM or in pinned host memory.
@@ -22,10 +22,12 @@ namespace cg = cooperative_groups;
 namespace fathom {
 namespace {
 
-constexpr int kAttnThreads = 256;
-constexpr int kAttnWarps = kAttnThreads / 32;
-constexpr int kCluster = 8;  // CTAs per KV head (portable cluster size)
-constexpr int kUnroll = 4;   // winners in flight per warp
+constexpr int kClusterMax = 16;  // CTAs per KV head when non-portable clusters are allowed, else 8
+constexpr int kUnroll = 4;       // winners in flight per warp
+
+// threads per CTA: 512 while the per-thread state (G heads) stays small, else 256
+template <int G>
+constexpr int attn_threads() { return G <= 4 ? 512 : 256; }
 
 template <typename T>
 struct Row4;
@@ -57,31 +59,33 @@ struct Row4<__nv_bfloat16> {
 // weight of a partial with running max mw when merged under the overall max M
 __device__ __forceinline__ float merge_weight(float mw, float M) { return mw == -INFINITY ? 0.0f : expf(mw - M); }
 
-template <int G, typename KV>
-__global__ void __launch_bounds__(kAttnThreads) attn_cluster_kernel(int64_t n, int64_t k, int64_t stride,
+template <int G, typename KV, int T = attn_threads<G>()>
+__global__ void __launch_bounds__(T) attn_cluster_kernel(int64_t n, int64_t k, int64_t stride,
                                                                     const void* __restrict__ q, int q_dtype,
                                                                     const KV* __restrict__ K, const KV* __restrict__ V,
                                                                     const int32_t* __restrict__ idx,
                                                                     float* __restrict__ out,
                                                                     uint16_t* __restrict__ out_bf16) {
   __shared__ float s_q[G][kD];
-  __shared__ float s_m[kAttnWarps][G], s_l[kAttnWarps][G];
-  __shared__ float s_o[kAttnWarps][G][kD];
+  constexpr int kWarps = T / 32;
+  __shared__ float s_m[kWarps][G], s_l[kWarps][G];
+  __shared__ float s_o[kWarps][G][kD];
   __shared__ float c_m[G], c_l[G];  // this CTA's merged partial, read by CTA 0 of the cluster
   __shared__ float c_o[G][kD];
   cg::cluster_group cluster = cg::this_cluster();
   const int crank = int(cluster.block_rank());
+  const int csize = int(cluster.num_blocks());
   const int r = blockIdx.y;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const float scale = 0.08838834764831845f;  // 1/sqrt(128)
-  for (int i = tid; i < G * kD; i += kAttnThreads)
+  for (int i = tid; i < G * kD; i += T)
     s_q[i / kD][i % kD] = load_as_float(q, int64_t(r) * G * kD + i, q_dtype) * scale;
   __syncthreads();
   float4 qv[G];
 #pragma unroll
   for (int h = 0; h < G; ++h)
     qv[h] = make_float4(s_q[h][4 * lane], s_q[h][4 * lane + 1], s_q[h][4 * lane + 2], s_q[h][4 * lane + 3]);
-  const int64_t per = (k + kCluster - 1) / kCluster;
+  const int64_t per = (k + csize - 1) / csize;
   const int64_t i0 = int64_t(crank) * per, i1 = (i0 + per < k) ? i0 + per : k;
   const int32_t* ir = idx + int64_t(r) * k;
   const KV* Kr = K + int64_t(r) * n * stride;
@@ -95,7 +99,7 @@ __global__ void __launch_bounds__(kAttnThreads) attn_cluster_kernel(int64_t n, i
     l[h] = 0.0f;
     o[h] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
-  for (int64_t base = i0 + int64_t(warp) * kUnroll; base < i1; base += int64_t(kAttnWarps) * kUnroll) {
+  for (int64_t base = i0 + int64_t(warp) * kUnroll; base < i1; base += int64_t(kWarps) * kUnroll) {
     int32_t t[kUnroll];
     float4 kr[kUnroll], vr[kUnroll];
 #pragma unroll
@@ -156,14 +160,14 @@ __global__ void __launch_bounds__(kAttnThreads) attn_cluster_kernel(int64_t n, i
     s_o[warp][h][4 * lane + 3] = o[h].w;
   }
   __syncthreads();
-  for (int e = tid; e < G * kD; e += kAttnThreads) {
+  for (int e = tid; e < G * kD; e += T) {
     const int h = e / kD, c = e % kD;
     float M = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < kAttnWarps; ++w) M = fmaxf(M, s_m[w][h]);
+    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, s_m[w][h]);
     float L = 0.0f, O = 0.0f;
 #pragma unroll
-    for (int w = 0; w < kAttnWarps; ++w) {
+    for (int w = 0; w < kWarps; ++w) {
       const float wt = merge_weight(s_m[w][h], M);
       L = fmaf(s_l[w][h], wt, L);
       O = fmaf(s_o[w][h][c], wt, O);
@@ -176,12 +180,12 @@ __global__ void __launch_bounds__(kAttnThreads) attn_cluster_kernel(int64_t n, i
   }
   cluster.sync();  // every CTA's partial is visible to the cluster
   if (crank == 0) {
-    for (int e = tid; e < G * kD; e += kAttnThreads) {
+    for (int e = tid; e < G * kD; e += T) {
       const int h = e / kD, c = e % kD;
       float M = -INFINITY;
-      for (int rk = 0; rk < kCluster; ++rk) M = fmaxf(M, *cluster.map_shared_rank(&c_m[h], rk));
+      for (int rk = 0; rk < csize; ++rk) M = fmaxf(M, *cluster.map_shared_rank(&c_m[h], rk));
       float L = 0.0f, O = 0.0f;
-      for (int rk = 0; rk < kCluster; ++rk) {
+      for (int rk = 0; rk < csize; ++rk) {
         const float wt = merge_weight(*cluster.map_shared_rank(&c_m[h], rk), M);
         L = fmaf(*cluster.map_shared_rank(&c_l[h], rk), wt, L);
         O = fmaf(*cluster.map_shared_rank(&c_o[h][c], rk), wt, O);
@@ -201,20 +205,34 @@ __global__ void __launch_bounds__(kAttnThreads) attn_cluster_kernel(int64_t n, i
 template <int G, typename KV>
 cudaError_t launch_attn_t(int rows, int64_t n, int64_t k, const void* q, int q_dtype, const void* K, const void* V,
                           int64_t stride, const int32_t* idx, float* out, uint16_t* out_bf16, cudaStream_t st) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(kCluster, unsigned(rows), 1);
-  cfg.blockDim = dim3(kAttnThreads, 1, 1);
-  cfg.dynamicSmemBytes = 0;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = kCluster;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, attn_cluster_kernel<G, KV>, n, k, stride, q, q_dtype,
-                            reinterpret_cast<const KV*>(K), reinterpret_cast<const KV*>(V), idx, out, out_bf16);
+  auto kern = attn_cluster_kernel<G, KV>;
+  // 16-CTA clusters need an opt-in per kernel; fall back to the portable 8 if it is refused
+  static int cluster = 0;
+  if (cluster == 0) {
+    cluster = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess
+                  ? kClusterMax
+                  : 8;
+    cudaGetLastError();
+  }
+  for (;;) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(unsigned(cluster), unsigned(rows), 1);
+    cfg.blockDim = dim3(attn_threads<G>(), 1, 1);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = unsigned(cluster);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, n, k, stride, q, q_dtype, reinterpret_cast<const KV*>(K),
+                                             reinterpret_cast<const KV*>(V), idx, out, out_bf16);
+    if (e == cudaSuccess || cluster == 8) return e;
+    cudaGetLastError();  // the larger cluster could not be scheduled: use the portable size from now on
+    cluster = 8;
+  }
 }
 
 template <int G>
