@@ -9,6 +9,7 @@ this module only marshals numpy arrays into it.
 Function map (each C function cites the page passage it follows):
   pack            per-block min/max 4-bit codes -> MSB-first bit planes + var
   allocate        reverse water-filling (threshold binary search)
+  allocate_sparq  the SparQ-style comparator: full depth on the r largest |qbar|
   waterfill       the same for one row of weights, any channel count
   scan            fp64 score of every key from the chosen plane prefixes
   topk_f32/_f64   k largest, ties to the lower index, ascending output
@@ -48,6 +49,10 @@ def lib():
         L.oracle_waterfill.restype = i32
         L.oracle_allocate.argtypes = [i32, i32, P, P, P, P, P]
         L.oracle_allocate.restype = i32
+        L.oracle_allocate_heads.argtypes = [i32, i32, P, P, P, P]
+        L.oracle_allocate_heads.restype = i32
+        L.oracle_allocate_sparq.argtypes = [i32, i32, P, i32, P, P]
+        L.oracle_allocate_sparq.restype = i32
         L.oracle_scan.argtypes = [i64, i32, i64, P, P, P, P, P, P]
         L.oracle_scan.restype = None
         L.oracle_topk_f32.argtypes = [i64, i32, i64, P, P]
@@ -119,6 +124,53 @@ def allocate(q, var, budget, group):
     qbar = np.zeros((rows, D), np.float32)
     if lib().oracle_allocate(rows, group, _p(q), _p(var), _p(b), _p(bits), _p(qbar)):
         raise ValueError("oracle_allocate: invalid input")
+    return bits, qbar
+
+
+def allocate_heads(q, var, budget, group):
+    """Per-query-head allocation: bits [rows*group][128], each head water-filling the row's
+    budget with its own q_h (the alternative GQA reading)."""
+    q = _c(q, np.float32)
+    var = _c(var, np.float32)
+    rows = var.shape[0]
+    b = _c(np.broadcast_to(np.asarray(budget, np.int32), (rows,)), np.int32)
+    bits = np.zeros((rows * group, D), np.uint8)
+    if lib().oracle_allocate_heads(rows, group, _p(q), _p(var), _p(b), _p(bits)):
+        raise ValueError("oracle_allocate_heads: invalid input")
+    return bits
+
+
+def scan_heads(planes, meta, bits_heads, q, n, S, group, mode):
+    """Scores under per-head allocations: every query head h of KV row r scores every key with
+    its own depths bits_heads[r*group+h] and its own q_h (the oracle scan of row r, once per
+    head).  mode "per_head": scores [rows*group][n] (one winner set per query head);
+    mode "max": scores [rows][n] = max over the group's heads.  Also returns the matching L1
+    norms (for "max", the largest of the heads' norms)."""
+    bits_heads = _c(bits_heads, np.uint8)
+    q = _c(q, np.float32)
+    rows = bits_heads.shape[0] // group
+    per_s, per_l = [], []
+    for h in range(group):
+        s, l1 = scan(planes, meta, bits_heads.reshape(rows, group, D)[:, h], q.reshape(rows, group, D)[:, h], n, S)
+        per_s.append(s)
+        per_l.append(l1)
+    S_ = np.stack(per_s, 1)  # [rows][group][n]
+    L_ = np.stack(per_l, 1)
+    if mode == "per_head":
+        return S_.reshape(rows * group, n), L_.reshape(rows * group, n)
+    if mode == "max":
+        return S_.max(1), L_.max(1)
+    raise ValueError(mode)
+
+
+def allocate_sparq(q, r_channels, group):
+    """SparQ-style comparator: depth 4 on the r channels of largest |qbar|, 0 elsewhere."""
+    q = _c(q, np.float32)
+    rows = q.shape[0] // group
+    bits = np.zeros((rows, D), np.uint8)
+    qbar = np.zeros((rows, D), np.float32)
+    if lib().oracle_allocate_sparq(rows, group, _p(q), int(r_channels), _p(bits), _p(qbar)):
+        raise ValueError("oracle_allocate_sparq: invalid input")
     return bits, qbar
 
 

@@ -257,6 +257,58 @@ int oracle_allocate(int rows, int group, const float* q, const float* var, const
   return 0;
 }
 
+/* Per-query-head allocation (the alternative GQA reading): every query head h
+ * of a KV head water-fills its own budget with w_c = (q_hc * q_hc) * var_c,
+ * [A] "How each query picks its own depth" taken per query head instead of per
+ * summed group query.  bits: [rows*group][128]; budget: [rows] (shared by the
+ * group's heads).  Returns 0 or 1 (invalid). */
+int oracle_allocate_heads(int rows, int group, const float* q, const float* var, const int32_t* budget,
+                          uint8_t* bits) {
+  if (rows <= 0 || group <= 0) return 1;
+  for (int r = 0; r < rows; ++r) {
+    for (int h = 0; h < group; ++h) {
+      float w[D_CH];
+      const float* qh = q + ((size_t)r * group + h) * D_CH;
+      for (int c = 0; c < D_CH; ++c) {
+        if (!isfinite(qh[c]) || !isfinite(var[(size_t)r * D_CH + c])) return 1;
+        w[c] = (qh[c] * qh[c]) * var[(size_t)r * D_CH + c];
+      }
+      if (oracle_waterfill(D_CH, w, budget[r], bits + ((size_t)r * group + h) * D_CH)) return 1;
+    }
+  }
+  return 0;
+}
+
+/* SparQ-style comparator allocation, [A] "The catch": SparQ lets each query
+ * pick its own 32 channels; [G] "Key facts": SparQ's r = 16 read is 68 bits
+ * (16 channels x 4.25 bits of the 4-bit store with its block scale).
+ * reading: the r channels of largest |qbar_c| (ties to the lower channel) are
+ * read at full depth 4, all others are skipped.  qbar as in oracle_allocate. */
+int oracle_allocate_sparq(int rows, int group, const float* q, int r_channels, uint8_t* bits, float* qbar) {
+  if (rows <= 0 || group <= 0 || r_channels < 0 || r_channels > D_CH) return 1;
+  for (int r = 0; r < rows; ++r) {
+    float a[D_CH];
+    int taken[D_CH];
+    for (int c = 0; c < D_CH; ++c) {
+      float s = q[((size_t)r * group + 0) * D_CH + c];
+      for (int h = 1; h < group; ++h) s = s + q[((size_t)r * group + h) * D_CH + c];
+      if (!isfinite(s)) return 1;
+      qbar[(size_t)r * D_CH + c] = s;
+      a[c] = fabsf(s);
+      taken[c] = 0;
+      bits[(size_t)r * D_CH + c] = 0;
+    }
+    for (int i = 0; i < r_channels; ++i) {
+      int best = -1;
+      for (int c = 0; c < D_CH; ++c)
+        if (!taken[c] && (best < 0 || a[c] > a[best])) best = c;
+      taken[best] = 1;
+      bits[(size_t)r * D_CH + best] = 4;
+    }
+  }
+  return 0;
+}
+
 /* ------------------------------------------------------------------------ */
 /* Scan: approximate score of every key from only the planes chosen.        */
 /*                                                                            */

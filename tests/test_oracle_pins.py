@@ -478,3 +478,88 @@ def test_decode_step_composes_the_steps():
     assert np.array_equal(idx, idx2)
     out2 = oracle.sparse_attn(q, K, V, idx2, g)
     np.testing.assert_array_equal(out, out2)
+
+
+# ------------------------------------------------------ SparQ comparator ---
+@pytest.mark.parametrize("r", [0, 1, 16, 32, 127, 128])
+def test_sparq_allocation_is_top_r_magnitudes(r):
+    rng = np.random.default_rng(r)
+    q = rng.standard_normal((12, D)).astype(np.float32)
+    q[4:8] = np.round(q[4:8])  # ties in |qbar|
+    bits, qbar = oracle.allocate_sparq(q, r, 4)
+    for row in range(3):
+        a = np.abs(qbar[row].astype(np.float64))
+        order = sorted(range(D), key=lambda c: (-a[c], c))  # brute force: sort, ties to the lower channel
+        want = np.zeros(D, np.int64)
+        want[order[:r]] = 4
+        assert np.array_equal(bits[row].astype(np.int64), want)
+    assert (bits.sum(1) == 4 * r).all()
+
+
+# ------------------------------------------------ GQA: per-head allocations ---
+def test_allocate_heads_is_each_heads_own_waterfill():
+    """Every query head water-fills the row's budget with w_c = q_hc^2 var_c (sort definition)."""
+    rng = np.random.default_rng(11)
+    rows, g = 3, 4
+    q = rng.standard_normal((rows * g, D)).astype(np.float32)
+    q[5] = q[4]  # two identical heads get identical depths
+    var = np.exp(rng.normal(0, 1, (rows, D))).astype(np.float32)
+    budgets = np.array([92, 0, 300], np.int32)
+    bits = oracle.allocate_heads(q, var, budgets, g)
+    assert bits.shape == (rows * g, D)
+    for r in range(rows):
+        for h in range(g):
+            w = (q[r * g + h] * q[r * g + h]).astype(np.float32) * var[r]
+            assert np.array_equal(bits[r * g + h].astype(np.int64), waterfill_by_sort(w, budgets[r])), (r, h)
+    assert np.array_equal(bits[4], bits[5])
+    # one head per group: the same as the summed-query allocation
+    b1, _ = oracle.allocate(q[:rows], var, budgets, 1)
+    assert np.array_equal(oracle.allocate_heads(q[:rows], var, budgets, 1), b1)
+
+
+def _brute_head_scores(planes, meta, bits_heads, q, n, S, rows, g):
+    """Dequantise every key at each head's own depth and dot with that head's query (fp64)."""
+    codes = codes_from_planes(planes, n, S, rows)  # [rows][n][128]
+    mf = meta_f32(meta).astype(np.float64)
+    blk = np.arange(n) // 128
+    lo = mf[:, :, blk, 0].transpose(0, 2, 1)
+    dl = mf[:, :, blk, 1].transpose(0, 2, 1)
+    out = np.zeros((rows, g, n))
+    for r in range(rows):
+        for h in range(g):
+            b = bits_heads[r * g + h].astype(np.int64)
+            m = 2.0 ** (4 - b)
+            p = codes[r] >> (4 - b)[None, :]
+            x = lo[r] + dl[r] * (m * p + (m - 1) / 2)
+            out[r, h] = (x * np.where(b > 0, q[r * g + h].astype(np.float64), 0.0)).sum(1)
+    return out
+
+
+def test_scan_heads_per_head_and_max_by_brute_force():
+    rows, g, n, S = 2, 3, 300, 256
+    K = rand_keys(rows, n, seed=31)
+    planes, meta, var = oracle.pack(K, S)
+    q = np.random.default_rng(5).standard_normal((rows * g, D)).astype(np.float32)
+    bits = oracle.allocate_heads(q, var, 40, g)
+    want = _brute_head_scores(planes, meta, bits, q, n, S, rows, g)
+    s, l1 = oracle.scan_heads(planes, meta, bits, q, n, S, g, "per_head")
+    np.testing.assert_allclose(s, want.reshape(rows * g, n), rtol=1e-12, atol=1e-12)
+    assert (l1 >= np.abs(s) - 1e-12).all()
+    sm, _ = oracle.scan_heads(planes, meta, bits, q, n, S, g, "max")
+    np.testing.assert_allclose(sm, want.max(1), rtol=1e-12, atol=1e-12)
+
+
+def test_scan_heads_with_identical_heads_is_the_group_scan_scaled():
+    """g identical heads: per-head depths equal the summed-query depths (w scales by g^2), and
+    each head's score is the summed-query score / g."""
+    rows, g, n, S = 1, 4, 256, 256
+    K = rand_keys(rows, n, seed=8)
+    planes, meta, var = oracle.pack(K, S)
+    q1 = np.round(np.random.default_rng(1).standard_normal((1, D)) * 8).astype(np.float32) / 8  # exact x4
+    q = np.repeat(q1, g, 0)
+    bits_h = oracle.allocate_heads(q, var, 92, g)
+    bits, qbar = oracle.allocate(q, var, 92, g)
+    assert all(np.array_equal(bits_h[h], bits[0]) for h in range(g))
+    s_sum, _ = oracle.scan(planes, meta, bits, qbar, n, S)
+    s_max, _ = oracle.scan_heads(planes, meta, bits_h, q, n, S, g, "max")
+    np.testing.assert_allclose(s_max * g, s_sum, rtol=1e-12, atol=1e-9)
