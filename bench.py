@@ -125,6 +125,8 @@ class Model:
         import sparse_top_kv_fathom_gb300 as F
         from sparse_top_kv_fathom_gb300 import synth
         self.F, self.w, self.S, self.budget = F, w, S, budget
+        # per-row budgets (the session batch draws one budget per session)
+        self.budget_rows = (synth.row_budgets(w).to(torch.int16).cuda() if w.per_row_budget else None)
         L, H, n = w.layers, w.kv_heads, w.n
         self.kv_layers = KL = min(L, kv_layers or L)
         rows = w.rows
@@ -187,27 +189,33 @@ class Model:
         s = l % self.kv_layers
         return s * H, (s + 1) * H
 
-    def layer_index(self, store, l):
+    def layer_index(self, store, l, span=1):
         H = self.w.kv_heads
-        r0, r1 = l * H, (l + 1) * H
-        return self.F.BitPlaneIndex(store["planes"][r0:r1], store["meta"][r0:r1], self.var[r0:r1], self.w.n, H,
-                                    self.S)
+        r0, r1 = l * H, (l + span) * H
+        return self.F.BitPlaneIndex(store["planes"][r0:r1], store["meta"][r0:r1], self.var[r0:r1], self.w.n,
+                                    r1 - r0, self.S)
 
-    def steps(self, store, q, out, idx, ws=None):
-        """Per-layer DecodeStep objects sharing one workspace; outputs are views of out/idx."""
+    def steps(self, store, q, out, idx, ws=None, sparq_r=0):
+        """DecodeStep objects sharing one workspace; outputs are views of out/idx.  Layers of one
+        model run one after the other (a layer's query depends on the previous layer); independent
+        sessions run as one batched step over all their rows."""
         F, w = self.F, self.w
         H, G = w.kv_heads, w.group
-        ix0 = self.layer_index(store, 0)
-        nb = F.DecodeStep.workspace_bytes(ix0, w.k, G)
+        span = w.layers if (w.independent_layers and self.kv_layers == w.layers) else 1
+        ixs = [self.layer_index(store, l, span) for l in range(0, w.layers, span)]
+        nb = F.DecodeStep.workspace_bytes(ixs[0], w.k, G)
         ws = ws if ws is not None else torch.empty(nb, dtype=torch.uint8, device="cuda")
         out_b = torch.empty(out.shape, dtype=torch.bfloat16, device="cuda")
         res = []
-        for l in range(w.layers):
-            r0, r1 = l * H, (l + 1) * H
+        for i, l in enumerate(range(0, w.layers, span)):
+            r0, r1 = l * H, (l + span) * H
             k0, k1 = self.kv_rows(l)
-            res.append(F.DecodeStep(self.layer_index(store, l), store["K"][k0:k1], store["V"][k0:k1],
-                                    q[r0 * G:r1 * G], w.k, G, self.budget, workspace=ws,
-                                    idx=idx[r0:r1], out=out[r0 * G:r1 * G], out_bf16=out_b[r0 * G:r1 * G]))
+            k1 = k0 + (r1 - r0)
+            budget = self.budget_rows[r0:r1] if self.budget_rows is not None else self.budget
+            res.append(F.DecodeStep(ixs[i], store["K"][k0:k1], store["V"][k0:k1],
+                                    q[r0 * G:r1 * G], w.k, G, budget, workspace=ws,
+                                    idx=idx[r0:r1], out=out[r0 * G:r1 * G], out_bf16=out_b[r0 * G:r1 * G],
+                                    sparq_r=sparq_r))
         return res
 
     def comparator_steps(self, store, q, out, idx):
@@ -281,7 +289,8 @@ def scan_timing(model, store, steps, stream):
     layers = []
     for l in range(w.layers):
         ix = model.layer_index(store, l)
-        bits, qbar = F.allocate(model.q[l * H * G:(l + 1) * H * G], ix.var, model.budget, G)
+        bud = model.budget_rows[l * H:(l + 1) * H] if model.budget_rows is not None else model.budget
+        bits, qbar = F.allocate(model.q[l * H * G:(l + 1) * H * G], ix.var, bud, G)
         scores = torch.empty((H, w.n), dtype=torch.float32, device="cuda")
         layers.append((ix, bits, qbar, scores))
     torch.cuda.synchronize()
@@ -315,18 +324,26 @@ def scan_timing(model, store, steps, stream):
     return statistics.mean(durs), statistics.mean(algo), durs
 
 
-SCAN_SOURCE = os.path.join(ROOT, "sparse_top_kv_fathom_gb300", "csrc", "scan.cu")
+SCAN_SOURCES = [os.path.join(ROOT, "sparse_top_kv_fathom_gb300", "csrc", f) for f in ("scan.cu", "bitplane.cuh")]
 TRAFFIC_RECORD = os.path.join(ROOT, "profiles", "scan_kernel_traffic.json")
+
+
+def scan_source_hash():
+    """sha256 over the scan kernel's sources (scan.cu, then bitplane.cuh)."""
+    import hashlib
+    h = hashlib.sha256()
+    for f in SCAN_SOURCES:
+        h.update(open(f, "rb").read())
+    return h.hexdigest()
 
 
 def captured_traffic(residency, w, budget):
     """Bytes one scan launch (one layer: kv_heads rows x n tokens) moved, from the committed
     ncu capture record -- only if it was taken on this very scan kernel source and workload
     (DRAM bytes for the HBM-resident index; system-memory sectors x 32 B for the host one)."""
-    import hashlib
     try:
         rec = json.load(open(TRAFFIC_RECORD))
-        src = hashlib.sha256(open(SCAN_SOURCE, "rb").read()).hexdigest()
+        src = scan_source_hash()
     except (OSError, ValueError):
         return None
     if rec.get("scan_source_sha256") != src:
@@ -341,10 +358,9 @@ def captured_issue_rate(residency, w, budget, ms_per_launch):
     """Instruction-issue roofline of the scan (the bound with the index in HBM): warp
     instructions of one launch (committed ncu capture, same kernel source and workload) per
     second of the live launch time, against 4 issues per clock per SM at the maximum SM clock."""
-    import hashlib
     try:
         rec = json.load(open(TRAFFIC_RECORD))
-        src = hashlib.sha256(open(SCAN_SOURCE, "rb").read()).hexdigest()
+        src = scan_source_hash()
     except (OSError, ValueError):
         return None
     r = rec.get(residency)
@@ -356,9 +372,17 @@ def captured_issue_rate(residency, w, budget, ms_per_launch):
         if os.path.exists(os.path.join(ROOT, "MEASURED_PEAKS.json")) else 2070.0
     peak = 4.0 * props.multi_processor_count * sm_mhz * 1e6
     achieved = r["warp_instructions"] / (ms_per_launch * 1e-3)
-    return {"bound": "issue", "achieved": achieved, "peak": peak, "unit": "warp instructions/s",
-            "frac": achieved / peak, "kernel": "scan_kernel",
-            "source": "smsp__inst_executed.sum of one launch (ncu) / live launch time"}
+    out = {"bound": "issue", "achieved": achieved, "peak": peak, "unit": "warp instructions/s",
+           "frac": achieved / peak, "kernel": "scan_kernel",
+           "source": "smsp__inst_executed.sum of one launch (ncu) / live launch time"}
+    if "alu_warp_instructions" in r and "alu_peak_per_sm_cycle" in r:
+        # the integer pipe (shifts, bit selects, byte permutes) that bounds the scan in HBM
+        apeak = r["alu_peak_per_sm_cycle"] * props.multi_processor_count * sm_mhz * 1e6
+        aach = r["alu_warp_instructions"] / (ms_per_launch * 1e-3)
+        out["alu"] = {"bound": "alu", "achieved": aach, "peak": apeak, "unit": "ALU-pipe warp instructions/s",
+                      "frac": aach / apeak, "source": "sm__inst_executed_pipe_alu.sum of one launch (ncu) / "
+                      "live launch time; peak = sm__inst_executed_pipe_alu peak per SM cycle x SMs x max clock"}
+    return out
 
 
 def link_peak(log):
@@ -406,7 +430,8 @@ def cpu_baseline(model, store, log, seconds=(10.0, 30.0)):
     reps, t = 0, 0.0
     t0 = time.time()
     while t < seconds[0] and reps < 50:
-        oracle.decode_step(planes, meta, var, q, model.budget, K, V, w.k, G, model.S)
+        bud = model.budget_rows[:rows].cpu().numpy().astype(np.int32) if model.budget_rows is not None else model.budget
+        oracle.decode_step(planes, meta, var, q, bud, K, V, w.k, G, model.S)
         reps += 1
         t = time.time() - t0
     keys = reps * rows * w.n
@@ -512,6 +537,14 @@ def main():
             r["comparator_ms_per_step"] = max_over_ranks(ctot) / args.steps
             r["comparator_bytes_per_step"] = w.rows * w.n * 17
             del cg
+            # SparQ-style comparator on the same bit-plane store: r channels of largest |qbar| at 4 bits
+            r["sparq"] = {}
+            for rr in (16, 32):
+                sg = capture(model.steps(store, q, cout, cidx, sparq_r=rr), stream)
+                stot, _, _ = time_graph(sg, args.steps, args.warmup, stream)
+                r["sparq"]["r%d" % rr] = {"ms_per_step": max_over_ranks(stot) / args.steps,
+                                          "bits_per_key_read": 4 * rr + 32 * rr / 128}
+                del sg
         if res == primary:
             # e2e: q in from pinned host memory, output back to pinned host memory, every step
             qh = model.q.cpu().pin_memory()
@@ -584,7 +617,10 @@ def main():
     if comparator:
         line["comparator"] = {"index": "fixed 136-bit (32 channels x 4 bit + 8-bit scale)",
                               "ms_per_step": p.get("comparator_ms_per_step"),
-                              "fathom_speedup": p.get("comparator_ms_per_step", 0) / p["ms_per_step"]}
+                              "fathom_speedup": p.get("comparator_ms_per_step", 0) / p["ms_per_step"],
+                              "sparq": p.get("sparq")}
+        if "device" in result and "hbm_resident" in line:
+            line["hbm_resident"]["sparq"] = result["device"].get("sparq")
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(model, model.h if model.h else model.d, log)
     if rank == 0:

@@ -129,6 +129,15 @@ int fathom_pack(const fathom_index_desc* desc, const void* K, int k_dtype, uint3
 int fathom_allocate(int rows, int group, const void* q, int q_dtype, const float* var, const uint16_t* budgets,
                     int budget, uint8_t* bits, float* qbar, int32_t* status, void* stream);
 
+/* SparQ-style comparator allocation on the same bit-plane store ([A] "The
+ * catch": SparQ lets each query pick its own 32 channels; [G] "Key facts":
+ * SparQ's r = 16 read is 68 bits): the r_channels channels of largest |qbar_c|
+ * (ties to the lower channel) get depth 4, every other channel depth 0, so the
+ * scan reads r_channels x 4 bits plus their block (lo, delta) per key.
+ * Arguments as fathom_allocate; EINVAL if r_channels is outside [0, 128]. */
+int fathom_allocate_sparq(int rows, int group, const void* q, int q_dtype, int r_channels, uint8_t* bits,
+                          float* qbar, int32_t* status, void* stream);
+
 /* Variable-depth scan ([A] "How each query picks its own depth": read only
  * the chosen planes; channels with no bits are skipped entirely).
  *   planes, meta  device or mapped host, as packed by fathom_pack.
@@ -139,6 +148,39 @@ int fathom_allocate(int rows, int group, const void* q, int q_dtype, const float
  *     delta) of t's block.  fp32 accumulation. */
 int fathom_scan(const fathom_index_desc* desc, const uint32_t* planes, const uint16_t* meta, const uint8_t* bits,
                 const float* qbar, float* scores, void* stream);
+
+/* ---------------- GQA readings ----------------------------------------------
+ * The pages count B bits per key per (layer, KV head), which the default step
+ * reads with one allocation per KV head from the group's summed query.  The
+ * alternative readings allocate per query head ([A] "How each query picks its
+ * own depth", per query head): */
+#define FATHOM_GQA_SUM 0      /* one allocation and winner set per KV head (fathom_allocate) */
+#define FATHOM_GQA_PER_HEAD 1 /* per-head allocations, scores and winner sets */
+#define FATHOM_GQA_MAX 2      /* per-head allocations; one winner set per KV head by the max head score */
+
+/* Per-query-head allocation: every query head h of KV row r water-fills the
+ * row's budget (budgets[r] or `budget`) with its own w_c = (q_hc*q_hc)*var_rc,
+ * by the rule of fathom_allocate.
+ *   q     device [rows*group][128] of q_dtype (head h of row r at r*group + h).
+ *   var   device [rows][128]; budgets device uint16 [rows] or NULL.
+ *   bits  device uint8 [rows*group][128] out.
+ *   qh    device float [rows*group][128] out: q converted to fp32.
+ *   status as fathom_allocate.  EINVAL as fathom_allocate. */
+int fathom_allocate_heads(int rows, int group, const void* q, int q_dtype, const float* var, const uint16_t* budgets,
+                          int budget, uint8_t* bits, float* qh, int32_t* status, void* stream);
+
+/* Scan under per-head allocations.  Head h of row r scores key t with its own
+ * depths and query:
+ *   s_h(t) = sum over c with b_hc >= 1 of q_hc * (lo + delta*(m*p + (m-1)/2)),
+ * m = 2^(4-b_hc), p the b_hc-bit prefix (as fathom_scan).  Each channel's
+ * planes are read once, to the deepest of the heads' depths.
+ *   bits, qh  device [rows*group][128] from fathom_allocate_heads.
+ *   mode      FATHOM_GQA_PER_HEAD: scores device float [rows*group][n] out,
+ *             row r*group + h = s_h;  FATHOM_GQA_MAX: scores [rows][n] out,
+ *             max over the group's heads of s_h(t).
+ * EINVAL for another mode. */
+int fathom_scan_heads(const fathom_index_desc* desc, int group, int mode, const uint32_t* planes, const uint16_t* meta,
+                      const uint8_t* bits, const float* qh, float* scores, void* stream);
 
 /* Workspace bytes of fathom_topk (host-only). */
 int fathom_topk_workspace_bytes(int rows, int64_t n, int64_t k, size_t* bytes);
@@ -195,6 +237,14 @@ int fathom_sparse_attn(int rows, int group, int64_t n, int64_t k, const void* q,
                        const void* V, int kv_dtype, int64_t kv_stride, const int32_t* idx, float* out,
                        uint16_t* out_bf16, void* workspace, size_t ws_bytes, void* stream);
 
+/* fathom_sparse_attn with one winner set per query head (FATHOM_GQA_PER_HEAD):
+ * idx is device int32 [rows*group][k] and query head r*group + h attends over
+ * row r*group + h of idx, with the K/V of row r.  Other arguments as
+ * fathom_sparse_attn; EINVAL also if rows*group > 65535. */
+int fathom_sparse_attn_heads(int rows, int group, int64_t n, int64_t k, const void* q, int q_dtype, const void* K,
+                             const void* V, int kv_dtype, int64_t kv_stride, const int32_t* idx, float* out,
+                             uint16_t* out_bf16, void* workspace, size_t ws_bytes, void* stream);
+
 /* One decode step over `index.rows` rows: allocate -> scan -> top-k ->
  * sparse attention ([R] summary: the index scan ranks all n keys to choose
  * the top k; the selected rows are attended).  Same definitions as the
@@ -207,6 +257,11 @@ typedef struct fathom_step_desc {
   int32_t q_dtype;          /* dtype of q */
   int32_t kv_dtype;         /* dtype of K and V */
   int64_t kv_stride;        /* elements between consecutive tokens' K (and V) rows, see fathom_sparse_attn */
+  int32_t sparq_r;          /* 0: reverse water-filling of `budget`; r > 0: the SparQ-style allocation
+                               of fathom_allocate_sparq with r channels (budget ignored) */
+  int32_t gqa_mode;         /* FATHOM_GQA_SUM (0), FATHOM_GQA_PER_HEAD or FATHOM_GQA_MAX; the per-head
+                               modes water-fill `budget` per query head (fathom_allocate_heads) and need
+                               sparq_r == 0 */
   const uint32_t* planes;   /* index (device or mapped host) */
   const uint16_t* meta;     /* index (device or mapped host) */
   const float* var;         /* device [rows][128] */
@@ -214,7 +269,7 @@ typedef struct fathom_step_desc {
   const void* q;            /* device [rows*group][128] */
   const void* K;            /* device or mapped host, rows of kv_stride elements */
   const void* V;            /* device or mapped host, rows of kv_stride elements */
-  int32_t* idx;             /* device [rows][k] out */
+  int32_t* idx;             /* device [rows][k] out ([rows*group][k] for FATHOM_GQA_PER_HEAD) */
   float* out;               /* device [rows*group][128] out */
   uint16_t* out_bf16;       /* device [rows*group][128] out or NULL */
   int32_t* status;          /* device int32 or NULL (FATHOM_STATUS_* bits) */

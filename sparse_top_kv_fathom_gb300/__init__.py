@@ -7,6 +7,6 @@ package only marshals torch tensors into that library.
 """
 from ._native import FathomError, load  # noqa: F401
 from .api import (  # noqa: F401
-    BF16, D, F16, F32, QBLOCK, BitPlaneIndex, DecodeStep, Fixed136Index, Fixed136Step, allocate, decode_step,
-    fixed136_pack, fixed136_scan, host_empty, host_release, index_bytes, index_shapes, kv_stride, pack,
-    probe_stream_read, scan, sparse_attn, topk)
+    BF16, D, F16, F32, GQA_MODES, QBLOCK, BitPlaneIndex, DecodeStep, Fixed136Index, Fixed136Step, allocate,
+    allocate_heads, allocate_sparq, decode_step, fixed136_pack, fixed136_scan, host_empty, host_release, index_bytes,
+    index_shapes, kv_stride, pack, probe_stream_read, scan, scan_heads, sparse_attn, topk)

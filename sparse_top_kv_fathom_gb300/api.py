@@ -113,6 +113,48 @@ def allocate(q, var, budget, group, status=None, stream=None):
     return bits, qbar
 
 
+def allocate_sparq(q, r_channels, group, status=None, stream=None):
+    """SparQ-style comparator allocation: depth 4 on the r channels of largest |qbar|
+    -> (bits uint8 [rows][128], qbar fp32 [rows][128])."""
+    L = lib()
+    rows = q.shape[0] // group
+    bits = torch.empty((rows, D), dtype=torch.uint8, device=q.device)
+    qbar = torch.empty((rows, D), dtype=torch.float32, device=q.device)
+    N.check(L.fathom_allocate_sparq(rows, group, _ptr(q), _dt(q), int(r_channels), _ptr(bits), _ptr(qbar),
+                                    _ptr(status), _stream(stream)))
+    return bits, qbar
+
+
+GQA_MODES = {"sum": N.GQA_SUM, "per_head": N.GQA_PER_HEAD, "max": N.GQA_MAX}
+
+
+def allocate_heads(q, var, budget, group, status=None, stream=None):
+    """Per-query-head allocation: q [rows*group][128], var [rows][128], budget int or int16
+    cuda tensor [rows] -> (bits uint8 [rows*group][128], qh fp32 [rows*group][128])."""
+    L = lib()
+    rows = var.shape[0]
+    bits = torch.empty((rows * group, D), dtype=torch.uint8, device=q.device)
+    qh = torch.empty((rows * group, D), dtype=torch.float32, device=q.device)
+    budgets = budget if isinstance(budget, torch.Tensor) else None
+    scalar = 0 if budgets is not None else int(budget)
+    N.check(L.fathom_allocate_heads(rows, group, _ptr(q), _dt(q), _ptr(var), _ptr(budgets), scalar, _ptr(bits),
+                                    _ptr(qh), _ptr(status), _stream(stream)))
+    return bits, qh
+
+
+def scan_heads(index, bits, qh, group, mode, stream=None):
+    """Scores under per-head allocations: mode "per_head" -> fp32 [rows*group][n];
+    mode "max" -> fp32 [rows][n] (max over the group's heads)."""
+    L = lib()
+    m = GQA_MODES[mode]
+    srows = index.rows * group if m == N.GQA_PER_HEAD else index.rows
+    scores = torch.empty((srows, index.n), dtype=torch.float32, device=bits.device)
+    d = index.desc
+    N.check(L.fathom_scan_heads(ctypes.byref(d), group, m, _ptr(index.planes), _ptr(index.meta), _ptr(bits),
+                                _ptr(qh), _ptr(scores), _stream(stream)))
+    return scores
+
+
 def scan(index, bits, qbar, stream=None):
     """Scores fp32 [rows][n] from only the planes each row's depths select."""
     L = lib()
@@ -148,8 +190,9 @@ def kv_stride(K, V):
     return s
 
 
-def sparse_attn(q, K, V, idx, group, stream=None):
-    """Attention over the selected rows -> (out fp32 [rows*group][128], out bf16)."""
+def sparse_attn(q, K, V, idx, group, stream=None, per_head=False):
+    """Attention over the selected rows -> (out fp32 [rows*group][128], out bf16).
+    per_head: idx is [rows*group][k], one winner set per query head."""
     L = lib()
     rows, n, _ = K.shape
     k = idx.shape[1]
@@ -159,9 +202,9 @@ def sparse_attn(q, K, V, idx, group, stream=None):
     wsb = ctypes.c_size_t()
     N.check(L.fathom_sparse_attn_workspace_bytes(rows, group, k, ctypes.byref(wsb)))
     ws = _ws(wsb.value, dev)
-    N.check(L.fathom_sparse_attn(rows, group, n, k, _ptr(q), _dt(q), _ptr(K), _ptr(V), _dt(K), kv_stride(K, V),
-                                 _ptr(idx), _ptr(out),
-                                 _ptr(outb), _ptr(ws), wsb.value, _stream(stream)))
+    fn = L.fathom_sparse_attn_heads if per_head else L.fathom_sparse_attn
+    N.check(fn(rows, group, n, k, _ptr(q), _dt(q), _ptr(K), _ptr(V), _dt(K), kv_stride(K, V), _ptr(idx), _ptr(out),
+               _ptr(outb), _ptr(ws), wsb.value, _stream(stream)))
     return out, outb
 
 
@@ -173,12 +216,14 @@ class DecodeStep:
     K, V:  [rows][n][128] (device or pinned host), q: [rows*group][128] (device)."""
 
     def __init__(self, index, K, V, q, k, group, budget, status=None, device=None, workspace=None, idx=None,
-                 out=None, out_bf16=None):
+                 out=None, out_bf16=None, sparq_r=0, gqa="sum"):
         self.L = lib()
         self.index, self.K, self.V, self.q = index, K, V, q
         dev = device if device is not None else q.device
         rows = index.rows
-        self.idx = idx if idx is not None else torch.empty((rows, k), dtype=torch.int32, device=dev)
+        gqa_mode = GQA_MODES[gqa]
+        sel_rows = rows * group if gqa_mode == N.GQA_PER_HEAD else rows
+        self.idx = idx if idx is not None else torch.empty((sel_rows, k), dtype=torch.int32, device=dev)
         self.out = out if out is not None else torch.empty((rows * group, D), dtype=torch.float32, device=dev)
         self.out_bf16 = (out_bf16 if out_bf16 is not None else
                          torch.empty((rows * group, D), dtype=torch.bfloat16, device=dev))
@@ -192,6 +237,8 @@ class DecodeStep:
         self.desc.q_dtype = _dt(q)
         self.desc.kv_dtype = _dt(K)
         self.desc.kv_stride = kv_stride(K, V)
+        self.desc.sparq_r = int(sparq_r)  # 0: water-filling of `budget`; r > 0: SparQ-style comparator
+        self.desc.gqa_mode = gqa_mode     # "sum": one allocation per KV head; "per_head" / "max": per query head
         self._bind()
         wsb = ctypes.c_size_t()
         N.check(self.L.fathom_decode_step_workspace_bytes(ctypes.byref(self.desc), ctypes.byref(wsb)))
@@ -204,9 +251,9 @@ class DecodeStep:
         self.ws_bytes = wsb.value
 
     @staticmethod
-    def workspace_bytes(index, k, group):
+    def workspace_bytes(index, k, group, gqa="sum"):
         d = N.StepDesc()
-        d.index, d.group, d.k = index.desc, group, k
+        d.index, d.group, d.k, d.gqa_mode = index.desc, group, k, GQA_MODES[gqa]
         wsb = ctypes.c_size_t()
         N.check(lib().fathom_decode_step_workspace_bytes(ctypes.byref(d), ctypes.byref(wsb)))
         return wsb.value

@@ -8,6 +8,9 @@
 // gains with a fixed tie order is the same allocation).  Importance of channel c
 // is w_c = qbar_c^2 * var_c (Glonce summary: variance-weighted importance).
 //
+// fathom_allocate_heads takes the same allocation per query head (each head's
+// own q_h instead of the summed group query), the alternative reading of GQA.
+//
 // GPU form: one CTA per row, one thread per candidate (channel c, plane j).
 // As on the page, the threshold tau is found by binary search: over the bit
 // patterns of non-negative fp32 gains (which order like integers), the largest
@@ -21,7 +24,9 @@ namespace {
 
 constexpr int kCand = kD * kPlanes;  // 512 candidates per row
 
-__global__ void __launch_bounds__(kCand) allocate_kernel(int group, const void* __restrict__ q, int q_dtype,
+// Row r sums `group` query heads; its variance and budget are those of KV row r / heads
+// (heads = 1: one allocation per KV head; group = 1, heads = G: one per query head).
+__global__ void __launch_bounds__(kCand) allocate_kernel(int group, int heads, const void* __restrict__ q, int q_dtype,
                                                          const float* __restrict__ var,
                                                          const uint16_t* __restrict__ budgets, int budget,
                                                          uint8_t* __restrict__ bits, float* __restrict__ qbar,
@@ -41,7 +46,7 @@ __global__ void __launch_bounds__(kCand) allocate_kernel(int group, const void* 
     const int64_t q0 = int64_t(r) * group * kD + c;
     float s = load_as_float(q, q0, q_dtype);
     for (int h = 1; h < group; ++h) s = __fadd_rn(s, load_as_float(q, q0 + int64_t(h) * kD, q_dtype));
-    const float v = var[int64_t(r) * kD + c];
+    const float v = var[int64_t(r / heads) * kD + c];
     if (!isfinite(s) || !isfinite(v)) s_bad = 1;
     qbar[int64_t(r) * kD + c] = s;
     w = __fmul_rn(__fmul_rn(s, s), v);
@@ -58,7 +63,7 @@ __global__ void __launch_bounds__(kCand) allocate_kernel(int group, const void* 
     for (int jj = 0; jj < j; ++jj) w = __fmul_rn(w, 0.25f);
   }
   const uint32_t gb = __float_as_uint(w);  // w >= +0: bit patterns order like the values
-  int B = budgets ? int(budgets[r]) : budget;
+  int B = budgets ? int(budgets[r / heads]) : budget;
   if (B > kCand) {
     if (i == 0 && status) atomicOr(status, FATHOM_STATUS_BUDGET_CLAMPED);
     B = kCand;
@@ -85,6 +90,30 @@ __global__ void __launch_bounds__(kCand) allocate_kernel(int group, const void* 
   if (i < kD) bits[int64_t(r) * kD + i] = uint8_t(s_count[i]);
 }
 
+// SparQ-style comparator: full depth on the r channels of largest |qbar| (ties
+// to the lower channel), nothing elsewhere.  One CTA per row, one thread per channel.
+__global__ void __launch_bounds__(kD) allocate_sparq_kernel(int group, const void* __restrict__ q, int q_dtype,
+                                                            int r_channels, uint8_t* __restrict__ bits,
+                                                            float* __restrict__ qbar, int32_t* __restrict__ status) {
+  __shared__ float s_a[kD];
+  const int r = blockIdx.x, c = threadIdx.x;
+  const int64_t q0 = int64_t(r) * group * kD + c;
+  float s = load_as_float(q, q0, q_dtype);
+  for (int h = 1; h < group; ++h) s = __fadd_rn(s, load_as_float(q, q0 + int64_t(h) * kD, q_dtype));
+  qbar[int64_t(r) * kD + c] = s;
+  const float a = fabsf(s);
+  s_a[c] = a;
+  const int bad = __syncthreads_or(!isfinite(s));
+  if (bad) {
+    bits[int64_t(r) * kD + c] = 0;
+    if (c == 0 && status) atomicOr(status, FATHOM_STATUS_NONFINITE);
+    return;
+  }
+  int rank = 0;
+  for (int o = 0; o < kD; ++o) rank += (s_a[o] > a) || (s_a[o] == a && o < c);
+  bits[int64_t(r) * kD + c] = rank < r_channels ? uint8_t(kPlanes) : uint8_t(0);
+}
+
 __global__ void __launch_bounds__(kD) qbar_kernel(int group, const void* __restrict__ q, int q_dtype,
                                                   float* __restrict__ qbar) {
   const int r = blockIdx.x, c = threadIdx.x;
@@ -98,7 +127,20 @@ __global__ void __launch_bounds__(kD) qbar_kernel(int group, const void* __restr
 
 cudaError_t launch_allocate(int rows, int group, const void* q, int q_dtype, const float* var, const uint16_t* budgets,
                             int budget, uint8_t* bits, float* qbar, int32_t* status, cudaStream_t st) {
-  allocate_kernel<<<rows, kCand, 0, st>>>(group, q, q_dtype, var, budgets, budget, bits, qbar, status);
+  allocate_kernel<<<rows, kCand, 0, st>>>(group, 1, q, q_dtype, var, budgets, budget, bits, qbar, status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_allocate_heads(int rows, int group, const void* q, int q_dtype, const float* var,
+                                  const uint16_t* budgets, int budget, uint8_t* bits, float* qh, int32_t* status,
+                                  cudaStream_t st) {
+  allocate_kernel<<<rows * group, kCand, 0, st>>>(1, group, q, q_dtype, var, budgets, budget, bits, qh, status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_allocate_sparq(int rows, int group, const void* q, int q_dtype, int r_channels, uint8_t* bits,
+                                  float* qbar, int32_t* status, cudaStream_t st) {
+  allocate_sparq_kernel<<<rows, kD, 0, st>>>(group, q, q_dtype, r_channels, bits, qbar, status);
   return cudaGetLastError();
 }
 
@@ -128,5 +170,42 @@ extern "C" int fathom_allocate(int rows, int group, const void* q, int q_dtype, 
   FATHOM_TRY(device_view(status, "status", &dst, true));
   FATHOM_TRY_CUDA(launch_allocate(rows, group, dq, q_dtype, (const float*)dv, (const uint16_t*)db, budget,
                                   (uint8_t*)dbits, (float*)dqb, (int32_t*)dst, as_stream(stream)));
+  return FATHOM_OK;
+}
+
+extern "C" int fathom_allocate_heads(int rows, int group, const void* q, int q_dtype, const float* var,
+                                     const uint16_t* budgets, int budget, uint8_t* bits, float* qh, int32_t* status,
+                                     void* stream) {
+  clear_error();
+  if (rows < 1 || group < 1 || group > 64 || int64_t(rows) * group > 0x7fffffff)
+    return set_error(FATHOM_EINVAL, "rows >= 1 and 1 <= group <= 64 required");
+  if (!valid_dtype(q_dtype)) return set_error(FATHOM_EINVAL, "q_dtype %d invalid", q_dtype);
+  if (!budgets && (budget < 0 || budget > kD * kPlanes))
+    return set_error(FATHOM_EINVAL, "budget %d outside [0, 512]", budget);
+  const void *dq, *dv, *db, *dbits, *dqh, *dst;
+  FATHOM_TRY(device_view(q, "q", &dq));
+  FATHOM_TRY(device_view(var, "var", &dv));
+  FATHOM_TRY(device_view(budgets, "budgets", &db, true));
+  FATHOM_TRY(device_view(bits, "bits", &dbits));
+  FATHOM_TRY(device_view(qh, "qh", &dqh));
+  FATHOM_TRY(device_view(status, "status", &dst, true));
+  FATHOM_TRY_CUDA(launch_allocate_heads(rows, group, dq, q_dtype, (const float*)dv, (const uint16_t*)db, budget,
+                                        (uint8_t*)dbits, (float*)dqh, (int32_t*)dst, as_stream(stream)));
+  return FATHOM_OK;
+}
+
+extern "C" int fathom_allocate_sparq(int rows, int group, const void* q, int q_dtype, int r_channels, uint8_t* bits,
+                                     float* qbar, int32_t* status, void* stream) {
+  clear_error();
+  if (rows < 1 || group < 1 || group > 64) return set_error(FATHOM_EINVAL, "rows >= 1 and 1 <= group <= 64 required");
+  if (!valid_dtype(q_dtype)) return set_error(FATHOM_EINVAL, "q_dtype %d invalid", q_dtype);
+  if (r_channels < 0 || r_channels > kD) return set_error(FATHOM_EINVAL, "r_channels %d outside [0, 128]", r_channels);
+  const void *dq, *dbits, *dqb, *dst;
+  FATHOM_TRY(device_view(q, "q", &dq));
+  FATHOM_TRY(device_view(bits, "bits", &dbits));
+  FATHOM_TRY(device_view(qbar, "qbar", &dqb));
+  FATHOM_TRY(device_view(status, "status", &dst, true));
+  FATHOM_TRY_CUDA(launch_allocate_sparq(rows, group, dq, q_dtype, r_channels, (uint8_t*)dbits, (float*)dqb,
+                                        (int32_t*)dst, as_stream(stream)));
   return FATHOM_OK;
 }

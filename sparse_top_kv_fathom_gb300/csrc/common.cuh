@@ -96,14 +96,22 @@ size_t attn_ws_bytes(int rows, int group, int64_t k);
 // launchers used by the step functions (arguments already validated)
 cudaError_t launch_allocate(int rows, int group, const void* q, int q_dtype, const float* var, const uint16_t* budgets,
                             int budget, uint8_t* bits, float* qbar, int32_t* status, cudaStream_t st);
+cudaError_t launch_allocate_heads(int rows, int group, const void* q, int q_dtype, const float* var,
+                                  const uint16_t* budgets, int budget, uint8_t* bits, float* qh, int32_t* status,
+                                  cudaStream_t st);
+cudaError_t launch_scan_heads(const IndexGeom& g, int group, int mode, const uint32_t* planes, const __half2* meta,
+                              const uint8_t* bits, const float* qh, float* scores, uint32_t* hist, cudaStream_t st);
 cudaError_t launch_qbar(int rows, int group, const void* q, int q_dtype, float* qbar, cudaStream_t st);
+cudaError_t launch_allocate_sparq(int rows, int group, const void* q, int q_dtype, int r_channels, uint8_t* bits,
+                                  float* qbar, int32_t* status, cudaStream_t st);
 cudaError_t launch_scan(const IndexGeom& g, const uint32_t* planes, const __half2* meta, const uint8_t* bits,
                         const float* qbar, float* scores, uint32_t* hist, cudaStream_t st);
 cudaError_t launch_topk(int rows, int64_t n, int64_t k, const float* scores, int32_t* idx, float* vals, void* ws,
                         bool hist_ready, cudaStream_t st);
+// per_head: idx holds one winner set per query head ([rows*group][k]), each head attends over its own
 cudaError_t launch_attn(int rows, int group, int64_t n, int64_t k, const void* q, int q_dtype, const void* K,
                         const void* V, int kv_dtype, int64_t kv_stride, const int32_t* idx, float* out, uint16_t* out_bf16, void* ws,
-                        cudaStream_t st);
+                        cudaStream_t st, bool per_head = false);
 cudaError_t launch_fixed136_scan(int rows, int64_t n, const int32_t* chans, const uint8_t* codes, const uint8_t* exps,
                                  const float* qbar, float* scores, uint32_t* hist, cudaStream_t st);
 

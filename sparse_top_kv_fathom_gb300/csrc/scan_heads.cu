@@ -1,0 +1,283 @@
+// fathom_scan_heads: the bit-plane scan under per-query-head allocations, the
+// alternative reading of GQA (Fathom article, "How each query picks its own
+// depth", taken per query head): head h of KV row r has its own depths b_hc
+// and scores every key with its own query,
+//     s_h(t) = sum_{c: b_hc>=1} q_hc * (lo + delta*(m_hc*p_hc(t) + (m_hc-1)/2)),
+// p_hc the b_hc-bit prefix, m_hc = 2^(4-b_hc).  The scores are kept per head
+// (one winner set per query head) or reduced to their maximum over the group's
+// heads (one winner set per KV head).
+//
+// GPU form: one pass reads each channel's planes once, to the deepest depth
+// any head of the launch asks for (the union of the heads' planes); every head
+// takes its own prefix of those planes by masking the nibbles to its depth.
+// Up to four heads per launch (their accumulators live in registers); a group
+// of more heads takes several launches, the max mode folding each into the
+// scores of the previous ones.  Same per-token arithmetic as fathom_scan: the
+// byte-permute float 1 + u/16, then x and qbar*x as packed f32x2 FMAs.
+#include "bitplane.cuh"
+#include "common.cuh"
+
+namespace fathom {
+namespace {
+
+using namespace bitplane;
+
+constexpr int kHThreads = 128;                // one thread per 32 tokens
+constexpr int kHTile = kHThreads * 32;        // tokens per CTA
+constexpr int kHStages = 4;
+constexpr int kHeadsPerLaunch = 4;
+
+template <int DEP>
+__device__ __forceinline__ void nibbles(uint32_t (&o)[4], uint32_t w0, uint32_t w1, uint32_t w2, uint32_t w3) {
+  o[0] = nibble_word<DEP, 0>(w0, w1, w2, w3);
+  o[1] = nibble_word<DEP, 1>(w0, w1, w2, w3);
+  o[2] = nibble_word<DEP, 2>(w0, w1, w2, w3);
+  o[3] = nibble_word<DEP, 3>(w0, w1, w2, w3);
+}
+
+// acc[4m + k] holds tokens (4m + k, 4m + 16 + k); mbyte keeps this head's prefix bits.
+__device__ __forceinline__ void head_terms(float2* acc, const uint32_t (&o)[4], uint32_t mbyte, float2 d16,
+                                           float2 lop, float2 q2) {
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const uint32_t e = ((o[k] << 3) & mbyte) | 0x80808080u;
+    const uint32_t od = ((o[k] >> 1) & mbyte) | 0x80808080u;
+    const float2 f0 = make_float2(prefix_float<0>(e), prefix_float<2>(e));
+    const float2 f1 = make_float2(prefix_float<0>(od), prefix_float<2>(od));
+    const float2 f2 = make_float2(prefix_float<1>(e), prefix_float<3>(e));
+    const float2 f3 = make_float2(prefix_float<1>(od), prefix_float<3>(od));
+    acc[0 + k] = __ffma2_rn(q2, __ffma2_rn(d16, f0, lop), acc[0 + k]);
+    acc[4 + k] = __ffma2_rn(q2, __ffma2_rn(d16, f1, lop), acc[4 + k]);
+    acc[8 + k] = __ffma2_rn(q2, __ffma2_rn(d16, f2, lop), acc[8 + k]);
+    acc[12 + k] = __ffma2_rn(q2, __ffma2_rn(d16, f3, lop), acc[12 + k]);
+  }
+}
+
+// NH heads h0..h0+NH-1 of every KV row.  kMax: write max over the heads (and over
+// the scores already there when `combine`); else each head's own score row.
+template <int NH, bool kMax, bool kHist>
+__global__ void __launch_bounds__(kHThreads, 2)
+    scan_heads_kernel(const uint32_t* __restrict__ planes, const __half2* __restrict__ meta,
+                      const uint8_t* __restrict__ bits, const float* __restrict__ qh, float* __restrict__ scores,
+                      uint32_t* __restrict__ hist, int group, int h0, int combine, int64_t n, int64_t nsb, int log2S,
+                      int64_t nblk) {
+  __shared__ int s_ch[kD];
+  __shared__ int s_dep[kD];
+  __shared__ int s_hb[NH][kD];
+  __shared__ float s_hq[NH][kD];
+  __shared__ int s_wcnt[kD / 32];
+  __shared__ uint32_t s_w[kHStages][kPlanes][kHThreads];
+  __shared__ __half2 s_m[kHStages][kHThreads];
+  __shared__ uint32_t s_hist[kHist ? kHistBins : 1];
+
+  const int r = blockIdx.y;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+
+  // Channel tid: every head's depth and query, and the union depth.
+  int hb[NH];
+  float hq[NH];
+  int dep = 0;
+#pragma unroll
+  for (int h = 0; h < NH; ++h) {
+    const int64_t row = int64_t(r) * group + h0 + h;
+    hb[h] = min(int(bits[row * kD + tid]), kPlanes);
+    hq[h] = qh[row * kD + tid];
+    dep = max(dep, hb[h]);
+  }
+  const unsigned ball = __ballot_sync(0xffffffffu, dep > 0);
+  if (lane == 0) s_wcnt[warp] = __popc(ball);
+  if constexpr (kHist) {
+    for (int i = tid; i < kHistBins; i += kHThreads) s_hist[i] = 0u;
+  }
+  __syncthreads();
+  int nact = 0;
+#pragma unroll
+  for (int w = 0; w < kD / 32; ++w) nact += s_wcnt[w];
+  if (dep > 0) {
+    int off = 0;
+    for (int w = 0; w < warp; ++w) off += s_wcnt[w];
+    const int pos = off + __popc(ball & ((1u << lane) - 1u));
+    s_ch[pos] = tid;
+    s_dep[pos] = dep;
+#pragma unroll
+    for (int h = 0; h < NH; ++h) {
+      s_hb[h][pos] = hb[h];
+      s_hq[h][pos] = hq[h];
+    }
+  }
+  __syncthreads();
+
+  const int64_t t0 = (int64_t(blockIdx.x) * kHThreads + tid) * 32;
+  const bool valid = t0 < n;
+  const int64_t S = int64_t(1) << log2S;
+  const int64_t run = S >> 5;
+  const int64_t tt = valid ? t0 : 0;
+  const uint32_t* pb = planes + (int64_t(r) * nsb + (tt >> log2S)) * (kD * kPlanes) * run + ((tt & (S - 1)) >> 5);
+  const __half2* mb = meta + int64_t(r) * kD * nblk + (tt >> 7);
+
+  auto issue = [&](int a) {
+    if (a < nact && valid) {
+      const int st = a % kHStages;
+      const int c = s_ch[a], d = s_dep[a];
+      const uint32_t* p = pb + int64_t(c) * kPlanes * run;
+      cp_async<4>(&s_w[st][0][tid], p);
+      if (d > 1) cp_async<4>(&s_w[st][1][tid], p + run);
+      if (d > 2) cp_async<4>(&s_w[st][2][tid], p + 2 * run);
+      if (d > 3) cp_async<4>(&s_w[st][3][tid], p + 3 * run);
+      cp_async<4>(&s_m[st][tid], mb + int64_t(c) * nblk);
+    }
+    cp_async_commit();
+  };
+
+  float2 acc[NH][16];
+#pragma unroll
+  for (int h = 0; h < NH; ++h)
+#pragma unroll
+    for (int i = 0; i < 16; ++i) acc[h][i] = make_float2(0.0f, 0.0f);
+
+#pragma unroll
+  for (int a = 0; a < kHStages - 1; ++a) issue(a);
+  for (int a = 0; a < nact; ++a) {
+    issue(a + kHStages - 1);
+    cp_async_wait<kHStages - 1>();
+    if (!valid) continue;
+    const int st = a % kHStages;
+    const int d = s_dep[a];
+    const __half2 mh = s_m[st][tid];
+    const float lo = __low2float(mh), dl = __high2float(mh);
+    const float2 d16 = make_float2(16.0f * dl, 16.0f * dl);
+    uint32_t o[4];
+    const uint32_t w0 = s_w[st][0][tid];
+    switch (d) {  // union depth, uniform across the CTA
+      case 1: nibbles<1>(o, w0, 0u, 0u, 0u); break;
+      case 2: nibbles<2>(o, w0, s_w[st][1][tid], 0u, 0u); break;
+      case 3: nibbles<3>(o, w0, s_w[st][1][tid], s_w[st][2][tid], 0u); break;
+      default: nibbles<4>(o, w0, s_w[st][1][tid], s_w[st][2][tid], s_w[st][3][tid]); break;
+    }
+#pragma unroll
+    for (int h = 0; h < NH; ++h) {
+      const int b = s_hb[h][a];
+      if (b == 0) continue;  // uniform
+      const uint32_t mbyte = ((((0xF0u >> b) & 0xFu) << 3) * 0x01010101u);
+      const float half_m1 = float((1 << (4 - b)) - 1) * 0.5f;
+      const float lo1 = fmaf(dl, half_m1 - 16.0f, lo);
+      const float q = s_hq[h][a];
+      head_terms(acc[h], o, mbyte, d16, make_float2(lo1, lo1), make_float2(q, q));
+    }
+  }
+  cp_async_wait<0>();
+
+  if (valid) {
+    const bool full = t0 + 32 <= n;
+    if constexpr (kMax) {
+      float* out = scores + int64_t(r) * n + t0;
+      float v[32];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        float x = acc[0][i].x, y = acc[0][i].y;
+#pragma unroll
+        for (int h = 1; h < NH; ++h) {
+          x = fmaxf(x, acc[h][i].x);
+          y = fmaxf(y, acc[h][i].y);
+        }
+        v[i] = x;
+        v[16 + i] = y;
+      }
+      if (combine) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          if (t0 + i < n) v[i] = fmaxf(v[i], out[i]);
+      }
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        if (full || t0 + i < n) {
+          out[i] = v[i];
+          if constexpr (kHist) atomicAdd(&s_hist[score_key(v[i]) >> (32 - kHistBits)], 1u);
+        }
+      }
+    } else {
+#pragma unroll
+      for (int h = 0; h < NH; ++h) {
+        float* out = scores + (int64_t(r) * group + h0 + h) * n + t0;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          if (full || t0 + i < n) out[i] = acc[h][i].x;
+          if (full || t0 + 16 + i < n) out[16 + i] = acc[h][i].y;
+        }
+      }
+    }
+  }
+  if constexpr (kHist) {
+    __syncthreads();
+    uint32_t* gh = hist + int64_t(r) * kHistBins;
+    for (int i = tid; i < kHistBins; i += kHThreads) {
+      const uint32_t v = s_hist[i];
+      if (v) atomicAdd(gh + i, v);
+    }
+  }
+}
+
+template <int NH>
+cudaError_t launch_chunk(const IndexGeom& g, int group, int h0, bool max_mode, bool last, const uint32_t* planes,
+                         const __half2* meta, const uint8_t* bits, const float* qh, float* scores, uint32_t* hist,
+                         cudaStream_t st) {
+  const dim3 grid{unsigned((g.n + kHTile - 1) / kHTile), unsigned(g.rows), 1u};
+  const int combine = h0 > 0;
+  if (!max_mode)
+    scan_heads_kernel<NH, false, false><<<grid, kHThreads, 0, st>>>(planes, meta, bits, qh, scores, nullptr, group,
+                                                                    h0, combine, g.n, g.nsb, g.log2S, g.nblk);
+  else if (last && hist)
+    scan_heads_kernel<NH, true, true><<<grid, kHThreads, 0, st>>>(planes, meta, bits, qh, scores, hist, group, h0,
+                                                                  combine, g.n, g.nsb, g.log2S, g.nblk);
+  else
+    scan_heads_kernel<NH, true, false><<<grid, kHThreads, 0, st>>>(planes, meta, bits, qh, scores, nullptr, group,
+                                                                   h0, combine, g.n, g.nsb, g.log2S, g.nblk);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_scan_heads(const IndexGeom& g, int group, int mode, const uint32_t* planes, const __half2* meta,
+                              const uint8_t* bits, const float* qh, float* scores, uint32_t* hist, cudaStream_t st) {
+  const bool max_mode = mode == FATHOM_GQA_MAX;
+  for (int h0 = 0; h0 < group; h0 += kHeadsPerLaunch) {
+    const int nh = group - h0 < kHeadsPerLaunch ? group - h0 : kHeadsPerLaunch;
+    const bool last = h0 + nh == group;
+    cudaError_t e;
+    switch (nh) {
+      case 1: e = launch_chunk<1>(g, group, h0, max_mode, last, planes, meta, bits, qh, scores, hist, st); break;
+      case 2: e = launch_chunk<2>(g, group, h0, max_mode, last, planes, meta, bits, qh, scores, hist, st); break;
+      case 3: e = launch_chunk<3>(g, group, h0, max_mode, last, planes, meta, bits, qh, scores, hist, st); break;
+      default: e = launch_chunk<4>(g, group, h0, max_mode, last, planes, meta, bits, qh, scores, hist, st); break;
+    }
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+}  // namespace fathom
+
+using namespace fathom;
+
+extern "C" int fathom_scan_heads(const fathom_index_desc* desc, int group, int mode, const uint32_t* planes,
+                                 const uint16_t* meta, const uint8_t* bits, const float* qh, float* scores,
+                                 void* stream) {
+  clear_error();
+  IndexGeom g;
+  FATHOM_TRY(index_geom(desc, &g));
+  if (g.rows > 65535) return set_error(FATHOM_EINVAL, "rows > 65535");
+  if (group < 1 || group > 64) return set_error(FATHOM_EINVAL, "group must be 1..64");
+  if (mode != FATHOM_GQA_PER_HEAD && mode != FATHOM_GQA_MAX)
+    return set_error(FATHOM_EINVAL, "mode must be FATHOM_GQA_PER_HEAD or FATHOM_GQA_MAX (got %d)", mode);
+  const void *dP, *dM, *dB, *dQ, *dS;
+  FATHOM_TRY(device_view(planes, "planes", &dP));
+  FATHOM_TRY(device_view(meta, "meta", &dM));
+  FATHOM_TRY(device_view(bits, "bits", &dB));
+  FATHOM_TRY(device_view(qh, "qh", &dQ));
+  FATHOM_TRY(device_view(scores, "scores", &dS));
+  if ((reinterpret_cast<uintptr_t>(dP) & 3) != 0 || (reinterpret_cast<uintptr_t>(dM) & 3) != 0)
+    return set_error(FATHOM_EINVAL, "planes and meta must be 4-byte aligned");
+  FATHOM_TRY_CUDA(launch_scan_heads(g, group, mode, (const uint32_t*)dP, (const __half2*)dM, (const uint8_t*)dB,
+                                    (const float*)dQ, (float*)dS, nullptr, as_stream(stream)));
+  return FATHOM_OK;
+}

@@ -20,17 +20,23 @@ struct StepWs {
   size_t end;
 };
 
-StepWs carve_step(void* base, int rows, int group, int64_t n, int64_t k) {
+// gqa: FATHOM_GQA_* -- the per-head modes keep depths and queries per query head,
+// and FATHOM_GQA_PER_HEAD also scores and selects per query head.
+StepWs carve_step(void* base, int rows, int group, int64_t n, int64_t k, int gqa = FATHOM_GQA_SUM) {
+  const int64_t arows = gqa == FATHOM_GQA_SUM ? rows : int64_t(rows) * group;
+  const int64_t srows = gqa == FATHOM_GQA_PER_HEAD ? int64_t(rows) * group : rows;
   Carve cv(base, ~size_t(0));
   StepWs w;
-  w.bits = cv.take<uint8_t>(size_t(rows) * kD);
-  w.qbar = cv.take<float>(size_t(rows) * kD);
-  w.scores = cv.take<float>(size_t(rows) * n);
-  w.topk = cv.take<char>(topk_ws_bytes(rows, n, k));
+  w.bits = cv.take<uint8_t>(size_t(arows) * kD);
+  w.qbar = cv.take<float>(size_t(arows) * kD);
+  w.scores = cv.take<float>(size_t(srows) * n);
+  w.topk = cv.take<char>(topk_ws_bytes(int(srows), n, k));
   w.attn = cv.take<char>(attn_ws_bytes(rows, group, k));
   w.end = cv.off;
   return w;
 }
+
+bool valid_gqa(int m) { return m == FATHOM_GQA_SUM || m == FATHOM_GQA_PER_HEAD || m == FATHOM_GQA_MAX; }
 
 }  // namespace
 }  // namespace fathom
@@ -45,7 +51,8 @@ int fathom_decode_step_workspace_bytes(const fathom_step_desc* s, size_t* bytes)
   IndexGeom g;
   FATHOM_TRY(index_geom(&s->index, &g));
   if (s->group < 1 || s->group > 8 || s->k < 1) return set_error(FATHOM_EINVAL, "group (1..8) or k out of range");
-  *bytes = carve_step(nullptr, g.rows, s->group, g.n, s->k).end + 256;
+  if (!valid_gqa(s->gqa_mode)) return set_error(FATHOM_EINVAL, "gqa_mode %d invalid", s->gqa_mode);
+  *bytes = carve_step(nullptr, g.rows, s->group, g.n, s->k, s->gqa_mode).end + 256;
   return FATHOM_OK;
 }
 
@@ -58,7 +65,14 @@ int fathom_decode_step(const fathom_step_desc* s, void* workspace, size_t ws_byt
   if (s->group < 1 || s->group > 8) return set_error(FATHOM_EINVAL, "group must be 1..8");
   if (s->k < 1 || s->k > 0x7fffffff) return set_error(FATHOM_EINVAL, "k out of range");
   if (!valid_dtype(s->q_dtype) || !valid_dtype(s->kv_dtype)) return set_error(FATHOM_EINVAL, "invalid dtype");
-  if (!s->budgets && (s->budget < 0 || s->budget > kD * kPlanes))
+  if (s->sparq_r < 0 || s->sparq_r > kD) return set_error(FATHOM_EINVAL, "sparq_r %d outside [0, 128]", s->sparq_r);
+  if (!valid_gqa(s->gqa_mode)) return set_error(FATHOM_EINVAL, "gqa_mode %d invalid", s->gqa_mode);
+  if (s->gqa_mode != FATHOM_GQA_SUM && s->sparq_r != 0)
+    return set_error(FATHOM_EINVAL, "the per-head GQA modes take the water-filling allocation (sparq_r must be 0)");
+  const int gqa = s->gqa_mode;
+  if (gqa == FATHOM_GQA_PER_HEAD && int64_t(g.rows) * s->group > 65535)
+    return set_error(FATHOM_EINVAL, "rows*group > 65535");
+  if (s->sparq_r == 0 && !s->budgets && (s->budget < 0 || s->budget > kD * kPlanes))
     return set_error(FATHOM_EINVAL, "budget %d outside [0, 512]", s->budget);
   const void *dP, *dM, *dVar, *dBud, *dq, *dK, *dV, *dI, *dO, *dB, *dSt, *dW;
   FATHOM_TRY(device_view(s->planes, "planes", &dP));
@@ -74,7 +88,7 @@ int fathom_decode_step(const fathom_step_desc* s, void* workspace, size_t ws_byt
   FATHOM_TRY(device_view(s->status, "status", &dSt, true));
   FATHOM_TRY(device_view(workspace, "workspace", &dW));
   if (!dO && !dB) return set_error(FATHOM_EINVAL, "out and out_bf16 are both NULL");
-  StepWs w = carve_step(const_cast<void*>(dW), g.rows, s->group, g.n, s->k);
+  StepWs w = carve_step(const_cast<void*>(dW), g.rows, s->group, g.n, s->k, gqa);
   if (reinterpret_cast<uintptr_t>(dW) & 255) return set_error(FATHOM_EINVAL, "workspace must be 256-byte aligned");
   if (ws_bytes < w.end + 256) return set_error(FATHOM_ENOMEM, "workspace %zu < %zu bytes", ws_bytes, w.end + 256);
   if (s->kv_stride < kD || (s->kv_stride & 3)) return set_error(FATHOM_EINVAL, "kv_stride must be >= 128, a multiple of 4");
@@ -83,11 +97,31 @@ int fathom_decode_step(const fathom_step_desc* s, void* workspace, size_t ws_byt
       (reinterpret_cast<uintptr_t>(dP) & 3) || (reinterpret_cast<uintptr_t>(dM) & 3))
     return set_error(FATHOM_EINVAL, "misaligned planes, meta, K or V");
   cudaStream_t st = as_stream(stream);
+  if (gqa != FATHOM_GQA_SUM) {
+    // per-head depths; PER_HEAD scores and selects rows*group rows (histogram by the top-k's own pass)
+    const int srows = gqa == FATHOM_GQA_PER_HEAD ? g.rows * s->group : g.rows;
+    const bool use_hist = gqa == FATHOM_GQA_MAX && s->k < g.n;
+    uint32_t* hist = use_hist ? topk_hist_ptr(w.topk, srows, g.n, s->k) : nullptr;
+    if (hist) FATHOM_TRY_CUDA(cudaMemsetAsync(hist, 0, size_t(srows) * kHistBins * sizeof(uint32_t), st));
+    FATHOM_TRY_CUDA(launch_allocate_heads(g.rows, s->group, dq, s->q_dtype, (const float*)dVar,
+                                          (const uint16_t*)dBud, s->budget, w.bits, w.qbar, (int32_t*)dSt, st));
+    FATHOM_TRY_CUDA(launch_scan_heads(g, s->group, gqa, (const uint32_t*)dP, (const __half2*)dM, w.bits, w.qbar,
+                                      w.scores, hist, st));
+    FATHOM_TRY_CUDA(launch_topk(srows, g.n, s->k, w.scores, (int32_t*)dI, nullptr, w.topk, use_hist, st));
+    FATHOM_TRY_CUDA(launch_attn(g.rows, s->group, g.n, s->k, dq, s->q_dtype, dK, dV, s->kv_dtype, s->kv_stride,
+                                (const int32_t*)dI, (float*)dO, (uint16_t*)dB, w.attn, st,
+                                gqa == FATHOM_GQA_PER_HEAD));
+    return FATHOM_OK;
+  }
   const bool use_hist = s->k < g.n;
   uint32_t* hist = use_hist ? topk_hist_ptr(w.topk, g.rows, g.n, s->k) : nullptr;
   if (hist) FATHOM_TRY_CUDA(cudaMemsetAsync(hist, 0, size_t(g.rows) * kHistBins * sizeof(uint32_t), st));
-  FATHOM_TRY_CUDA(launch_allocate(g.rows, s->group, dq, s->q_dtype, (const float*)dVar, (const uint16_t*)dBud,
-                                  s->budget, w.bits, w.qbar, (int32_t*)dSt, st));
+  if (s->sparq_r > 0)
+    FATHOM_TRY_CUDA(launch_allocate_sparq(g.rows, s->group, dq, s->q_dtype, s->sparq_r, w.bits, w.qbar,
+                                          (int32_t*)dSt, st));
+  else
+    FATHOM_TRY_CUDA(launch_allocate(g.rows, s->group, dq, s->q_dtype, (const float*)dVar, (const uint16_t*)dBud,
+                                    s->budget, w.bits, w.qbar, (int32_t*)dSt, st));
   FATHOM_TRY_CUDA(launch_scan(g, (const uint32_t*)dP, (const __half2*)dM, w.bits, w.qbar, w.scores, hist, st));
   FATHOM_TRY_CUDA(launch_topk(g.rows, g.n, s->k, w.scores, (int32_t*)dI, nullptr, w.topk, use_hist, st));
   FATHOM_TRY_CUDA(launch_attn(g.rows, s->group, g.n, s->k, dq, s->q_dtype, dK, dV, s->kv_dtype, s->kv_stride, (const int32_t*)dI,

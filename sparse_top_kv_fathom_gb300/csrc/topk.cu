@@ -12,10 +12,11 @@
 //      candidates (appended to a bounded candidate list);
 //   4. per row, one CTA finishes the select on the candidates (two more 10-bit
 //      digits give the exact threshold key T), hands out the keys equal to T
-//      to the lowest indices (a radix select on the index), and sorts the k
-//      chosen indices.
-// If the candidate list overflows, or k is larger than the sort buffer, step 4
-// instead runs the same definition directly over the row's scores (3 digit
+//      to the lowest indices (a radix select on the index), and puts the k
+//      chosen indices in order: through a bitmap of the row in shared memory
+//      (n <= 2^20: set bits, popcount prefix, emit), else a bitonic sort.
+// If the candidate list overflows, or k is larger than the sort buffer when
+// the row is too long for the bitmap, step 4 instead runs the same definition directly over the row's scores (3 digit
 // passes, an ordered count of the keys equal to T, then an ordered compaction);
 // both routes produce the identical result.
 #include "common.cuh"
@@ -25,9 +26,12 @@ namespace {
 
 constexpr int kFinThreads = 1024;
 constexpr int kSortMax = 8192;    // largest k sorted in shared memory
-constexpr int kCandSmem = 16384;  // candidates staged in shared memory by the final select
+constexpr int kCandSmem = 8192;   // candidates staged in shared memory by the final select
+constexpr int kBitmapWords = 32768;  // n <= 2^20: the chosen indices leave the final select through a bitmap
+constexpr int kRegionA = kBitmapWords > kSortMax ? kBitmapWords : kSortMax;  // bitmap or sort buffer (words)
 constexpr int kPassThreads = 256;
 constexpr int kPassItems = 16;  // items per thread in the histogram / compaction passes
+constexpr int kCompactCtasPerSm = 3;  // resident CTAs per SM of the persistent compaction pass
 
 struct RowState {
   uint32_t b1;      // bin (top 12 key bits) holding the k-th largest key
@@ -179,63 +183,142 @@ __global__ void __launch_bounds__(kFinThreads) topk_bin_kernel(int64_t k, const 
   }
 }
 
-__global__ void __launch_bounds__(kPassThreads) topk_compact_kernel(int64_t n, int64_t k, int64_t cap,
+// Persistent pass over all (row, tile) pairs: keys in bins above b1 go to the
+// row's sure list, keys in b1 to its candidate list.  Per tile, every thread
+// marks its hits in two bit masks, one block scan of the packed counts gives
+// each thread its slots, and one thread reserves the tile's slots in each list
+// with a single atomic; the next tile's scores are in flight meanwhile.
+template <bool kVec>
+struct CompactTile {
+  static constexpr int kItems = kPassItems;
+  static constexpr int kTile = kPassThreads * kItems;
+  // position of a thread's item i inside the tile
+  __device__ static int pos(int i) {
+    return kVec ? 4 * ((i >> 2) * kPassThreads + int(threadIdx.x)) + (i & 3) : i * kPassThreads + int(threadIdx.x);
+  }
+  __device__ static void load(const float* __restrict__ s, int64_t n, int64_t t0, float (&v)[kItems]) {
+    if (kVec && t0 + kTile <= n) {
+#pragma unroll
+      for (int j = 0; j < kItems / 4; ++j) {
+        const float4 x = __ldg(reinterpret_cast<const float4*>(s + t0) + j * kPassThreads + threadIdx.x);
+        v[4 * j] = x.x;
+        v[4 * j + 1] = x.y;
+        v[4 * j + 2] = x.z;
+        v[4 * j + 3] = x.w;
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < kItems; ++i) {
+        const int64_t t = t0 + pos(i);
+        v[i] = t < n ? __ldg(s + t) : 0.0f;
+      }
+    }
+  }
+};
+
+// Key of a score without branches: sign-dependent flip, -0.0 moved onto +0.0's key
+// (the same map as score_key).
+__device__ __forceinline__ uint32_t score_key_fast(float v) {
+  const uint32_t u = __float_as_uint(v);
+  const uint32_t k = u ^ (uint32_t(int32_t(u) >> 31) | 0x80000000u);
+  return k + uint32_t(u == 0x80000000u);
+}
+
+template <bool kVec>
+__global__ void __launch_bounds__(kPassThreads, kCompactCtasPerSm) topk_compact_kernel(int64_t n, int64_t k, int64_t cap, int rows,
                                                                     const float* __restrict__ scores,
                                                                     RowState* __restrict__ state,
                                                                     int32_t* __restrict__ sure,
                                                                     uint32_t* __restrict__ cand_key,
                                                                     int32_t* __restrict__ cand_idx) {
-  // Gather this tile's sure winners and candidates in shared memory first, then
-  // reserve space in the row's global lists with one atomic per list per CTA.
-  constexpr int kTileItems = kPassThreads * kPassItems;
-  __shared__ int32_t s_si[kTileItems];
-  __shared__ uint32_t s_ck[kTileItems];
-  __shared__ int32_t s_ci[kTileItems];
-  __shared__ int32_t s_ns, s_nc, s_bs, s_bc;
-  const int r = blockIdx.y;
-  const uint32_t b1 = state[r].b1;
-  if (threadIdx.x == 0) s_ns = s_nc = 0;
-  __syncthreads();
-  const int64_t t0 = int64_t(blockIdx.x) * kTileItems;
-  const float* s = scores + int64_t(r) * n;
-  float sv[kPassItems];  // all loads in flight before any is used
+  using C = CompactTile<kVec>;
+  static_assert(C::kItems <= 16 && C::kTile < 65536, "packed 16-bit counts");
+  constexpr int kWarps = kPassThreads / 32;
+  __shared__ uint32_t s_warp[2][kWarps];  // inclusive scan of the warps' packed counts, per tile parity
+  __shared__ int32_t s_base[2][2];        // the tile's first slot in the sure and candidate lists
+  const int64_t tiles_row = (n + C::kTile - 1) / C::kTile;
+  const int64_t total = tiles_row * rows;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int64_t g = blockIdx.x;
+  if (g >= total) return;
+  float cur[C::kItems];
+  C::load(scores + (g / tiles_row) * n, n, (g % tiles_row) * C::kTile, cur);
+  for (int par = 0; g < total; g += gridDim.x, par ^= 1) {
+    const int64_t r = g / tiles_row;
+    const int64_t t0 = (g % tiles_row) * C::kTile;
+    float nxt[C::kItems];
+    const int64_t gn = g + gridDim.x;
+    if (gn < total) C::load(scores + (gn / tiles_row) * n, n, (gn % tiles_row) * C::kTile, nxt);
+    // keys in (khi, ~0] are sure, keys in [klo, khi] candidates
+    const uint32_t b1 = __ldg(&state[r].b1);
+    const uint32_t klo = b1 << (32 - kHistBits), khi = klo | ((1u << (32 - kHistBits)) - 1u);
+    const int lim = n - t0 < C::kTile ? int(n - t0) : C::kTile;  // items of this tile inside the row
+    uint32_t ns = 0u, nc = 0u;
+    if (lim == C::kTile) {
 #pragma unroll
-  for (int i = 0; i < kPassItems; ++i) {
-    const int64_t t = t0 + int64_t(i) * kPassThreads + threadIdx.x;
-    sv[i] = t < n ? __ldg(s + t) : 0.0f;
-  }
+      for (int i = 0; i < C::kItems; ++i) {
+        const uint32_t key = score_key_fast(cur[i]);
+        ns += key > khi;
+        nc += key >= klo && key <= khi;
+      }
+    } else {
 #pragma unroll
-  for (int i = 0; i < kPassItems; ++i) {
-    const int64_t t = t0 + int64_t(i) * kPassThreads + threadIdx.x;
-    uint32_t key = 0u;
-    if (t < n) key = score_key(sv[i]);
-    const uint32_t bin = key >> (32 - kHistBits);
-    const bool is_sure = (t < n) && bin > b1;
-    const bool is_cand = (t < n) && bin == b1;
-    int slot;
-    warp_append(is_sure, &s_ns, &slot);
-    if (is_sure) s_si[slot] = int32_t(t);
-    warp_append(is_cand, &s_nc, &slot);
-    if (is_cand) {
-      s_ck[slot] = key;
-      s_ci[slot] = int32_t(t);
+      for (int i = 0; i < C::kItems; ++i) {
+        const uint32_t key = score_key_fast(cur[i]);
+        const bool in = C::pos(i) < lim;
+        ns += in && key > khi;
+        nc += in && key >= klo && key <= khi;
+      }
     }
-  }
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    s_bs = s_ns ? atomicAdd(&state[r].sure_cnt, s_ns) : 0;
-    s_bc = s_nc ? atomicAdd(&state[r].cand_cnt, s_nc) : 0;
-  }
-  __syncthreads();
-  for (int i = threadIdx.x; i < s_ns; i += kPassThreads) {
-    const int64_t slot = int64_t(s_bs) + i;
-    if (slot < k) sure[int64_t(r) * k + slot] = s_si[i];
-  }
-  for (int i = threadIdx.x; i < s_nc; i += kPassThreads) {
-    const int64_t slot = int64_t(s_bc) + i;
-    if (slot < cap) {
-      cand_key[int64_t(r) * cap + slot] = s_ck[i];
-      cand_idx[int64_t(r) * cap + slot] = s_ci[i];
+    const uint32_t mine = ns | (nc << 16);
+    uint32_t x = mine;  // inclusive warp scan of the packed (sure, candidate) counts
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    if (lane == 31) s_warp[par][warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+      uint32_t v = lane < kWarps ? s_warp[par][lane] : 0u;
+#pragma unroll
+      for (int o = 1; o < kWarps; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += y;
+      }
+      if (lane < kWarps) s_warp[par][lane] = v;
+      if (lane == kWarps - 1) {
+        const int ts = int(v & 0xFFFFu), tc = int(v >> 16);
+        s_base[par][0] = ts ? atomicAdd(&state[r].sure_cnt, ts) : 0;
+        s_base[par][1] = tc ? atomicAdd(&state[r].cand_cnt, tc) : 0;
+      }
+    }
+    __syncthreads();
+    if (mine) {  // rare: this thread holds hits; find them again and write them
+      const uint32_t excl = x - mine + (warp ? s_warp[par][warp - 1] : 0u);
+      int64_t ps = int64_t(s_base[par][0]) + (excl & 0xFFFFu);
+      int64_t pc = int64_t(s_base[par][1]) + (excl >> 16);
+#pragma unroll
+      for (int i = 0; i < C::kItems; ++i) {
+        const uint32_t key = score_key_fast(cur[i]);
+        const int p = C::pos(i);
+        if (p >= lim) continue;
+        const int32_t t = int32_t(t0 + p);
+        if (key > khi) {
+          if (ps < k) sure[r * k + ps] = t;
+          ++ps;
+        } else if (key >= klo) {
+          if (pc < cap) {
+            cand_key[r * cap + pc] = key;
+            cand_idx[r * cap + pc] = t;
+          }
+          ++pc;
+        }
+      }
+    }
+    if (gn < total) {
+#pragma unroll
+      for (int i = 0; i < C::kItems; ++i) cur[i] = nxt[i];
     }
   }
 }
@@ -364,10 +447,10 @@ __global__ void __launch_bounds__(kFinThreads) topk_final_kernel(int64_t n, int6
                                                                  const uint32_t* __restrict__ cand_key,
                                                                  const int32_t* __restrict__ cand_idx,
                                                                  int32_t* __restrict__ idx, float* __restrict__ vals) {
-  extern __shared__ int32_t s_dyn[];  // kSortMax sort entries, then kCandSmem keys and indices
+  extern __shared__ int32_t s_dyn[];  // region A (sort buffer or bitmap), then kCandSmem keys and indices
   int32_t* s_sel = s_dyn;
-  uint32_t* s_ck = reinterpret_cast<uint32_t*>(s_dyn + kSortMax);
-  int32_t* s_ci = s_dyn + kSortMax + kCandSmem;
+  uint32_t* s_ck = reinterpret_cast<uint32_t*>(s_dyn + kRegionA);
+  int32_t* s_ci = s_dyn + kRegionA + kCandSmem;
   __shared__ uint32_t h[kFinThreads];
   __shared__ int s_out[2];
   __shared__ int s_fill;
@@ -378,7 +461,8 @@ __global__ void __launch_bounds__(kFinThreads) topk_final_kernel(int64_t n, int6
   int32_t* oi = idx + int64_t(r) * k;
   float* ov = vals ? vals + int64_t(r) * k : nullptr;
   const int m = st.cand_cnt;
-  if (m > cap || k > kSortMax) {
+  const int64_t words = (n + 31) >> 5;
+  if (m > cap || (k > kSortMax && words > kBitmapWords)) {
     select_row_direct(n, k, s, oi, ov, h, s_out);
     return;
   }
@@ -481,6 +565,61 @@ __global__ void __launch_bounds__(kFinThreads) topk_final_kernel(int64_t n, int6
       cut = int32_t(ip);
     }
   }
+  if (words <= kBitmapWords) {
+    // --- mark the k chosen indices in a bitmap (and the words touched in a second
+    // one), then emit them in index order
+    uint32_t* bm = reinterpret_cast<uint32_t*>(s_dyn);
+    uint32_t* touch = h;  // 1024 words: one bit per bitmap word
+    const int64_t words4 = (words + 3) >> 2;
+    for (int64_t i = tid; i < words4; i += kFinThreads) reinterpret_cast<uint4*>(bm)[i] = make_uint4(0u, 0u, 0u, 0u);
+    touch[tid] = 0u;
+    __syncthreads();
+    for (int i = tid; i < st.above; i += kFinThreads) {
+      const int32_t t = sure[int64_t(r) * k + i];
+      if (uint32_t(t) < uint32_t(n)) {
+        atomicOr(&bm[t >> 5], 1u << (t & 31));
+        atomicOr(&touch[t >> 10], 1u << ((t >> 5) & 31));
+      }
+    }
+    for (int i = tid; i < m; i += kFinThreads) {
+      const uint32_t key = ck[i];
+      const int32_t t = ci[i];
+      if (key > T || (key == T && t <= cut)) {
+        atomicOr(&bm[t >> 5], 1u << (t & 31));
+        atomicOr(&touch[t >> 10], 1u << ((t >> 5) & 31));
+      }
+    }
+    __syncthreads();
+    // thread tid owns words [w0, w0 + per); its touched words are bits w0.. of `touch`
+    const int per = int((words + kFinThreads - 1) / kFinThreads);  // <= 32
+    const int w0 = tid * per;
+    uint32_t nz = 0u;
+    if (w0 < words) {
+      const int tw = w0 >> 5, sh = w0 & 31;
+      uint64_t win = touch[tw];
+      if (tw + 1 < kFinThreads) win |= uint64_t(touch[tw + 1]) << 32;
+      nz = uint32_t(win >> sh) & (per == 32 ? 0xFFFFFFFFu : ((1u << per) - 1u));
+    }
+    int cnt = 0;
+    for (uint32_t z = nz; z; z &= z - 1u) cnt += __popc(bm[w0 + __ffs(z) - 1]);
+    int tot;
+    int pos = block_exclusive_scan(cnt, &tot);
+    while (nz) {
+      const int j = __ffs(nz) - 1;
+      nz &= nz - 1u;
+      uint32_t b = bm[w0 + j];
+      while (b) {
+        const int32_t t = int32_t(w0 + j) * 32 + (__ffs(b) - 1);
+        b &= b - 1u;
+        if (pos < k) {
+          oi[pos] = t;
+          if (ov) ov[pos] = s[t];
+        }
+        ++pos;
+      }
+    }
+    return;
+  }
   // --- gather the k chosen indices and sort them
   int pow2 = 1;
   while (pow2 < k) pow2 <<= 1;
@@ -490,12 +629,12 @@ __global__ void __launch_bounds__(kFinThreads) topk_final_kernel(int64_t n, int6
   for (int i = tid; i < st.above; i += kFinThreads) s_sel[i] = sure[int64_t(r) * k + i];
   if (tid == 0) s_fill = st.above;
   __syncthreads();
-  for (int i = tid; i < m; i += kFinThreads) {
-    const uint32_t key = ck[i];
-    if (key > T || (key == T && ci[i] <= cut)) {
-      const int p = atomicAdd(&s_fill, 1);
-      s_sel[p] = ci[i];
-    }
+  for (int i0 = 0; i0 < m; i0 += kFinThreads) {  // whole warps: one shared atomic per warp
+    const int i = i0 + tid;
+    const bool take = i < m && (ck[i] > T || (ck[i] == T && ci[i] <= cut));
+    int p;
+    warp_append(take, &s_fill, &p);
+    if (take) s_sel[p] = ci[i];
   }
   __syncthreads();
   bitonic_sort(s_sel, pow2);
@@ -534,9 +673,19 @@ cudaError_t launch_topk(int rows, int64_t n, int64_t k, const float* scores, int
   }
   topk_bin_kernel<<<rows, kFinThreads, 0, st>>>(k, w.hist, w.state);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  topk_compact_kernel<<<pgrid, kPassThreads, 0, st>>>(n, k, w.cap, scores, w.state, w.sure, w.cand_key, w.cand_idx);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  const size_t smem = (kSortMax + 2 * kCandSmem) * sizeof(int32_t);
+  {
+    const int64_t ctiles = tiles * rows;
+    const int64_t resident = int64_t(num_sms()) * kCompactCtasPerSm;
+    const unsigned cgrid = unsigned(ctiles < resident ? ctiles : resident);
+    if (n % 4 == 0 && (reinterpret_cast<uintptr_t>(scores) & 15) == 0)
+      topk_compact_kernel<true><<<cgrid, kPassThreads, 0, st>>>(n, k, w.cap, rows, scores, w.state, w.sure,
+                                                                w.cand_key, w.cand_idx);
+    else
+      topk_compact_kernel<false><<<cgrid, kPassThreads, 0, st>>>(n, k, w.cap, rows, scores, w.state, w.sure,
+                                                                 w.cand_key, w.cand_idx);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  const size_t smem = (kRegionA + 2 * kCandSmem) * sizeof(int32_t);
   static bool attr_set = false;
   if (!attr_set) {
     e = cudaFuncSetAttribute(topk_final_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));

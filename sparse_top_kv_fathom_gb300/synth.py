@@ -43,6 +43,7 @@ class Workload:
     layer_scale: tuple = None   # (lo, hi) log-uniform per-layer std multiplier
     student_t: float = 0.0      # nu > 0: Student-t keys
     per_row_budget: bool = False
+    independent_layers: bool = False  # "layers" are independent sessions (one batched step)
     description: str = ""
 
     @property
@@ -72,7 +73,7 @@ WORKLOADS = {
                     "pinned host memory"),
     "sessions": Workload(
         "sessions", 16, 8, 4, 131072, 1024, (48, 68, 92, 136, 256), 4, torch.bfloat16, torch.bfloat16,
-        outliers=3, outlier_scale=10.0, student_t=3.0, per_row_budget=True,
+        outliers=3, outlier_scale=10.0, student_t=3.0, per_row_budget=True, independent_layers=True,
         description="16 sessions x 131072 tokens, one layer (8 KV heads, 32 query heads), Student-t "
                     "(nu=3) keys with 3 channels per head at 10x scale, per-session budgets uniform "
                     "over {48,68,92,136,256}, k=1024"),

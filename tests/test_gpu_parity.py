@@ -201,14 +201,21 @@ def _score_sets(rng, rows, n):
     yield "wide", (rng.standard_normal((rows, n)) * np.exp(rng.normal(0, 20, (rows, n)))).astype(np.float32)
 
 
-@pytest.mark.parametrize("n", [1, 33, 4096, 70001])
+# n = 2^20 is the longest row whose chosen indices are ordered through the
+# shared-memory bitmap; 2^20 + 1 takes the sort; n % 4 picks the vector or the
+# scalar compaction pass.
+@pytest.mark.parametrize("n", [1, 33, 4096, 70001, 1 << 20, (1 << 20) + 1])
 def test_topk_bit_exact(gpu_lib, n):
     F = gpu_lib
     rng = np.random.default_rng(n)
-    rows = 3
+    big = n > 100000
+    rows = 2 if big else 3
     for name, s in _score_sets(rng, rows, n):
+        if big and name not in ("normal", "ties8", "allequal"):
+            continue
         sd = torch.from_numpy(s).cuda()
-        for k in sorted({1, 7, 64, max(1, n // 3), max(1, n - 1), n, n + 5, 9000}):
+        ks = {7, 2048, 9000, n - 1} if big else {1, 7, 64, max(1, n // 3), max(1, n - 1), n, n + 5, 9000}
+        for k in sorted(ks):
             idx, vals = F.topk(sd, k, with_values=True)
             want = oracle.topk_f32(s, k)
             assert np.array_equal(idx.cpu().numpy(), want), (name, n, k)
@@ -232,4 +239,98 @@ def test_sparse_attention_parity(gpu_lib, dtype, group):
     idx[1, -5:] = -1  # padding entries are skipped
     out, outb = F.sparse_attn(q.cuda(), K.cuda(), V.cuda(), torch.from_numpy(idx).cuda(), group)
     ref = oracle.sparse_attn(f32(q), f32(K), f32(V), idx, group)
+    check_attn(out.cpu().numpy(), outb, ref)
+
+
+@pytest.mark.parametrize("r", [0, 16, 32, 128])
+def test_sparq_comparator_parity(case, gpu_lib, r):
+    F, w = gpu_lib, case["w"]
+    bits, qbar = F.allocate_sparq(case["qd"], r, w.group)
+    ob, oq = oracle.allocate_sparq(f32(case["q"]), r, w.group)
+    assert np.array_equal(bits.cpu().numpy(), ob)
+    assert np.array_equal(qbar.cpu().numpy().view(np.uint32), oq.view(np.uint32))
+    s = F.scan(case["index"], bits, qbar)
+    ref, l1 = oracle.scan(case["planes"], case["meta"], ob, oq, w.n, case["S"])
+    check_scores(s.cpu().numpy(), ref, l1)
+    k = min(w.k, w.n)
+    st = F.DecodeStep(case["index"], case["Kd"], case["Vd"], case["qd"], k, w.group, 0, sparq_r=r)
+    idx, out, _ = st()
+    if r > 0:
+        assert np.array_equal(idx.cpu().numpy(), oracle.topk_f32(s.cpu().numpy(), k))
+
+
+# ------------------------------------------------------- GQA: per-head readings ---
+@pytest.mark.parametrize("budget", [0, 1, 92, 512, "rows"])
+def test_allocate_heads_bit_exact(case, gpu_lib, budget):
+    F, w = gpu_lib, case["w"]
+    if budget == "rows":
+        b = np.array([[0, 1, 68, 92, 136, 256, 511, 512][r % 8] for r in range(w.rows)], np.int32)
+        bt = torch.from_numpy(b.astype(np.int16)).cuda()
+    else:
+        b, bt = budget, budget
+    bits, qh = F.allocate_heads(case["qd"], case["index"].var, bt, w.group)
+    assert np.array_equal(bits.cpu().numpy(), oracle.allocate_heads(f32(case["q"]), case["var"], b, w.group))
+    assert np.array_equal(qh.cpu().numpy().view(np.uint32), f32(case["q"]).view(np.uint32))
+
+
+@pytest.mark.parametrize("mode", ["per_head", "max"])
+@pytest.mark.parametrize("budget", [1, 68, 136, 512])
+def test_scan_heads_within_tolerance(case, gpu_lib, mode, budget):
+    F, w = gpu_lib, case["w"]
+    bits, qh = F.allocate_heads(case["qd"], case["index"].var, budget, w.group)
+    s = F.scan_heads(case["index"], bits, qh, w.group, mode)
+    ref, l1 = oracle.scan_heads(case["planes"], case["meta"], bits.cpu().numpy(), qh.cpu().numpy(), w.n,
+                                case["S"], w.group, mode)
+    check_scores(s.cpu().numpy(), ref, l1)
+    if mode == "max":  # host-resident index: identical scores
+        assert torch.equal(s, F.scan_heads(case["index"].to_host(), bits, qh, w.group, mode))
+
+
+@pytest.mark.parametrize("mode", ["per_head", "max"])
+def test_gqa_decode_step_parity(case, gpu_lib, mode):
+    F, w = gpu_lib, case["w"]
+    B, k = w.budgets[len(w.budgets) // 2], min(w.k, w.n)
+    st = F.DecodeStep(case["index"], case["Kd"], case["Vd"], case["qd"], k, w.group, B, gqa=mode)
+    idx, out, outb = st()
+    bits, qh = F.allocate_heads(case["qd"], case["index"].var, B, w.group)
+    s = F.scan_heads(case["index"], bits, qh, w.group, mode)
+    gi = idx.cpu().numpy()
+    assert np.array_equal(gi, oracle.topk_f32(s.cpu().numpy(), k))
+    if mode == "per_head":  # head h of row r attends over its own set, with row r's K/V
+        rep = lambda t: np.repeat(f32(t), w.group, 0)
+        oatt = oracle.sparse_attn(f32(case["q"]), rep(case["K"]), rep(case["V"]), gi, 1)
+    else:
+        oatt = oracle.sparse_attn(f32(case["q"]), f32(case["K"]), f32(case["V"]), gi, w.group)
+    check_attn(out.cpu().numpy(), outb, oatt)
+
+
+@pytest.mark.parametrize("mode", ["per_head", "max"])
+def test_scan_heads_more_heads_than_one_launch(gpu_lib, mode):
+    """group 6: two launches (4 + 2 heads), the max mode folding the second into the first."""
+    F = gpu_lib
+    g, rows, n, S = 6, 2, 5000, 1024
+    rng = np.random.default_rng(6)
+    K = (rng.standard_normal((rows, n, 128)) * np.exp(rng.uniform(-2, 1.4, 128))).astype(np.float32)
+    q = rng.standard_normal((rows * g, 128)).astype(np.float32)
+    index = F.pack(torch.from_numpy(K).cuda(), S)
+    planes, meta, var = oracle.pack(K, S)
+    for B in (40, 92, 300):
+        bits, qh = F.allocate_heads(torch.from_numpy(q).cuda(), index.var, B, g)
+        assert np.array_equal(bits.cpu().numpy(), oracle.allocate_heads(q, var, B, g))
+        s = F.scan_heads(index, bits, qh, g, mode)
+        ref, l1 = oracle.scan_heads(planes, meta, bits.cpu().numpy(), q, n, S, g, mode)
+        check_scores(s.cpu().numpy(), ref, l1)
+
+
+def test_sparse_attention_per_head_sets(gpu_lib):
+    F = gpu_lib
+    rng = np.random.default_rng(12)
+    rows, g, n, k = 3, 4, 2000, 300
+    K = torch.from_numpy(rng.standard_normal((rows, n, 128)).astype(np.float32)).to(torch.bfloat16)
+    V = torch.from_numpy(rng.standard_normal((rows, n, 128)).astype(np.float32)).to(torch.bfloat16)
+    q = torch.from_numpy(rng.standard_normal((rows * g, 128)).astype(np.float32)).to(torch.bfloat16)
+    idx = np.sort(np.stack([rng.choice(n, k, replace=False) for _ in range(rows * g)]), 1).astype(np.int32)
+    idx[5, -7:] = -1
+    out, outb = F.sparse_attn(q.cuda(), K.cuda(), V.cuda(), torch.from_numpy(idx).cuda(), g, per_head=True)
+    ref = oracle.sparse_attn(f32(q), np.repeat(f32(K), g, 0), np.repeat(f32(V), g, 0), idx, 1)
     check_attn(out.cpu().numpy(), outb, ref)
