@@ -61,6 +61,8 @@ def lib():
         L.oracle_topk_f64.restype = i32
         L.oracle_sparse_attn.argtypes = [i32, i32, i64, i64, P, P, P, P, P]
         L.oracle_sparse_attn.restype = None
+        L.oracle_sparse_attn_q4.argtypes = [i32, i32, i64, i64, i64, P, P, P, P, P, P]
+        L.oracle_sparse_attn_q4.restype = None
         L.oracle_fixed136_pack.argtypes = [i64, i32, P, P, P, P, P]
         L.oracle_fixed136_pack.restype = i32
         L.oracle_fixed136_scan.argtypes = [i64, i32, P, P, P, P, P, P]
@@ -214,6 +216,20 @@ def sparse_attn(q, K, V, idx, group):
     k = idx.shape[1]
     out = np.zeros((rows * group, D), np.float64)
     lib().oracle_sparse_attn(rows, group, n, k, _p(q), _p(K), _p(V), _p(idx), _p(out))
+    return out
+
+
+def sparse_attn_q4(planes, meta, q, V, idx, group, n, S):
+    """Attention whose keys are the 4-bit dequantised keys lo + delta*code read from the
+    bit-plane index; V: [rows][n][128]; idx: [rows][k] -> [rows*group][128] fp64."""
+    planes = _c(planes, np.uint32)
+    meta = _c(meta, np.uint16)
+    q = _c(q, np.float32)
+    V = _c(V, np.float32)
+    idx = _c(idx, np.int32)
+    rows, k = idx.shape
+    out = np.zeros((rows * group, D), np.float64)
+    lib().oracle_sparse_attn_q4(rows, group, n, S, k, _p(planes), _p(meta), _p(q), _p(V), _p(idx), _p(out))
     return out
 
 

@@ -443,6 +443,59 @@ void oracle_sparse_attn(int rows, int group, int64_t n, int64_t k, const float* 
 }
 
 /* ------------------------------------------------------------------------ */
+/* Attention on the unified 4-bit store: the keys are read back from the bit- */
+/* plane index itself instead of a separate 16-bit copy.  [A] "Where this    */
+/* does not work": the index is free only in a stack whose key cache is      */
+/* already 4-bit and channel-major, where index and cache are the same bytes; */
+/* [G] "How to use it": Fathom reads the 4-bit K cache a quantized serving    */
+/* stack already holds.  reading: the key of token t is its full 4-bit        */
+/* dequantisation lo + delta*code_c(t) with its block's fp16 (lo, delta); the  */
+/* values come from V as in oracle_sparse_attn.  fp64.                        */
+/* ------------------------------------------------------------------------ */
+void oracle_sparse_attn_q4(int rows, int group, int64_t n, int64_t S, int64_t k, const uint32_t* planes,
+                           const uint16_t* meta, const float* q, const float* V, const int32_t* idx, double* out) {
+  int64_t nsb = (n + S - 1) / S;
+  int64_t nblk = (n + QBLOCK - 1) / QBLOCK;
+  double* z = (double*)malloc(sizeof(double) * (size_t)(k > 0 ? k : 1));
+  double* kt = (double*)malloc(sizeof(double) * D_CH);
+  for (int r = 0; r < rows; ++r) {
+    const int32_t* id = idx + (size_t)r * k;
+    for (int h = 0; h < group; ++h) {
+      const float* qh = q + ((size_t)r * group + h) * D_CH;
+      double zmax = -INFINITY;
+      for (int64_t i = 0; i < k; ++i) {
+        if (id[i] < 0) { z[i] = -INFINITY; continue; }
+        int64_t t = id[i], b = t / QBLOCK;
+        double dot = 0.0;
+        for (int c = 0; c < D_CH; ++c) {
+          int code = 0;
+          for (int j = 0; j < NPLANES; ++j) code = (code << 1) | plane_bit(planes, r, nsb, S, c, j, t);
+          size_t mi = (((size_t)r * D_CH + c) * nblk + b) * 2;
+          kt[c] = (double)oracle_f16_to_f32(meta[mi]) + (double)oracle_f16_to_f32(meta[mi + 1]) * (double)code;
+          dot += (double)qh[c] * kt[c];
+        }
+        z[i] = dot / sqrt((double)D_CH);
+        if (z[i] > zmax) zmax = z[i];
+      }
+      double denom = 0.0;
+      double acc[D_CH];
+      for (int c = 0; c < D_CH; ++c) acc[c] = 0.0;
+      for (int64_t i = 0; i < k; ++i) {
+        if (id[i] < 0) continue;
+        double p = exp(z[i] - zmax);
+        denom += p;
+        const float* vt = V + ((size_t)r * n + id[i]) * D_CH;
+        for (int c = 0; c < D_CH; ++c) acc[c] += p * (double)vt[c];
+      }
+      double* o = out + ((size_t)r * group + h) * D_CH;
+      for (int c = 0; c < D_CH; ++c) o[c] = denom > 0.0 ? acc[c] / denom : 0.0;
+    }
+  }
+  free(kt);
+  free(z);
+}
+
+/* ------------------------------------------------------------------------ */
 /* Fixed 136-bit comparator (Double-Sparsity style: 32 channels chosen        */
 /* offline, read at 4 bits, plus a scale), [A] "The catch": Double Sparsity    */
 /* keeps 32 channels chosen offline; these indexes land near 136 bits/token.  */

@@ -563,3 +563,47 @@ def test_scan_heads_with_identical_heads_is_the_group_scan_scaled():
     s_sum, _ = oracle.scan(planes, meta, bits, qbar, n, S)
     s_max, _ = oracle.scan_heads(planes, meta, bits_h, q, n, S, g, "max")
     np.testing.assert_allclose(s_max * g, s_sum, rtol=1e-12, atol=1e-9)
+
+
+# ------------------------------------------------- unified 4-bit store ---
+def test_unified_store_attention_is_attention_on_dequantised_keys():
+    rows, n, S, g, k = 2, 700, 256, 3, 90
+    K = rand_keys(rows, n, seed=41)
+    planes, meta, var = oracle.pack(K, S)
+    rng = np.random.default_rng(41)
+    q = rng.standard_normal((rows * g, D)).astype(np.float32)
+    V = rng.standard_normal((rows, n, D)).astype(np.float32)
+    idx = np.sort(np.stack([rng.choice(n, k, replace=False) for _ in range(rows)]), 1).astype(np.int32)
+    idx[1, :4] = -1
+    codes = codes_from_planes(planes, n, S, rows).astype(np.float64)
+    mf = meta_f32(meta).astype(np.float64)
+    blk = np.arange(n) // 128
+    Kq = mf[:, :, blk, 0].transpose(0, 2, 1) + mf[:, :, blk, 1].transpose(0, 2, 1) * codes
+    want = oracle.sparse_attn(q, Kq.astype(np.float32), V, idx, g)
+    got = oracle.sparse_attn_q4(planes, meta, q, V, idx, g, n, S)
+    np.testing.assert_allclose(got, want, rtol=1e-6, atol=1e-6)
+
+
+def test_unified_store_is_exact_for_keys_on_the_grid():
+    """Keys built as lo + delta*code (fp16 lo, power-of-two delta, codes 0 and 15 present in every
+    block) pack losslessly, so attention on the 4-bit store equals attention on the keys."""
+    rows, n, S, g, k = 2, 300, 128, 2, 64  # 300: a partial last block
+    rng = np.random.default_rng(5)
+    nblk = -(-n // 128)
+    K = np.zeros((rows, n, D), np.float32)
+    for r in range(rows):
+        for c in range(D):
+            for b in range(nblk):
+                t0, t1 = b * 128, min(n, (b + 1) * 128)
+                e = int(rng.integers(-6, 3))
+                delta = 2.0 ** e
+                lo = float(rng.integers(-64, 64)) * 2.0 ** (e - 2)
+                code = rng.integers(0, 16, t1 - t0)
+                code[0], code[-1] = 0, 15
+                K[r, t0:t1, c] = (lo + delta * code).astype(np.float32)
+    planes, meta, _ = oracle.pack(K, S)
+    q = rng.standard_normal((rows * g, D)).astype(np.float32)
+    V = rng.standard_normal((rows, n, D)).astype(np.float32)
+    idx = np.sort(np.stack([rng.choice(n, k, replace=False) for _ in range(rows)]), 1).astype(np.int32)
+    np.testing.assert_allclose(oracle.sparse_attn_q4(planes, meta, q, V, idx, g, n, S),
+                               oracle.sparse_attn(q, K, V, idx, g), rtol=1e-12, atol=1e-12)
