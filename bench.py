@@ -195,7 +195,7 @@ class Model:
         return self.F.BitPlaneIndex(store["planes"][r0:r1], store["meta"][r0:r1], self.var[r0:r1], self.w.n,
                                     r1 - r0, self.S)
 
-    def steps(self, store, q, out, idx, ws=None, sparq_r=0):
+    def steps(self, store, q, out, idx, ws=None, sparq_r=0, k_source="rows"):
         """DecodeStep objects sharing one workspace; outputs are views of out/idx.  Layers of one
         model run one after the other (a layer's query depends on the previous layer); independent
         sessions run as one batched step over all their rows."""
@@ -215,7 +215,7 @@ class Model:
             res.append(F.DecodeStep(ixs[i], store["K"][k0:k1], store["V"][k0:k1],
                                     q[r0 * G:r1 * G], w.k, G, budget, workspace=ws,
                                     idx=idx[r0:r1], out=out[r0 * G:r1 * G], out_bf16=out_b[r0 * G:r1 * G],
-                                    sparq_r=sparq_r))
+                                    sparq_r=sparq_r, k_source=k_source))
         return res
 
     def comparator_steps(self, store, q, out, idx):
@@ -545,6 +545,13 @@ def main():
                 r["sparq"]["r%d" % rr] = {"ms_per_step": max_over_ranks(stot) / args.steps,
                                           "bits_per_key_read": 4 * rr + 32 * rr / 128}
                 del sg
+            # unified 4-bit store: attention reads the winners' keys back from the bit-plane index
+            ug = capture(model.steps(store, q, cout, cidx, k_source="index"), stream)
+            utot, _, _ = time_graph(ug, args.steps, args.warmup, stream)
+            r["unified_store"] = {"ms_per_step": max_over_ranks(utot) / args.steps,
+                                  "k_bytes_per_token_per_head": 64 + 4,
+                                  "k_bytes_per_token_per_head_with_16bit_copy": 64 + 4 + 256}
+            del ug
         if res == primary:
             # e2e: q in from pinned host memory, output back to pinned host memory, every step
             qh = model.q.cpu().pin_memory()
@@ -618,9 +625,10 @@ def main():
         line["comparator"] = {"index": "fixed 136-bit (32 channels x 4 bit + 8-bit scale)",
                               "ms_per_step": p.get("comparator_ms_per_step"),
                               "fathom_speedup": p.get("comparator_ms_per_step", 0) / p["ms_per_step"],
-                              "sparq": p.get("sparq")}
+                              "sparq": p.get("sparq"), "unified_store": p.get("unified_store")}
         if "device" in result and "hbm_resident" in line:
             line["hbm_resident"]["sparq"] = result["device"].get("sparq")
+            line["hbm_resident"]["unified_store"] = result["device"].get("unified_store")
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(model, model.h if model.h else model.d, log)
     if rank == 0:

@@ -245,6 +245,26 @@ int fathom_sparse_attn_heads(int rows, int group, int64_t n, int64_t k, const vo
                              const void* V, int kv_dtype, int64_t kv_stride, const int32_t* idx, float* out,
                              uint16_t* out_bf16, void* workspace, size_t ws_bytes, void* stream);
 
+/* Attention on the unified 4-bit store ([A] "Where this does not work": the
+ * index costs nothing extra only in a stack whose K cache is already 4-bit and
+ * channel-major, where index and cache are the same bytes; [G] "How to use
+ * it").  As fathom_sparse_attn, except that the key of token t of row r is its
+ * 4-bit dequantisation lo + delta*code_c(t), read back from the index (planes,
+ * meta of `desc`, as packed by fathom_pack) -- no 16-bit K copy is read.
+ *   V        device or mapped host, rows of v_stride elements of v_dtype
+ *            (token t of row r at V + (r*n + t)*v_stride).
+ *   idx      device int32 [rows][k]; entries < 0 are skipped.
+ * The gather reads, per winner, one 32-bit word of each of the 512 (channel,
+ * plane) runs of its superblock: far more bytes than a 256-byte K row, so
+ * this trades attention speed for the memory of the K copy. */
+int fathom_sparse_attn_q4(const fathom_index_desc* desc, int group, int64_t k, const void* q, int q_dtype,
+                          const uint32_t* planes, const uint16_t* meta, const void* V, int v_dtype, int64_t v_stride,
+                          const int32_t* idx, float* out, uint16_t* out_bf16, void* stream);
+
+/* Where the decode step's attention takes its keys from. */
+#define FATHOM_KSRC_ROWS 0  /* the 16-bit (or fp32) K rows */
+#define FATHOM_KSRC_INDEX 1 /* the bit-plane index (fathom_sparse_attn_q4); K may be NULL */
+
 /* One decode step over `index.rows` rows: allocate -> scan -> top-k ->
  * sparse attention ([R] summary: the index scan ranks all n keys to choose
  * the top k; the selected rows are attended).  Same definitions as the
@@ -262,12 +282,14 @@ typedef struct fathom_step_desc {
   int32_t gqa_mode;         /* FATHOM_GQA_SUM (0), FATHOM_GQA_PER_HEAD or FATHOM_GQA_MAX; the per-head
                                modes water-fill `budget` per query head (fathom_allocate_heads) and need
                                sparq_r == 0 */
+  int32_t k_source;         /* FATHOM_KSRC_ROWS (0) or FATHOM_KSRC_INDEX */
+  int32_t reserved;         /* 0 */
   const uint32_t* planes;   /* index (device or mapped host) */
   const uint16_t* meta;     /* index (device or mapped host) */
   const float* var;         /* device [rows][128] */
   const uint16_t* budgets;  /* device [rows] or NULL */
   const void* q;            /* device [rows*group][128] */
-  const void* K;            /* device or mapped host, rows of kv_stride elements */
+  const void* K;            /* device or mapped host, rows of kv_stride elements (NULL with FATHOM_KSRC_INDEX) */
   const void* V;            /* device or mapped host, rows of kv_stride elements */
   int32_t* idx;             /* device [rows][k] out ([rows*group][k] for FATHOM_GQA_PER_HEAD) */
   float* out;               /* device [rows*group][128] out */

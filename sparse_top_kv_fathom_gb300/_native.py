@@ -21,6 +21,7 @@ class StepDesc(ctypes.Structure):
     _fields_ = [("index", IndexDesc), ("group", ctypes.c_int32), ("budget", ctypes.c_int32),
                 ("k", ctypes.c_int64), ("q_dtype", ctypes.c_int32), ("kv_dtype", ctypes.c_int32),
                 ("kv_stride", ctypes.c_int64), ("sparq_r", ctypes.c_int32), ("gqa_mode", ctypes.c_int32),
+                ("k_source", ctypes.c_int32), ("reserved", ctypes.c_int32),
                 ("planes", P), ("meta", P), ("var", P), ("budgets", P), ("q", P), ("K", P), ("V", P),
                 ("idx", P), ("out", P), ("out_bf16", P), ("status", P)]
 
@@ -35,6 +36,7 @@ class Fixed136StepDesc(ctypes.Structure):
 IDP = ctypes.POINTER(IndexDesc)
 
 GQA_SUM, GQA_PER_HEAD, GQA_MAX = 0, 1, 2  # FATHOM_GQA_*
+KSRC_ROWS, KSRC_INDEX = 0, 1  # FATHOM_KSRC_*
 
 # name -> (argtypes, restype)
 SIGNATURES = {
@@ -54,6 +56,7 @@ SIGNATURES = {
     "fathom_sparse_attn_workspace_bytes": ([I32, I32, I64, SZP], I32),
     "fathom_sparse_attn": ([I32, I32, I64, I64, P, I32, P, P, I32, I64, P, P, P, P, SZ, P], I32),
     "fathom_sparse_attn_heads": ([I32, I32, I64, I64, P, I32, P, P, I32, I64, P, P, P, P, SZ, P], I32),
+    "fathom_sparse_attn_q4": ([IDP, I32, I64, P, I32, P, P, P, I32, I64, P, P, P, P], I32),
     "fathom_decode_step_workspace_bytes": ([ctypes.POINTER(StepDesc), SZP], I32),
     "fathom_decode_step": ([ctypes.POINTER(StepDesc), P, SZ, P], I32),
     "fathom_fixed136_pack_workspace_bytes": ([I32, I64, SZP], I32),

@@ -9,8 +9,9 @@ computed here in plain torch on the original 16-bit K/V:
   for the "sum" reading, per head for "per_head", the max over the group's heads for "max")
   that the step selected;
 * error: ||o - o_dense|| / ||o_dense|| per query head (mean over heads), o_dense being full
-  softmax attention over all n keys; the same for the exact top-k's attention ("exact-k"),
-  the floor any k-key selection reaches.
+  softmax attention over all n keys; the same with attention's keys read back from the 4-bit
+  index (the unified store) instead of the 16-bit K; and for the exact top-k's attention
+  ("exact-k"), the floor any k-key selection reaches.
 
 The pages measure this on real models and tasks (needle-in-a-haystack, recall against the
 fixed-channel index); those are not available, so this is the synthetic analogue.  Run:
@@ -80,8 +81,11 @@ def curve(workload="qwen_layer", n=None, budgets=(16, 32, 48, 68, 92, 136, 256, 
         for B in budgets:
             st = F.DecodeStep(index, K, V, q, k, w.group, B, gqa=mode)
             idx, o, _ = st()
+            # the same step with the keys of attention read back from the 4-bit index
+            _, o4, _ = F.DecodeStep(index, None, V, q, k, w.group, B, gqa=mode, k_source="index")()
             out["rows"].append({"mode": mode, "budget": B, "recall": recall(idx, ref),
-                                "error": rel_error(o, o_dense), "error_exact_k": floor})
+                                "error": rel_error(o, o_dense), "error_4bit_keys": rel_error(o4, o_dense),
+                                "error_exact_k": floor})
     return out
 
 
@@ -97,10 +101,10 @@ def main():
         return
     print("workload %s: n=%d, k=%d, %d KV heads x %d query heads" % (res["workload"], res["n"], res["k"],
                                                                    res["kv_heads"], res["group"]))
-    print("%-9s %6s %8s %10s %12s" % ("reading", "B", "recall", "error", "exact-k err"))
+    print("%-9s %6s %8s %10s %14s %12s" % ("reading", "B", "recall", "error", "4-bit-K error", "exact-k err"))
     for r in res["rows"]:
-        print("%-9s %6d %8.4f %10.4f %12.4f" % (r["mode"], r["budget"], r["recall"], r["error"],
-                                              r["error_exact_k"]))
+        print("%-9s %6d %8.4f %10.4f %14.4f %12.4f" % (r["mode"], r["budget"], r["recall"], r["error"],
+                                                     r["error_4bit_keys"], r["error_exact_k"]))
 
 
 if __name__ == "__main__":

@@ -208,6 +208,25 @@ def sparse_attn(q, K, V, idx, group, stream=None, per_head=False):
     return out, outb
 
 
+def sparse_attn_q4(index, q, V, idx, group, stream=None):
+    """Attention whose keys are read back from the bit-plane index (the unified 4-bit store:
+    lo + delta*code per channel) with values from V ([rows][n][128] view, dense or interleaved)
+    -> (out fp32 [rows*group][128], out bf16)."""
+    L = lib()
+    rows, n, d = V.shape
+    if rows != index.rows or n != index.n or d != D or V.stride(2) != 1 or (rows > 1 and V.stride(0) != n * V.stride(1)):
+        raise ValueError("V must be a [rows][n][128] view matching the index, rows following each other")
+    k = idx.shape[1]
+    dev = q.device
+    out = torch.empty((rows * group, D), dtype=torch.float32, device=dev)
+    outb = torch.empty((rows * group, D), dtype=torch.bfloat16, device=dev)
+    dsc = index.desc
+    N.check(L.fathom_sparse_attn_q4(ctypes.byref(dsc), group, k, _ptr(q), _dt(q), _ptr(index.planes),
+                                    _ptr(index.meta), _ptr(V), _dt(V), V.stride(1), _ptr(idx), _ptr(out), _ptr(outb),
+                                    _stream(stream)))
+    return out, outb
+
+
 class DecodeStep:
     """A reusable decode step over one index: workspace and outputs are allocated once,
     so repeated calls launch kernels only (and can be captured in a CUDA graph).
@@ -216,7 +235,7 @@ class DecodeStep:
     K, V:  [rows][n][128] (device or pinned host), q: [rows*group][128] (device)."""
 
     def __init__(self, index, K, V, q, k, group, budget, status=None, device=None, workspace=None, idx=None,
-                 out=None, out_bf16=None, sparq_r=0, gqa="sum"):
+                 out=None, out_bf16=None, sparq_r=0, gqa="sum", k_source="rows"):
         self.L = lib()
         self.index, self.K, self.V, self.q = index, K, V, q
         dev = device if device is not None else q.device
@@ -235,10 +254,12 @@ class DecodeStep:
         self.desc.budget = 0 if self.budgets is not None else int(budget)
         self.desc.k = k
         self.desc.q_dtype = _dt(q)
-        self.desc.kv_dtype = _dt(K)
-        self.desc.kv_stride = kv_stride(K, V)
+        self.desc.kv_dtype = _dt(V)
+        self.desc.kv_stride = kv_stride(K, V) if K is not None else kv_stride(V, V)
         self.desc.sparq_r = int(sparq_r)  # 0: water-filling of `budget`; r > 0: SparQ-style comparator
         self.desc.gqa_mode = gqa_mode     # "sum": one allocation per KV head; "per_head" / "max": per query head
+        # "rows": keys from K; "index": keys read back from the bit-plane index (K may be None)
+        self.desc.k_source = {"rows": N.KSRC_ROWS, "index": N.KSRC_INDEX}[k_source]
         self._bind()
         wsb = ctypes.c_size_t()
         N.check(self.L.fathom_decode_step_workspace_bytes(ctypes.byref(self.desc), ctypes.byref(wsb)))
@@ -262,7 +283,8 @@ class DecodeStep:
         d = self.desc
         d.planes, d.meta, d.var = self.index.planes.data_ptr(), self.index.meta.data_ptr(), self.index.var.data_ptr()
         d.budgets = self.budgets.data_ptr() if self.budgets is not None else None
-        d.q, d.K, d.V = self.q.data_ptr(), self.K.data_ptr(), self.V.data_ptr()
+        d.q, d.V = self.q.data_ptr(), self.V.data_ptr()
+        d.K = self.K.data_ptr() if self.K is not None else None
         d.idx, d.out, d.out_bf16 = self.idx.data_ptr(), self.out.data_ptr(), self.out_bf16.data_ptr()
         d.status = self.status.data_ptr() if self.status is not None else None
 

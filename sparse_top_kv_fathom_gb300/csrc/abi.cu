@@ -93,7 +93,7 @@ extern "C" {
 
 const char* fathom_last_error(void) { return g_err; }
 
-int fathom_abi_version(void) { return 1; }
+int fathom_abi_version(void) { return 2; }
 
 int fathom_index_bytes(const fathom_index_desc* desc, size_t* plane_bytes, size_t* meta_bytes) {
   IndexGeom g;

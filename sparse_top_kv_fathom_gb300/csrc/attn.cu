@@ -91,6 +91,76 @@ struct Row4<__nv_bfloat16> {
   __device__ static raw zero() { return make_uint2(0u, 0u); }
 };
 
+// Where a winner's key comes from.  Keys16: the original 16-bit (or fp32) K rows.
+// KeysQ4: the unified 4-bit store -- the bit-plane index itself, each key the
+// full 4-bit dequantisation lo + delta*code of its block's fp16 (lo, delta).
+template <typename KV>
+struct Keys16 {
+  struct Args {
+    const KV* K;
+    int64_t n, stride;
+  };
+  using raw = typename Row4<KV>::raw;
+  static constexpr bool kQ4 = false;
+  __device__ static raw load(const Args& a, int64_t kvrow, int64_t t, int lane) {
+    return Row4<KV>::load(a.K + kvrow * a.n * a.stride, t, a.stride, lane);
+  }
+  __device__ static float4 cvt(const raw& x) { return Row4<KV>::cvt(x); }
+  __device__ static raw zero() { return Row4<KV>::zero(); }
+};
+
+struct KeysQ4 {
+  struct Args {
+    const uint32_t* planes;
+    const __half2* meta;
+    int64_t n, nsb, nblk;
+    int log2S;
+  };
+  // this lane's channels 4*lane .. 4*lane+3: their 4 plane words each, their blocks' (lo, delta),
+  // and the token's bit position in the words
+  struct raw {
+    uint32_t w[16];
+    __half2 m[4];
+    uint32_t bit;
+  };
+  static constexpr bool kQ4 = true;
+  __device__ static raw load(const Args& a, int64_t kvrow, int64_t t, int lane) {
+    raw x;
+    const int64_t run = (int64_t(1) << a.log2S) >> 5;
+    const uint32_t* pb = a.planes + (kvrow * a.nsb + (t >> a.log2S)) * (kD * kPlanes) * run +
+                         ((t & ((int64_t(1) << a.log2S) - 1)) >> 5);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int c = 4 * lane + i;
+#pragma unroll
+      for (int j = 0; j < kPlanes; ++j) x.w[4 * i + j] = __ldg(pb + (int64_t(c) * kPlanes + j) * run);
+      x.m[i] = a.meta[(kvrow * kD + c) * a.nblk + (t >> 7)];
+    }
+    x.bit = uint32_t(t & 31);
+    return x;
+  }
+  __device__ static float4 cvt(const raw& x) {
+    float k[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      uint32_t code = 0u;
+#pragma unroll
+      for (int j = 0; j < kPlanes; ++j) code = (code << 1) | ((x.w[4 * i + j] >> x.bit) & 1u);  // plane 0 = MSB
+      k[i] = fmaf(__high2float(x.m[i]), float(code), __low2float(x.m[i]));
+    }
+    return make_float4(k[0], k[1], k[2], k[3]);
+  }
+  __device__ static raw zero() {
+    raw x;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) x.w[i] = 0u;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) x.m[i] = __floats2half2_rn(0.0f, 0.0f);
+    x.bit = 0u;
+    return x;
+  }
+};
+
 // weight of a partial with running max mw when merged under the overall max M
 __device__ __forceinline__ float merge_weight(float mw, float M) { return mw == -INFINITY ? 0.0f : expf(mw - M); }
 
@@ -117,16 +187,20 @@ __device__ __forceinline__ void cluster_arrive_relaxed() {
 }
 __device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.aligned;" ::: "memory"); }
 
-template <int G, typename KV, int T = attn_threads<G>()>
+// threads per CTA for a key source: the 4-bit keys need the register room of 256 threads
+template <int G, typename KS>
+constexpr int attn_threads_ks() { return KS::kQ4 ? 256 : attn_threads<G>(); }
+
+template <int G, typename KV, typename KS, int T = attn_threads_ks<G, KS>()>
 __global__ void __launch_bounds__(T) attn_cluster_kernel(int64_t n, int64_t k, int64_t stride, int kv_div,
                                                          const void* __restrict__ q, int q_dtype,
-                                                         const KV* __restrict__ K, const KV* __restrict__ V,
+                                                         const typename KS::Args ka, const KV* __restrict__ V,
                                                          const int32_t* __restrict__ idx, float* __restrict__ out,
                                                          uint16_t* __restrict__ out_bf16) {
   using L = AttnSmem<G, T>;
   using R = Row4<KV>;
   constexpr int kWarps = T / 32;
-  constexpr int U = attn_batch<G>();
+  constexpr int U = KS::kQ4 ? 4 : attn_batch<G>();  // a 4-bit key holds 21 registers per lane until converted
   extern __shared__ float smem[];
   float* s_q = smem + L::q;
   cg::cluster_group cluster = cg::this_cluster();
@@ -138,8 +212,8 @@ __global__ void __launch_bounds__(T) attn_cluster_kernel(int64_t n, int64_t k, i
   const int64_t per = (k + csize - 1) / csize;
   const int64_t i0 = int64_t(crank) * per, i1 = (i0 + per < k) ? i0 + per : k;
   const int32_t* ir = idx + int64_t(r) * k;
-  const KV* Kr = K + int64_t(r / kv_div) * n * stride;  // kv_div > 1: row r is one query head of KV row r / kv_div
-  const KV* Vr = V + int64_t(r / kv_div) * n * stride;
+  const int64_t kvrow = r / kv_div;  // kv_div > 1: row r is one query head of KV row r / kv_div
+  const KV* Vr = V + kvrow * n * stride;
   constexpr int64_t kStep = int64_t(kWarps) * U;
   int64_t base = i0 + int64_t(warp) * U;
   // lane u < U holds the index of winner base + u (loaded one batch ahead)
@@ -165,7 +239,8 @@ __global__ void __launch_bounds__(T) attn_cluster_kernel(int64_t n, int64_t k, i
   for (; base < i1; base += kStep) {
     const int32_t tcur = tl;
     int32_t t[U];
-    typename R::raw kr[U], vr[U];
+    typename KS::raw kr[U];
+    typename R::raw vr[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       t[u] = __shfl_sync(0xffffffffu, tcur, u);
@@ -174,10 +249,11 @@ __global__ void __launch_bounds__(T) attn_cluster_kernel(int64_t n, int64_t k, i
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       if (t[u] >= 0) {
-        kr[u] = R::load(Kr, t[u], stride, lane);
+        kr[u] = KS::load(ka, kvrow, t[u], lane);
         vr[u] = R::load(Vr, t[u], stride, lane);
       } else {
-        kr[u] = vr[u] = R::zero();
+        kr[u] = KS::zero();
+        vr[u] = R::zero();
       }
     }
     {  // the next batch's indices travel while this batch is reduced
@@ -190,7 +266,7 @@ __global__ void __launch_bounds__(T) attn_cluster_kernel(int64_t n, int64_t k, i
     for (int i = 0; i < 32; ++i) v[i] = 0.0f;
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-      const float4 kf = R::cvt(kr[u]);
+      const float4 kf = KS::cvt(kr[u]);
 #pragma unroll
       for (int h = 0; h < G; ++h) {
         float d = qv[h].x * kf.x;
@@ -319,12 +395,13 @@ __global__ void __launch_bounds__(T) attn_cluster_kernel(int64_t n, int64_t k, i
   }
 }
 
-template <int G, typename KV>
-cudaError_t launch_attn_t(int rows, int64_t n, int64_t k, const void* q, int q_dtype, const void* K, const void* V,
-                          int64_t stride, int kv_div, const int32_t* idx, float* out, uint16_t* out_bf16,
-                          cudaStream_t st) {
-  auto kern = attn_cluster_kernel<G, KV>;
-  constexpr size_t smem = AttnSmem<G, attn_threads<G>()>::bytes;
+template <int G, typename KV, typename KS>
+cudaError_t launch_attn_t(int rows, int64_t n, int64_t k, const void* q, int q_dtype, const typename KS::Args& ka,
+                          const void* V, int64_t stride, int kv_div, const int32_t* idx, float* out,
+                          uint16_t* out_bf16, cudaStream_t st) {
+  auto kern = attn_cluster_kernel<G, KV, KS>;
+  constexpr int T = attn_threads_ks<G, KS>();
+  constexpr size_t smem = AttnSmem<G, T>::bytes;
   // 16-CTA clusters need an opt-in per kernel; fall back to the portable 8 if it is refused
   static int cluster = 0;
   if (cluster == 0) {
@@ -338,7 +415,7 @@ cudaError_t launch_attn_t(int rows, int64_t n, int64_t k, const void* q, int q_d
   for (;;) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(unsigned(cluster), unsigned(rows), 1);
-    cfg.blockDim = dim3(attn_threads<G>(), 1, 1);
+    cfg.blockDim = dim3(T, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
@@ -348,7 +425,7 @@ cudaError_t launch_attn_t(int rows, int64_t n, int64_t k, const void* q, int q_d
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, n, k, stride, kv_div, q, q_dtype, reinterpret_cast<const KV*>(K),
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, n, k, stride, kv_div, q, q_dtype, ka,
                                              reinterpret_cast<const KV*>(V), idx, out, out_bf16);
     if (e == cudaSuccess || cluster == 8) return e;
     cudaGetLastError();  // the larger cluster could not be scheduled: use the portable size from now on
@@ -356,15 +433,59 @@ cudaError_t launch_attn_t(int rows, int64_t n, int64_t k, const void* q, int q_d
   }
 }
 
-template <int G>
-cudaError_t launch_attn_g(int rows, int64_t n, int64_t k, const void* q, int q_dtype, const void* K, const void* V,
-                          int kv_dtype, int64_t stride, const int32_t* idx, float* out, uint16_t* out_bf16,
-                          cudaStream_t st, int kv_div = 1) {
+// KS: the key source; K16 is the K pointer of the 16-bit (or fp32) path, unused for the 4-bit store
+template <int G, template <typename> class KSel>
+cudaError_t launch_attn_g(int rows, int64_t n, int64_t k, const void* q, int q_dtype, const void* K,
+                          const KeysQ4::Args* q4, const void* V, int kv_dtype, int64_t stride, const int32_t* idx,
+                          float* out, uint16_t* out_bf16, cudaStream_t st, int kv_div) {
   if (kv_dtype == FATHOM_F32)
-    return launch_attn_t<G, float>(rows, n, k, q, q_dtype, K, V, stride, kv_div, idx, out, out_bf16, st);
+    return launch_attn_t<G, float, typename KSel<float>::type>(rows, n, k, q, q_dtype,
+                                                                KSel<float>::args(K, q4, n, stride), V, stride,
+                                                                kv_div, idx, out, out_bf16, st);
   if (kv_dtype == FATHOM_F16)
-    return launch_attn_t<G, __half>(rows, n, k, q, q_dtype, K, V, stride, kv_div, idx, out, out_bf16, st);
-  return launch_attn_t<G, __nv_bfloat16>(rows, n, k, q, q_dtype, K, V, stride, kv_div, idx, out, out_bf16, st);
+    return launch_attn_t<G, __half, typename KSel<__half>::type>(rows, n, k, q, q_dtype,
+                                                                  KSel<__half>::args(K, q4, n, stride), V, stride,
+                                                                  kv_div, idx, out, out_bf16, st);
+  return launch_attn_t<G, __nv_bfloat16, typename KSel<__nv_bfloat16>::type>(
+      rows, n, k, q, q_dtype, KSel<__nv_bfloat16>::args(K, q4, n, stride), V, stride, kv_div, idx, out, out_bf16,
+      st);
+}
+
+template <typename KV>
+struct Sel16 {
+  using type = Keys16<KV>;
+  static typename Keys16<KV>::Args args(const void* K, const KeysQ4::Args*, int64_t n, int64_t stride) {
+    return {reinterpret_cast<const KV*>(K), n, stride};
+  }
+};
+template <typename KV>
+struct SelQ4 {
+  using type = KeysQ4;
+  static KeysQ4::Args args(const void*, const KeysQ4::Args* q4, int64_t, int64_t) { return *q4; }
+};
+
+template <template <typename> class KSel>
+cudaError_t launch_attn_any(int rows, int group, int64_t n, int64_t k, const void* q, int q_dtype, const void* K,
+                            const KeysQ4::Args* q4, const void* V, int kv_dtype, int64_t kv_stride,
+                            const int32_t* idx, float* out, uint16_t* out_bf16, cudaStream_t st, bool per_head) {
+  if (per_head)  // every query head is a row of its own over its KV row's K/V
+    return launch_attn_g<1, KSel>(rows * group, n, k, q, q_dtype, K, q4, V, kv_dtype, kv_stride, idx, out, out_bf16,
+                                  st, group);
+#define FATHOM_ATTN_G(GG)                                                                                          \
+  case GG:                                                                                                         \
+    return launch_attn_g<GG, KSel>(rows, n, k, q, q_dtype, K, q4, V, kv_dtype, kv_stride, idx, out, out_bf16, st, 1);
+  switch (group) {
+    FATHOM_ATTN_G(1)
+    FATHOM_ATTN_G(2)
+    FATHOM_ATTN_G(3)
+    FATHOM_ATTN_G(4)
+    FATHOM_ATTN_G(5)
+    FATHOM_ATTN_G(6)
+    FATHOM_ATTN_G(7)
+    FATHOM_ATTN_G(8)
+    default: return cudaErrorInvalidValue;
+  }
+#undef FATHOM_ATTN_G
 }
 
 }  // namespace
@@ -374,20 +495,16 @@ size_t attn_ws_bytes(int, int, int64_t) { return 256; }
 cudaError_t launch_attn(int rows, int group, int64_t n, int64_t k, const void* q, int q_dtype, const void* K,
                         const void* V, int kv_dtype, int64_t kv_stride, const int32_t* idx, float* out,
                         uint16_t* out_bf16, void* /*ws*/, cudaStream_t st, bool per_head) {
-  if (per_head)  // every query head is a row of its own over its KV row's K/V
-    return launch_attn_g<1>(rows * group, n, k, q, q_dtype, K, V, kv_dtype, kv_stride, idx, out, out_bf16, st,
-                            group);
-  switch (group) {
-    case 1: return launch_attn_g<1>(rows, n, k, q, q_dtype, K, V, kv_dtype, kv_stride, idx, out, out_bf16, st);
-    case 2: return launch_attn_g<2>(rows, n, k, q, q_dtype, K, V, kv_dtype, kv_stride, idx, out, out_bf16, st);
-    case 3: return launch_attn_g<3>(rows, n, k, q, q_dtype, K, V, kv_dtype, kv_stride, idx, out, out_bf16, st);
-    case 4: return launch_attn_g<4>(rows, n, k, q, q_dtype, K, V, kv_dtype, kv_stride, idx, out, out_bf16, st);
-    case 5: return launch_attn_g<5>(rows, n, k, q, q_dtype, K, V, kv_dtype, kv_stride, idx, out, out_bf16, st);
-    case 6: return launch_attn_g<6>(rows, n, k, q, q_dtype, K, V, kv_dtype, kv_stride, idx, out, out_bf16, st);
-    case 7: return launch_attn_g<7>(rows, n, k, q, q_dtype, K, V, kv_dtype, kv_stride, idx, out, out_bf16, st);
-    case 8: return launch_attn_g<8>(rows, n, k, q, q_dtype, K, V, kv_dtype, kv_stride, idx, out, out_bf16, st);
-    default: return cudaErrorInvalidValue;
-  }
+  return launch_attn_any<Sel16>(rows, group, n, k, q, q_dtype, K, nullptr, V, kv_dtype, kv_stride, idx, out,
+                                out_bf16, st, per_head);
+}
+
+cudaError_t launch_attn_q4(const IndexGeom& g, int group, int64_t k, const void* q, int q_dtype,
+                           const uint32_t* planes, const __half2* meta, const void* V, int v_dtype, int64_t v_stride,
+                           const int32_t* idx, float* out, uint16_t* out_bf16, cudaStream_t st, bool per_head) {
+  const KeysQ4::Args a{planes, meta, g.n, g.nsb, g.nblk, g.log2S};
+  return launch_attn_any<SelQ4>(g.rows, group, g.n, k, q, q_dtype, nullptr, &a, V, v_dtype, v_stride, idx, out,
+                                out_bf16, st, per_head);
 }
 
 }  // namespace fathom
@@ -436,6 +553,34 @@ int fathom_sparse_attn(int rows, int group, int64_t n, int64_t k, const void* q,
                        uint16_t* out_bf16, void* workspace, size_t ws_bytes, void* stream) {
   return sparse_attn_impl(rows, group, n, k, q, q_dtype, K, V, kv_dtype, kv_stride, idx, out, out_bf16, workspace,
                           ws_bytes, stream, false);
+}
+
+int fathom_sparse_attn_q4(const fathom_index_desc* desc, int group, int64_t k, const void* q, int q_dtype,
+                          const uint32_t* planes, const uint16_t* meta, const void* V, int v_dtype, int64_t v_stride,
+                          const int32_t* idx, float* out, uint16_t* out_bf16, void* stream) {
+  clear_error();
+  IndexGeom g;
+  FATHOM_TRY(index_geom(desc, &g));
+  if (g.rows > 65535 || group < 1 || group > 8 || k < 1 || k > 0x7fffffff)
+    return set_error(FATHOM_EINVAL, "rows (<= 65535), group (1..8) or k out of range");
+  if (v_stride < kD || (v_stride & 3)) return set_error(FATHOM_EINVAL, "v_stride must be >= 128, a multiple of 4");
+  if (!valid_dtype(q_dtype) || !valid_dtype(v_dtype)) return set_error(FATHOM_EINVAL, "invalid dtype");
+  const void *dq, *dP, *dM, *dV, *dI, *dO, *dB;
+  FATHOM_TRY(device_view(q, "q", &dq));
+  FATHOM_TRY(device_view(planes, "planes", &dP));
+  FATHOM_TRY(device_view(meta, "meta", &dM));
+  FATHOM_TRY(device_view(V, "V", &dV));
+  FATHOM_TRY(device_view(idx, "idx", &dI));
+  FATHOM_TRY(device_view(out, "out", &dO, true));
+  FATHOM_TRY(device_view(out_bf16, "out_bf16", &dB, true));
+  if (!dO && !dB) return set_error(FATHOM_EINVAL, "out and out_bf16 are both NULL");
+  const size_t al = v_dtype == FATHOM_F32 ? 16 : 8;
+  if ((reinterpret_cast<uintptr_t>(dV) % al) || (reinterpret_cast<uintptr_t>(dP) & 3) ||
+      (reinterpret_cast<uintptr_t>(dM) & 3))
+    return set_error(FATHOM_EINVAL, "misaligned planes, meta or V");
+  FATHOM_TRY_CUDA(launch_attn_q4(g, group, k, dq, q_dtype, (const uint32_t*)dP, (const __half2*)dM, dV, v_dtype,
+                                 v_stride, (const int32_t*)dI, (float*)dO, (uint16_t*)dB, as_stream(stream)));
+  return FATHOM_OK;
 }
 
 int fathom_sparse_attn_heads(int rows, int group, int64_t n, int64_t k, const void* q, int q_dtype, const void* K,

@@ -112,6 +112,10 @@ cudaError_t launch_topk(int rows, int64_t n, int64_t k, const float* scores, int
 cudaError_t launch_attn(int rows, int group, int64_t n, int64_t k, const void* q, int q_dtype, const void* K,
                         const void* V, int kv_dtype, int64_t kv_stride, const int32_t* idx, float* out, uint16_t* out_bf16, void* ws,
                         cudaStream_t st, bool per_head = false);
+// attention whose keys are read back from the bit-plane index (the unified 4-bit store)
+cudaError_t launch_attn_q4(const IndexGeom& g, int group, int64_t k, const void* q, int q_dtype,
+                           const uint32_t* planes, const __half2* meta, const void* V, int v_dtype, int64_t v_stride,
+                           const int32_t* idx, float* out, uint16_t* out_bf16, cudaStream_t st, bool per_head = false);
 cudaError_t launch_fixed136_scan(int rows, int64_t n, const int32_t* chans, const uint8_t* codes, const uint8_t* exps,
                                  const float* qbar, float* scores, uint32_t* hist, cudaStream_t st);
 

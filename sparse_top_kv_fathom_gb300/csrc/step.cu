@@ -70,6 +70,9 @@ int fathom_decode_step(const fathom_step_desc* s, void* workspace, size_t ws_byt
   if (s->gqa_mode != FATHOM_GQA_SUM && s->sparq_r != 0)
     return set_error(FATHOM_EINVAL, "the per-head GQA modes take the water-filling allocation (sparq_r must be 0)");
   const int gqa = s->gqa_mode;
+  if (s->k_source != FATHOM_KSRC_ROWS && s->k_source != FATHOM_KSRC_INDEX)
+    return set_error(FATHOM_EINVAL, "k_source %d invalid", s->k_source);
+  const bool q4 = s->k_source == FATHOM_KSRC_INDEX;
   if (gqa == FATHOM_GQA_PER_HEAD && int64_t(g.rows) * s->group > 65535)
     return set_error(FATHOM_EINVAL, "rows*group > 65535");
   if (s->sparq_r == 0 && !s->budgets && (s->budget < 0 || s->budget > kD * kPlanes))
@@ -80,7 +83,7 @@ int fathom_decode_step(const fathom_step_desc* s, void* workspace, size_t ws_byt
   FATHOM_TRY(device_view(s->var, "var", &dVar));
   FATHOM_TRY(device_view(s->budgets, "budgets", &dBud, true));
   FATHOM_TRY(device_view(s->q, "q", &dq));
-  FATHOM_TRY(device_view(s->K, "K", &dK));
+  FATHOM_TRY(device_view(s->K, "K", &dK, q4));
   FATHOM_TRY(device_view(s->V, "V", &dV));
   FATHOM_TRY(device_view(s->idx, "idx", &dI));
   FATHOM_TRY(device_view(s->out, "out", &dO, true));
@@ -108,9 +111,14 @@ int fathom_decode_step(const fathom_step_desc* s, void* workspace, size_t ws_byt
     FATHOM_TRY_CUDA(launch_scan_heads(g, s->group, gqa, (const uint32_t*)dP, (const __half2*)dM, w.bits, w.qbar,
                                       w.scores, hist, st));
     FATHOM_TRY_CUDA(launch_topk(srows, g.n, s->k, w.scores, (int32_t*)dI, nullptr, w.topk, use_hist, st));
-    FATHOM_TRY_CUDA(launch_attn(g.rows, s->group, g.n, s->k, dq, s->q_dtype, dK, dV, s->kv_dtype, s->kv_stride,
-                                (const int32_t*)dI, (float*)dO, (uint16_t*)dB, w.attn, st,
-                                gqa == FATHOM_GQA_PER_HEAD));
+    if (q4)
+      FATHOM_TRY_CUDA(launch_attn_q4(g, s->group, s->k, dq, s->q_dtype, (const uint32_t*)dP, (const __half2*)dM, dV,
+                                     s->kv_dtype, s->kv_stride, (const int32_t*)dI, (float*)dO, (uint16_t*)dB, st,
+                                     gqa == FATHOM_GQA_PER_HEAD));
+    else
+      FATHOM_TRY_CUDA(launch_attn(g.rows, s->group, g.n, s->k, dq, s->q_dtype, dK, dV, s->kv_dtype, s->kv_stride,
+                                  (const int32_t*)dI, (float*)dO, (uint16_t*)dB, w.attn, st,
+                                  gqa == FATHOM_GQA_PER_HEAD));
     return FATHOM_OK;
   }
   const bool use_hist = s->k < g.n;
@@ -124,8 +132,12 @@ int fathom_decode_step(const fathom_step_desc* s, void* workspace, size_t ws_byt
                                     s->budget, w.bits, w.qbar, (int32_t*)dSt, st));
   FATHOM_TRY_CUDA(launch_scan(g, (const uint32_t*)dP, (const __half2*)dM, w.bits, w.qbar, w.scores, hist, st));
   FATHOM_TRY_CUDA(launch_topk(g.rows, g.n, s->k, w.scores, (int32_t*)dI, nullptr, w.topk, use_hist, st));
-  FATHOM_TRY_CUDA(launch_attn(g.rows, s->group, g.n, s->k, dq, s->q_dtype, dK, dV, s->kv_dtype, s->kv_stride, (const int32_t*)dI,
-                              (float*)dO, (uint16_t*)dB, w.attn, st));
+  if (q4)
+    FATHOM_TRY_CUDA(launch_attn_q4(g, s->group, s->k, dq, s->q_dtype, (const uint32_t*)dP, (const __half2*)dM, dV,
+                                   s->kv_dtype, s->kv_stride, (const int32_t*)dI, (float*)dO, (uint16_t*)dB, st));
+  else
+    FATHOM_TRY_CUDA(launch_attn(g.rows, s->group, g.n, s->k, dq, s->q_dtype, dK, dV, s->kv_dtype, s->kv_stride,
+                                (const int32_t*)dI, (float*)dO, (uint16_t*)dB, w.attn, st));
   return FATHOM_OK;
 }
 

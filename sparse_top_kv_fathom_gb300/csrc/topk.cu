@@ -183,11 +183,11 @@ __global__ void __launch_bounds__(kFinThreads) topk_bin_kernel(int64_t k, const 
   }
 }
 
-// Persistent pass over all (row, tile) pairs: keys in bins above b1 go to the
-// row's sure list, keys in b1 to its candidate list.  Per tile, every thread
-// marks its hits in two bit masks, one block scan of the packed counts gives
-// each thread its slots, and one thread reserves the tile's slots in each list
-// with a single atomic; the next tile's scores are in flight meanwhile.
+// Candidate pass over all (row, tile) pairs, each CTA a contiguous range of
+// them: keys in bins above b1 go to the row's sure list, keys in b1 to its
+// candidate list.  Per tile every thread counts its hits, one block scan of the
+// packed counts gives each thread its slots, and the next tile's scores are in
+// flight meanwhile.
 template <bool kVec>
 struct CompactTile {
   static constexpr int kItems = kPassItems;
@@ -224,6 +224,26 @@ __device__ __forceinline__ uint32_t score_key_fast(float v) {
   return k + uint32_t(u == 0x80000000u);
 }
 
+// Hits of a CTA are staged in shared memory across its tiles and written out
+// (one slot reservation per list) when the row changes, the stage would
+// overflow, or the CTA is done; a tile with more hits than the stage holds is
+// written straight to the global lists.  The same-address atomics on the
+// row counters are thus about one per CTA instead of two per tile.
+constexpr int kStage = 1024;
+
+__device__ __forceinline__ void stage_flush(int64_t row, int ns, int nc, int64_t bs, int64_t bc, int64_t k,
+                                            int64_t cap, const int32_t* st_si, const uint32_t* st_ck,
+                                            const int32_t* st_ci, int32_t* sure, uint32_t* cand_key,
+                                            int32_t* cand_idx) {
+  for (int i = threadIdx.x; i < ns; i += kPassThreads)
+    if (bs + i < k) sure[row * k + bs + i] = st_si[i];
+  for (int i = threadIdx.x; i < nc; i += kPassThreads)
+    if (bc + i < cap) {
+      cand_key[row * cap + bc + i] = st_ck[i];
+      cand_idx[row * cap + bc + i] = st_ci[i];
+    }
+}
+
 template <bool kVec>
 __global__ void __launch_bounds__(kPassThreads, kCompactCtasPerSm) topk_compact_kernel(int64_t n, int64_t k, int64_t cap, int rows,
                                                                     const float* __restrict__ scores,
@@ -234,21 +254,37 @@ __global__ void __launch_bounds__(kPassThreads, kCompactCtasPerSm) topk_compact_
   using C = CompactTile<kVec>;
   static_assert(C::kItems <= 16 && C::kTile < 65536, "packed 16-bit counts");
   constexpr int kWarps = kPassThreads / 32;
-  __shared__ uint32_t s_warp[2][kWarps];  // inclusive scan of the warps' packed counts, per tile parity
-  __shared__ int32_t s_base[2][2];        // the tile's first slot in the sure and candidate lists
+  __shared__ uint32_t s_warp[kWarps];  // inclusive scan of the warps' packed counts
+  __shared__ int32_t st_si[kStage];    // staged sure winners
+  __shared__ uint32_t st_ck[kStage];   // staged candidates (key, index)
+  __shared__ int32_t st_ci[kStage];
+  // Per tile, written by the control thread (warp 0, lane kWarps-1) between the tile's first two
+  // barriers and read by all after them: [0], [1] stage offsets of this tile's sure / candidate
+  // hits, [2] flush the stage first?, [3] this tile direct to global?, [4], [5] slot bases of the
+  // flushed hits, [6], [7] slot bases of a direct tile, [8] row, [9], [10] counts of the flushed
+  // stage.  The stage's own state (row, counts) is touched by the control thread only until the
+  // last tile is done.
+  __shared__ int64_t s_ctl[11];
+  __shared__ int64_t s_row;
+  __shared__ int s_ns, s_nc;
   const int64_t tiles_row = (n + C::kTile - 1) / C::kTile;
   const int64_t total = tiles_row * rows;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  int64_t g = blockIdx.x;
-  if (g >= total) return;
+  // a contiguous range of (row, tile) pairs per CTA: a CTA's tiles mostly share one row
+  const int64_t per = (total + gridDim.x - 1) / gridDim.x;
+  const int64_t g0 = int64_t(blockIdx.x) * per, g1 = g0 + per < total ? g0 + per : total;
+  if (g0 >= g1) return;
+  if (threadIdx.x == 0) {
+    s_row = g0 / tiles_row;
+    s_ns = s_nc = 0;
+  }
   float cur[C::kItems];
-  C::load(scores + (g / tiles_row) * n, n, (g % tiles_row) * C::kTile, cur);
-  for (int par = 0; g < total; g += gridDim.x, par ^= 1) {
+  C::load(scores + (g0 / tiles_row) * n, n, (g0 % tiles_row) * C::kTile, cur);
+  for (int64_t g = g0; g < g1; ++g) {
     const int64_t r = g / tiles_row;
     const int64_t t0 = (g % tiles_row) * C::kTile;
     float nxt[C::kItems];
-    const int64_t gn = g + gridDim.x;
-    if (gn < total) C::load(scores + (gn / tiles_row) * n, n, (gn % tiles_row) * C::kTile, nxt);
+    if (g + 1 < g1) C::load(scores + ((g + 1) / tiles_row) * n, n, ((g + 1) % tiles_row) * C::kTile, nxt);
     // keys in (khi, ~0] are sure, keys in [klo, khi] candidates
     const uint32_t b1 = __ldg(&state[r].b1);
     const uint32_t klo = b1 << (32 - kHistBits), khi = klo | ((1u << (32 - kHistBits)) - 1u);
@@ -277,27 +313,53 @@ __global__ void __launch_bounds__(kPassThreads, kCompactCtasPerSm) topk_compact_
       const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
       if (lane >= o) x += y;
     }
-    if (lane == 31) s_warp[par][warp] = x;
+    if (lane == 31) s_warp[warp] = x;
     __syncthreads();
     if (warp == 0) {
-      uint32_t v = lane < kWarps ? s_warp[par][lane] : 0u;
+      uint32_t v = lane < kWarps ? s_warp[lane] : 0u;
 #pragma unroll
       for (int o = 1; o < kWarps; o <<= 1) {
         const uint32_t y = __shfl_up_sync(0xffffffffu, v, o);
         if (lane >= o) v += y;
       }
-      if (lane < kWarps) s_warp[par][lane] = v;
-      if (lane == kWarps - 1) {
+      if (lane < kWarps) s_warp[lane] = v;
+      if (lane == kWarps - 1) {  // the control thread
         const int ts = int(v & 0xFFFFu), tc = int(v >> 16);
-        s_base[par][0] = ts ? atomicAdd(&state[r].sure_cnt, ts) : 0;
-        s_base[par][1] = tc ? atomicAdd(&state[r].cand_cnt, tc) : 0;
+        const bool direct = ts > kStage || tc > kStage;
+        const bool flush = s_ns + s_nc > 0 && (s_row != r || direct || s_ns + ts > kStage || s_nc + tc > kStage);
+        s_ctl[2] = flush;
+        s_ctl[3] = direct;
+        if (flush) {  // reserve the staged hits' slots in their row's lists
+          s_ctl[4] = s_ns ? atomicAdd(&state[s_row].sure_cnt, s_ns) : 0;
+          s_ctl[5] = s_nc ? atomicAdd(&state[s_row].cand_cnt, s_nc) : 0;
+          s_ctl[8] = s_row;
+          s_ctl[9] = s_ns;
+          s_ctl[10] = s_nc;
+          s_ns = s_nc = 0;
+        }
+        if (direct) {  // this tile's own hits go straight to the global lists
+          s_ctl[6] = ts ? atomicAdd(&state[r].sure_cnt, ts) : 0;
+          s_ctl[7] = tc ? atomicAdd(&state[r].cand_cnt, tc) : 0;
+        } else {
+          s_ctl[0] = s_ns;
+          s_ctl[1] = s_nc;
+          s_ns += ts;
+          s_nc += tc;
+          s_row = r;
+        }
       }
     }
     __syncthreads();
-    if (mine) {  // rare: this thread holds hits; find them again and write them
-      const uint32_t excl = x - mine + (warp ? s_warp[par][warp - 1] : 0u);
-      int64_t ps = int64_t(s_base[par][0]) + (excl & 0xFFFFu);
-      int64_t pc = int64_t(s_base[par][1]) + (excl >> 16);
+    if (s_ctl[2]) {  // rare: write out the stage before this tile's hits land in it
+      stage_flush(s_ctl[8], int(s_ctl[9]), int(s_ctl[10]), s_ctl[4], s_ctl[5], k, cap, st_si, st_ck, st_ci, sure,
+                  cand_key, cand_idx);
+      __syncthreads();
+    }
+    const bool direct = s_ctl[3] != 0;
+    if (mine) {  // this thread holds hits: find them again and place them
+      const uint32_t excl = x - mine + (warp ? s_warp[warp - 1] : 0u);
+      int64_t ps = int64_t(excl & 0xFFFFu) + (direct ? s_ctl[6] : s_ctl[0]);
+      int64_t pc = int64_t(excl >> 16) + (direct ? s_ctl[7] : s_ctl[1]);
 #pragma unroll
       for (int i = 0; i < C::kItems; ++i) {
         const uint32_t key = score_key_fast(cur[i]);
@@ -305,10 +367,14 @@ __global__ void __launch_bounds__(kPassThreads, kCompactCtasPerSm) topk_compact_
         if (p >= lim) continue;
         const int32_t t = int32_t(t0 + p);
         if (key > khi) {
-          if (ps < k) sure[r * k + ps] = t;
+          if (!direct) st_si[ps] = t;
+          else if (ps < k) sure[r * k + ps] = t;
           ++ps;
         } else if (key >= klo) {
-          if (pc < cap) {
+          if (!direct) {
+            st_ck[pc] = key;
+            st_ci[pc] = t;
+          } else if (pc < cap) {
             cand_key[r * cap + pc] = key;
             cand_idx[r * cap + pc] = t;
           }
@@ -316,10 +382,20 @@ __global__ void __launch_bounds__(kPassThreads, kCompactCtasPerSm) topk_compact_
         }
       }
     }
-    if (gn < total) {
+    __syncthreads();  // stage writes and s_warp / s_ctl reads done before the next tile
+    if (g + 1 < g1) {
 #pragma unroll
       for (int i = 0; i < C::kItems; ++i) cur[i] = nxt[i];
     }
+  }
+  // the control thread's last update of the stage state is visible after the loop's last barrier
+  if (s_ns + s_nc > 0) {
+    if (threadIdx.x == 0) {
+      s_ctl[4] = s_ns ? atomicAdd(&state[s_row].sure_cnt, s_ns) : 0;
+      s_ctl[5] = s_nc ? atomicAdd(&state[s_row].cand_cnt, s_nc) : 0;
+    }
+    __syncthreads();
+    stage_flush(s_row, s_ns, s_nc, s_ctl[4], s_ctl[5], k, cap, st_si, st_ck, st_ci, sure, cand_key, cand_idx);
   }
 }
 

@@ -334,3 +334,41 @@ def test_sparse_attention_per_head_sets(gpu_lib):
     out, outb = F.sparse_attn(q.cuda(), K.cuda(), V.cuda(), torch.from_numpy(idx).cuda(), g, per_head=True)
     ref = oracle.sparse_attn(f32(q), np.repeat(f32(K), g, 0), np.repeat(f32(V), g, 0), idx, 1)
     check_attn(out.cpu().numpy(), outb, ref)
+
+
+# ------------------------------------------------------- unified 4-bit store ---
+def test_sparse_attention_on_the_index_parity(case, gpu_lib):
+    """Keys read back from the bit-plane index (lo + delta*code), values from V."""
+    F, w = gpu_lib, case["w"]
+    rng = np.random.default_rng(w.n)
+    k = min(300, w.n)
+    idx = np.sort(np.stack([rng.choice(w.n, k, replace=False) for _ in range(w.rows)]), 1).astype(np.int32)
+    idx[0, -3:] = -1
+    idt = torch.from_numpy(idx).cuda()
+    out, outb = F.sparse_attn_q4(case["index"], case["qd"], case["Vd"], idt, w.group)
+    ref = oracle.sparse_attn_q4(case["planes"], case["meta"], f32(case["q"]), f32(case["V"]), idx, w.group, w.n,
+                                case["S"])
+    check_attn(out.cpu().numpy(), outb, ref)
+    # index and V in pinned host memory: the same result
+    o2, _ = F.sparse_attn_q4(case["index"].to_host(), case["qd"], case["Vd"].cpu().pin_memory(), idt, w.group)
+    assert torch.equal(out, o2)
+
+
+@pytest.mark.parametrize("gqa", ["sum", "per_head"])
+def test_decode_step_with_keys_from_the_index(case, gpu_lib, gqa):
+    F, w = gpu_lib, case["w"]
+    B, k = w.budgets[len(w.budgets) // 2], min(w.k, w.n)
+    a = F.DecodeStep(case["index"], case["Kd"], case["Vd"], case["qd"], k, w.group, B, gqa=gqa)()
+    st = F.DecodeStep(case["index"], None, case["Vd"], case["qd"], k, w.group, B, gqa=gqa, k_source="index")
+    idx, out, outb = st()
+    assert torch.equal(idx, a[0])  # the selection does not depend on where attention reads keys
+    gi = idx.cpu().numpy()
+    if gqa == "per_head":
+        rep = lambda t: np.repeat(t, w.group, 0)
+        ref = oracle.sparse_attn_q4(rep(case["planes"].reshape(w.rows, -1)).reshape(-1),
+                                    rep(case["meta"].reshape(w.rows, -1)).reshape(-1), f32(case["q"]),
+                                    rep(f32(case["V"])), gi, 1, w.n, case["S"])
+    else:
+        ref = oracle.sparse_attn_q4(case["planes"], case["meta"], f32(case["q"]), f32(case["V"]), gi, w.group, w.n,
+                                    case["S"])
+    check_attn(out.cpu().numpy(), outb, ref)
