@@ -385,6 +385,25 @@ def captured_issue_rate(residency, w, budget, ms_per_launch):
     return out
 
 
+def machine_balance(int_ops, hbm_gbs, link_gbs, w, budget):
+    """Integer ALU operations per byte of bandwidth (the pages' argument that a scan is
+    arithmetic-bound wherever ops per byte fall short of what it needs), beside what the scan
+    needs: its ALU-pipe operations (committed ncu record, 32 lanes per warp instruction) per
+    algorithmic byte of index read."""
+    out = {"int_alu_ops_per_s": int_ops, "ops_per_hbm_byte": int_ops / (hbm_gbs * 1e9),
+           "ops_per_link_byte": int_ops / (link_gbs * 1e9),
+           "probe": "fathom_probe_int_ops: 8 chains per thread of two right shifts and a 3-input XOR"}
+    try:
+        rec = json.load(open(TRAFFIC_RECORD))
+        r = rec.get("device", {})
+        if rec.get("scan_source_sha256") == scan_source_hash() and r.get("n") == w.n and r.get("budget") == budget \
+                and "alu_warp_instructions" in r:
+            out["scan_alu_ops_per_index_byte"] = 32.0 * r["alu_warp_instructions"] / r["algorithmic_bytes"]
+    except (OSError, ValueError):
+        pass
+    return out
+
+
 def link_peak(log):
     """Host-link streaming-read peak: zero-copy 16 B loads over pinned host memory, best of several shapes."""
     import sparse_top_kv_fathom_gb300 as F
@@ -507,6 +526,9 @@ def main():
         os.path.join(ROOT, "MEASURED_PEAKS.json")) else {}
     hbm_peak = peak.get("hbm_gbs", 6800.0)
     link_gbs, h2d_gbs = link_peak(log)
+    import sparse_top_kv_fathom_gb300 as FF
+    int_ops = FF.probe_int_ops()
+    log("integer ALU rate: %.2f T ops/s" % (int_ops / 1e12))
     model = Model(w, args.budget, args.superblock, args.residency, comparator, log, args.kv_layers)
     stream = torch.cuda.Stream()
     keys_per_step = w.rows * w.n
@@ -603,6 +625,7 @@ def main():
                      "peak_source": ("zero-copy streaming read of pinned host memory measured in this run"
                                      if primary == "host" else "MEASURED_PEAKS.json hbm_gbs")},
         "link": {"zero_copy_read_gbs": link_gbs, "copy_engine_h2d_gbs": h2d_gbs},
+        "machine_balance": machine_balance(int_ops, hbm_peak, link_gbs, w, args.budget),
         "e2e": p.get("e2e"),
         "clocks": p.get("clocks"),
         "gpu_launches": args.steps * w.layers * 7,

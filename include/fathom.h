@@ -80,6 +80,11 @@ typedef struct fathom_index_desc {
   int32_t d;          /* channels per row, must be 128 */
   int32_t block;      /* quantisation block in tokens, must be 128 */
   int32_t superblock; /* S, tokens per superblock: a power of two in [128, 65536] */
+  int64_t capacity;   /* tokens of storage per row, >= n (0: n).  The layout's per-row strides
+                         (superblocks ceil(capacity/S), blocks ceil(capacity/128)) follow it, so
+                         an index can grow by fathom_pack_append without moving its rows; the
+                         scan, top-k and steps work on the first n tokens, and a step's K/V rows
+                         are `capacity` tokens long. */
 } fathom_index_desc;
 
 /* Message for the calling thread's last failure ("" if none). */
@@ -109,6 +114,25 @@ int fathom_pack_workspace_bytes(const fathom_index_desc* desc, size_t* bytes);
  * outputs are unspecified. */
 int fathom_pack(const fathom_index_desc* desc, const void* K, int k_dtype, uint32_t* planes, uint16_t* meta,
                 float* var, void* workspace, size_t ws_bytes, void* stream);
+
+/* Streaming append: grow a packed index from n_old to desc->n tokens per row
+ * (desc->capacity fixed, >= desc->n), as new keys arrive during decoding.  The
+ * quantiser works per 128-token block, so only the blocks from the one holding
+ * token n_old (a partial block is re-quantised with its new tokens) to the one
+ * holding token n-1 are written; the result is bit-identical to fathom_pack of
+ * all n tokens with the same capacity.
+ *   K_tail   device, [rows][n - t0][128] of k_dtype: the keys of tokens
+ *            t0 .. n-1 of every row, t0 = 128*floor(n_old/128) (the start of the
+ *            block holding token n_old; the caller keeps the keys of a partial
+ *            last block until it fills).
+ *   planes, meta  as packed by fathom_pack (or earlier appends) with this capacity.
+ *   workspace  device scratch of at least 256 bytes (an error flag).
+ * var is not touched: it stays the variance the index was packed with (the
+ * importance weights of the allocation), until the caller packs again.
+ * EINVAL if n_old is outside [0, n]; n_old == n is a no-op.  Synchronises
+ * `stream` (EDATA as fathom_pack). */
+int fathom_pack_append(const fathom_index_desc* desc, int64_t n_old, const void* K_tail, int k_dtype,
+                       uint32_t* planes, uint16_t* meta, void* workspace, size_t ws_bytes, void* stream);
 
 /* Per-query allocation by reverse water-filling ([A] "How each query picks its
  * own depth").
@@ -252,7 +276,8 @@ int fathom_sparse_attn_heads(int rows, int group, int64_t n, int64_t k, const vo
  * 4-bit dequantisation lo + delta*code_c(t), read back from the index (planes,
  * meta of `desc`, as packed by fathom_pack) -- no 16-bit K copy is read.
  *   V        device or mapped host, rows of v_stride elements of v_dtype
- *            (token t of row r at V + (r*n + t)*v_stride).
+ *            (token t of row r at V + (r*capacity + t)*v_stride, capacity of
+ *            the index desc, n when it is 0).
  *   idx      device int32 [rows][k]; entries < 0 are skipped.
  * The gather reads, per winner, one 32-bit word of each of the 512 (channel,
  * plane) runs of its superblock: far more bytes than a 256-byte K row, so
@@ -289,7 +314,8 @@ typedef struct fathom_step_desc {
   const float* var;         /* device [rows][128] */
   const uint16_t* budgets;  /* device [rows] or NULL */
   const void* q;            /* device [rows*group][128] */
-  const void* K;            /* device or mapped host, rows of kv_stride elements (NULL with FATHOM_KSRC_INDEX) */
+  const void* K;            /* device or mapped host, rows of kv_stride elements (NULL with FATHOM_KSRC_INDEX);
+                               token t of row r at (r*capacity + t)*kv_stride, capacity of `index` */
   const void* V;            /* device or mapped host, rows of kv_stride elements */
   int32_t* idx;             /* device [rows][k] out ([rows*group][k] for FATHOM_GQA_PER_HEAD) */
   float* out;               /* device [rows*group][128] out */

@@ -29,6 +29,18 @@ extern "C" {
 int fathom_probe_stream_read(const void* buf, size_t bytes, int blocks_per_sm, int threads, uint32_t* sink,
                              void* stream);
 
+/* Integer ALU rate, for the machine balance of integer operations per byte of
+ * bandwidth ([A] "Where this does not work": about five integer operations per
+ * byte on an A100 or H100, so a scan that is arithmetic-bound on one of them is
+ * on all).  A grid of blocks_per_sm x (number of SMs) CTAs of `threads`
+ * threads; every thread runs 8 independent chains of `iters` steps, each step
+ * two right shifts and one three-input XOR: 24 * iters ALU operations per
+ * thread.  *sink (device uint32) keeps the result live.  Asynchronous. */
+int fathom_probe_int_ops(int iters, int blocks_per_sm, int threads, uint32_t* sink, void* stream);
+
+/* Number of SMs of the current device (the probes' grid unit). */
+int fathom_probe_num_sms(void);
+
 #ifdef __cplusplus
 }
 #endif

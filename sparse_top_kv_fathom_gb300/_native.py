@@ -14,7 +14,7 @@ SZP = ctypes.POINTER(ctypes.c_size_t)
 
 class IndexDesc(ctypes.Structure):
     _fields_ = [("n", ctypes.c_int64), ("rows", ctypes.c_int32), ("d", ctypes.c_int32),
-                ("block", ctypes.c_int32), ("superblock", ctypes.c_int32)]
+                ("block", ctypes.c_int32), ("superblock", ctypes.c_int32), ("capacity", ctypes.c_int64)]
 
 
 class StepDesc(ctypes.Structure):
@@ -45,6 +45,7 @@ SIGNATURES = {
     "fathom_index_bytes": ([IDP, SZP, SZP], I32),
     "fathom_pack_workspace_bytes": ([IDP, SZP], I32),
     "fathom_pack": ([IDP, P, I32, P, P, P, P, SZ, P], I32),
+    "fathom_pack_append": ([IDP, I64, P, I32, P, P, P, SZ, P], I32),
     "fathom_allocate": ([I32, I32, P, I32, P, P, I32, P, P, P, P], I32),
     "fathom_allocate_sparq": ([I32, I32, P, I32, I32, P, P, P, P], I32),
     "fathom_allocate_heads": ([I32, I32, P, I32, P, P, I32, P, P, P, P], I32),
@@ -65,6 +66,8 @@ SIGNATURES = {
     "fathom_fixed136_step_workspace_bytes": ([ctypes.POINTER(Fixed136StepDesc), SZP], I32),
     "fathom_fixed136_decode_step": ([ctypes.POINTER(Fixed136StepDesc), P, SZ, P], I32),
     "fathom_probe_stream_read": ([P, SZ, I32, I32, P, P], I32),
+    "fathom_probe_int_ops": ([I32, I32, I32, P, P], I32),
+    "fathom_probe_num_sms": ([], I32),
     "fathom_host_alloc": ([SZ, ctypes.POINTER(ctypes.c_void_p)], I32),
     "fathom_host_free": ([P, SZ], I32),
 }

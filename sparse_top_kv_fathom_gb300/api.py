@@ -41,8 +41,8 @@ def _ws(nbytes, device):
     return torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device)
 
 
-def _desc(n, rows, S):
-    return N.IndexDesc(int(n), int(rows), D, QBLOCK, int(S))
+def _desc(n, rows, S, capacity=0):
+    return N.IndexDesc(int(n), int(rows), D, QBLOCK, int(S), int(capacity or 0))
 
 
 def index_bytes(n, rows, superblock):
@@ -57,46 +57,68 @@ def index_bytes(n, rows, superblock):
 @dataclass
 class BitPlaneIndex:
     """Packed index.  planes: int32 (bit patterns) [rows][nsb][128][4][S/32];
-    meta: fp16 [rows][128][nblk][2] (lo, delta); var: fp32 [rows][128]."""
+    meta: fp16 [rows][128][nblk][2] (lo, delta); var: fp32 [rows][128].  nsb and nblk count
+    superblocks and blocks of the capacity (0: n), which lets the index grow by pack_append."""
     planes: torch.Tensor
     meta: torch.Tensor
     var: torch.Tensor
     n: int
     rows: int
     superblock: int
+    capacity: int = 0
 
     @property
     def desc(self):
-        return _desc(self.n, self.rows, self.superblock)
+        return _desc(self.n, self.rows, self.superblock, self.capacity)
 
     def to_host(self):
         """A copy whose planes and meta live in pinned host memory (read over the host link)."""
         return BitPlaneIndex(self.planes.cpu().pin_memory(), self.meta.cpu().pin_memory(), self.var, self.n,
-                             self.rows, self.superblock)
+                             self.rows, self.superblock, self.capacity)
 
 
-def index_shapes(n, rows, superblock):
-    nsb = -(-n // superblock)
-    nblk = -(-n // QBLOCK)
+def index_shapes(n, rows, superblock, capacity=None):
+    cap = capacity or n
+    nsb = -(-cap // superblock)
+    nblk = -(-cap // QBLOCK)
     return (rows, nsb, D, 4, superblock // 32), (rows, D, nblk, 2)
 
 
-def pack(K, superblock=4096, stream=None):
-    """K: [rows][n][128] cuda tensor (fp32/fp16/bf16) -> BitPlaneIndex on K's device."""
+def pack(K, superblock=4096, stream=None, capacity=None):
+    """K: [rows][n][128] cuda tensor (fp32/fp16/bf16) -> BitPlaneIndex on K's device, laid out for
+    `capacity` tokens per row (default n)."""
     L = lib()
     rows, n, d = K.shape
     assert d == D and K.is_cuda and K.is_contiguous()
-    ps, ms = index_shapes(n, rows, superblock)
+    ps, ms = index_shapes(n, rows, superblock, capacity)
     planes = torch.empty(ps, dtype=torch.int32, device=K.device)
     meta = torch.empty(ms, dtype=torch.float16, device=K.device)
     var = torch.empty((rows, D), dtype=torch.float32, device=K.device)
-    desc = _desc(n, rows, superblock)
+    desc = _desc(n, rows, superblock, capacity)
     wsb = ctypes.c_size_t()
     N.check(L.fathom_pack_workspace_bytes(ctypes.byref(desc), ctypes.byref(wsb)))
     ws = _ws(wsb.value, K.device)
     N.check(L.fathom_pack(ctypes.byref(desc), _ptr(K), _dt(K), _ptr(planes), _ptr(meta), _ptr(var), _ptr(ws),
                           wsb.value, _stream(stream)))
-    return BitPlaneIndex(planes, meta, var, n, rows, superblock)
+    return BitPlaneIndex(planes, meta, var, n, rows, superblock, capacity or 0)
+
+
+def pack_append(index, K_tail, n_new, stream=None):
+    """Grow `index` (packed with a capacity >= n_new) to n_new tokens per row.  K_tail:
+    [rows][n_new - t0][128] cuda tensor, the keys of tokens t0 .. n_new-1 with
+    t0 = 128 * (index.n // 128).  Returns the grown index (the same planes and meta tensors)."""
+    L = lib()
+    rows, m, d = K_tail.shape
+    t0 = QBLOCK * (index.n // QBLOCK)
+    if d != D or rows != index.rows or m != n_new - t0 or not K_tail.is_contiguous():
+        raise ValueError("K_tail must be a contiguous [rows][n_new - %d][128] tensor" % t0)
+    grown = BitPlaneIndex(index.planes, index.meta, index.var, int(n_new), index.rows, index.superblock,
+                          index.capacity)
+    d_ = grown.desc
+    ws = _ws(256, K_tail.device)
+    N.check(L.fathom_pack_append(ctypes.byref(d_), int(index.n), _ptr(K_tail), _dt(K_tail), _ptr(index.planes),
+                                 _ptr(index.meta), _ptr(ws), 256, _stream(stream)))
+    return grown
 
 
 def allocate(q, var, budget, group, status=None, stream=None):
@@ -409,3 +431,24 @@ def probe_stream_read(buf, blocks_per_sm=4, threads=512, sink=None, stream=None)
     nbytes -= nbytes % 16
     N.check(L.fathom_probe_stream_read(_ptr(buf), nbytes, blocks_per_sm, threads, _ptr(sink), _stream(stream)))
     return nbytes
+
+
+def probe_int_ops(iters=4096, blocks_per_sm=4, threads=256, reps=5, stream=None):
+    """Integer ALU operations per second (the rate of fathom_probe_int_ops: 24 * iters operations
+    per thread), best of `reps` timed launches."""
+    L = lib()
+    sink = torch.zeros(1, dtype=torch.int32, device="cuda")
+    st = torch.cuda.current_stream() if stream is None else stream
+    ops = 24.0 * iters * threads * blocks_per_sm * L.fathom_probe_num_sms()
+    best = 0.0
+    with torch.cuda.stream(st):
+        N.check(L.fathom_probe_int_ops(iters, blocks_per_sm, threads, _ptr(sink), _stream(st)))
+        for _ in range(reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(st)
+            N.check(L.fathom_probe_int_ops(iters, blocks_per_sm, threads, _ptr(sink), _stream(st)))
+            e1.record(st)
+            e1.synchronize()
+            best = max(best, ops / (e0.elapsed_time(e1) * 1e-3))
+    return best
+

@@ -74,11 +74,16 @@ int index_geom(const fathom_index_desc* d, IndexGeom* g) {
   int S = d->superblock;
   if (S < 128 || S > 65536 || (S & (S - 1)) != 0)
     return set_error(FATHOM_EINVAL, "superblock must be a power of two in [128, 65536] (got %d)", S);
+  const int64_t cap = d->capacity ? d->capacity : d->n;
+  if (cap < d->n || cap > (int64_t(1) << 31) - 1)
+    return set_error(FATHOM_EINVAL, "capacity must be 0 or in [n, 2^31-1] (got %lld)", (long long)d->capacity);
   g->n = d->n;
+  g->cap = cap;
   g->rows = d->rows;
   g->S = S;
-  g->nsb = (d->n + S - 1) / S;
-  g->nblk = (d->n + kBlock - 1) / kBlock;
+  g->nsb = (cap + S - 1) / S;
+  g->nblk = (cap + kBlock - 1) / kBlock;
+  g->nblk_live = (d->n + kBlock - 1) / kBlock;
   int l = 0;
   while ((1 << l) < S) ++l;
   g->log2S = l;
@@ -93,7 +98,7 @@ extern "C" {
 
 const char* fathom_last_error(void) { return g_err; }
 
-int fathom_abi_version(void) { return 2; }
+int fathom_abi_version(void) { return 3; }
 
 int fathom_index_bytes(const fathom_index_desc* desc, size_t* plane_bytes, size_t* meta_bytes) {
   IndexGeom g;

@@ -502,8 +502,9 @@ cudaError_t launch_attn(int rows, int group, int64_t n, int64_t k, const void* q
 cudaError_t launch_attn_q4(const IndexGeom& g, int group, int64_t k, const void* q, int q_dtype,
                            const uint32_t* planes, const __half2* meta, const void* V, int v_dtype, int64_t v_stride,
                            const int32_t* idx, float* out, uint16_t* out_bf16, cudaStream_t st, bool per_head) {
-  const KeysQ4::Args a{planes, meta, g.n, g.nsb, g.nblk, g.log2S};
-  return launch_attn_any<SelQ4>(g.rows, group, g.n, k, q, q_dtype, nullptr, &a, V, v_dtype, v_stride, idx, out,
+  // V rows, like the index, are `capacity` tokens long
+  const KeysQ4::Args a{planes, meta, g.cap, g.nsb, g.nblk, g.log2S};
+  return launch_attn_any<SelQ4>(g.rows, group, g.cap, k, q, q_dtype, nullptr, &a, V, v_dtype, v_stride, idx, out,
                                 out_bf16, st, per_head);
 }
 

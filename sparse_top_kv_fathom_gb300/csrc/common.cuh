@@ -80,11 +80,13 @@ struct Carve {
 
 // --------------------------------------------------- internal launchers ---
 struct IndexGeom {
-  int64_t n;
+  int64_t n;          // live tokens per row
+  int64_t cap;        // tokens of storage per row (>= n): the layout strides follow it
   int rows;
   int S;
-  int64_t nsb;   // superblocks per row
-  int64_t nblk;  // 128-token blocks per row
+  int64_t nsb;        // superblocks per row (of the capacity)
+  int64_t nblk;       // 128-token blocks per row (of the capacity): the meta row stride
+  int64_t nblk_live;  // blocks holding live tokens
   int log2S;
 };
 int index_geom(const fathom_index_desc* d, IndexGeom* g);

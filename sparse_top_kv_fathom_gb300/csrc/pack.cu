@@ -1,5 +1,6 @@
 // fathom_pack: K cache -> 4-bit bit-plane index (MSB-first planes, channel-major)
-// plus per-(channel, 128-token block) fp16 (lo, delta) and per-channel variance.
+// plus per-(channel, 128-token block) fp16 (lo, delta) and per-channel variance;
+// fathom_pack_append: the same quantiser on the blocks new tokens fall in.
 //
 // Follows the Fathom article, "Bit planes: how a partial read becomes a valid
 // read" (store the first bits of a block of tokens together, then the second
@@ -19,14 +20,17 @@ namespace {
 
 constexpr int kErrRange = 1;
 
-// One CTA per (row, 128-token block), one thread per channel.
-// Blocks past n (padding inside the last superblock) write zero plane words.
+// One CTA per (row, 128-token block), one thread per channel; block b0 + blockIdx.x.
+// Blocks past n (padding up to the capacity's last superblock) write zero plane
+// words and zero meta.  Key of token t of row r: K[(r*krow + t - korg)*128 + c]
+// (the whole row, or the tail of an append).  part: per-block sums for the
+// variance, or NULL.
 __global__ void __launch_bounds__(kD) pack_quant_kernel(const void* __restrict__ K, int k_dtype, int64_t n, int64_t nblk,
-                                                        int64_t nsb, int log2S, uint32_t* __restrict__ planes,
-                                                        __half2* __restrict__ meta, double* __restrict__ part,
-                                                        int* __restrict__ err) {
+                                                        int64_t nsb, int log2S, int64_t b0, int64_t krow, int64_t korg,
+                                                        uint32_t* __restrict__ planes, __half2* __restrict__ meta,
+                                                        double* __restrict__ part, int* __restrict__ err) {
   const int c = threadIdx.x;
-  const int64_t b = blockIdx.x;  // block index inside the row, < nsb * S / 128
+  const int64_t b = b0 + blockIdx.x;  // block index inside the row, < nsb * S / 128
   const int r = blockIdx.y;
   const int64_t S = int64_t(1) << log2S;
   const int64_t t0 = b * kBlock;
@@ -35,14 +39,15 @@ __global__ void __launch_bounds__(kD) pack_quant_kernel(const void* __restrict__
   const int64_t run = S >> 5;
   uint32_t* pw = planes + (((int64_t(r) * nsb + sb) * kD + c) * kPlanes) * run + w0;
 
-  if (t0 >= n) {  // padding block: zero words only
+  if (t0 >= n) {  // padding block: zero words only (and zero meta inside the capacity)
     const uint4 z = make_uint4(0, 0, 0, 0);
 #pragma unroll
     for (int j = 0; j < kPlanes; ++j) *reinterpret_cast<uint4*>(pw + j * run) = z;
+    if (b < nblk) meta[(int64_t(r) * kD + c) * nblk + b] = __floats2half2_rn(0.0f, 0.0f);
     return;
   }
   const int64_t t1 = (t0 + kBlock < n) ? t0 + kBlock : n;
-  const int64_t base = int64_t(r) * n * kD + c;
+  const int64_t base = (int64_t(r) * krow - korg) * kD + c;
 
   float lo = load_as_float(K, base + t0 * kD, k_dtype), hi = lo;
   bool bad = !(fabsf(lo) <= 65504.0f);
@@ -88,17 +93,18 @@ __global__ void __launch_bounds__(kD) pack_quant_kernel(const void* __restrict__
   }
 #pragma unroll
   for (int j = 0; j < kPlanes; ++j) *reinterpret_cast<uint4*>(pw + j * run) = words[j];
-  part[(int64_t(r) * kD + c) * nblk + b] = psum;
+  if (part) part[(int64_t(r) * kD + c) * nblk + b] = psum;
 }
 
-// One thread per (row, channel): sum block partials in block order.
-__global__ void pack_mean_kernel(const double* __restrict__ part, int rows, int64_t nblk, int64_t n,
+// One thread per (row, channel): sum the live blocks' partials in block order
+// (partials are laid out with the capacity's row stride nblk).
+__global__ void pack_mean_kernel(const double* __restrict__ part, int rows, int64_t nblk, int64_t nlive, int64_t n,
                                  double* __restrict__ mean) {
   const int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
   if (i >= int64_t(rows) * kD) return;
   const double* p = part + i * nblk;
   double tot = 0.0;
-  for (int64_t b = 0; b < nblk; ++b) tot = __dadd_rn(tot, p[b]);
+  for (int64_t b = 0; b < nlive; ++b) tot = __dadd_rn(tot, p[b]);
   mean[i] = __ddiv_rn(tot, double(n));
 }
 
@@ -119,13 +125,13 @@ __global__ void __launch_bounds__(kD) pack_m2_kernel(const void* __restrict__ K,
   part[(int64_t(r) * kD + c) * nblk + b] = s;
 }
 
-__global__ void pack_var_kernel(const double* __restrict__ part, int rows, int64_t nblk, int64_t n,
+__global__ void pack_var_kernel(const double* __restrict__ part, int rows, int64_t nblk, int64_t nlive, int64_t n,
                                 float* __restrict__ var) {
   const int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
   if (i >= int64_t(rows) * kD) return;
   const double* p = part + i * nblk;
   double m2 = 0.0;
-  for (int64_t b = 0; b < nblk; ++b) m2 = __dadd_rn(m2, p[b]);
+  for (int64_t b = 0; b < nlive; ++b) m2 = __dadd_rn(m2, p[b]);
   var[i] = __double2float_rn(__ddiv_rn(m2, double(n)));
 }
 
@@ -178,20 +184,54 @@ int fathom_pack(const fathom_index_desc* desc, const void* K, int k_dtype, uint3
   const int64_t blocks_all = g.nsb * (int64_t(g.S) / kBlock);
   if (blocks_all > 0x7fffffff || g.rows > 65535) return set_error(FATHOM_EINVAL, "index too large for one launch");
   dim3 gq(unsigned(blocks_all), unsigned(g.rows));
-  pack_quant_kernel<<<gq, kD, 0, st>>>(dK, k_dtype, g.n, g.nblk, g.nsb, g.log2S, (uint32_t*)dP, (__half2*)dM, part,
-                                       err);
+  pack_quant_kernel<<<gq, kD, 0, st>>>(dK, k_dtype, g.n, g.nblk, g.nsb, g.log2S, 0, g.n, 0, (uint32_t*)dP,
+                                       (__half2*)dM, part, err);
   FATHOM_TRY_CUDA(cudaGetLastError());
   const int rc = g.rows * kD;
-  pack_mean_kernel<<<(rc + 127) / 128, 128, 0, st>>>(part, g.rows, g.nblk, g.n, mean);
+  pack_mean_kernel<<<(rc + 127) / 128, 128, 0, st>>>(part, g.rows, g.nblk, g.nblk_live, g.n, mean);
   FATHOM_TRY_CUDA(cudaGetLastError());
-  pack_m2_kernel<<<dim3(unsigned(g.nblk), unsigned(g.rows)), kD, 0, st>>>(dK, k_dtype, g.n, g.nblk, mean, part);
+  pack_m2_kernel<<<dim3(unsigned(g.nblk_live), unsigned(g.rows)), kD, 0, st>>>(dK, k_dtype, g.n, g.nblk, mean,
+                                                                                part);
   FATHOM_TRY_CUDA(cudaGetLastError());
-  pack_var_kernel<<<(rc + 127) / 128, 128, 0, st>>>(part, g.rows, g.nblk, g.n, (float*)dV);
+  pack_var_kernel<<<(rc + 127) / 128, 128, 0, st>>>(part, g.rows, g.nblk, g.nblk_live, g.n, (float*)dV);
   FATHOM_TRY_CUDA(cudaGetLastError());
   int herr = 0;
   FATHOM_TRY_CUDA(cudaMemcpyAsync(&herr, err, sizeof(int), cudaMemcpyDeviceToHost, st));
   FATHOM_TRY_CUDA(cudaStreamSynchronize(st));
   if (herr & kErrRange) return set_error(FATHOM_EDATA, "K holds a non-finite value or one outside the fp16 range");
+  return FATHOM_OK;
+}
+
+int fathom_pack_append(const fathom_index_desc* desc, int64_t n_old, const void* K_tail, int k_dtype,
+                       uint32_t* planes, uint16_t* meta, void* workspace, size_t ws_bytes, void* stream) {
+  clear_error();
+  IndexGeom g;
+  FATHOM_TRY(index_geom(desc, &g));
+  if (!valid_dtype(k_dtype)) return set_error(FATHOM_EINVAL, "k_dtype %d invalid", k_dtype);
+  if (n_old < 0 || n_old > g.n) return set_error(FATHOM_EINVAL, "n_old %lld outside [0, n]", (long long)n_old);
+  const int64_t b0 = n_old / kBlock, b1 = g.nblk_live;  // blocks [b0, b1) are (re)written
+  if (b0 >= b1) return FATHOM_OK;
+  const void *dK, *dP, *dM, *dW;
+  FATHOM_TRY(device_view(K_tail, "K_tail", &dK));
+  FATHOM_TRY(device_view(planes, "planes", &dP));
+  FATHOM_TRY(device_view(meta, "meta", &dM));
+  FATHOM_TRY(device_view(workspace, "workspace", &dW));
+  if (ws_bytes < 256) return set_error(FATHOM_ENOMEM, "workspace %zu < 256 bytes", ws_bytes);
+  if ((reinterpret_cast<uintptr_t>(dP) & 15) != 0 || (reinterpret_cast<uintptr_t>(dM) & 3) != 0 ||
+      (reinterpret_cast<uintptr_t>(dW) & 3) != 0)
+    return set_error(FATHOM_EINVAL, "planes must be 16-byte aligned, meta and workspace 4-byte aligned");
+  if (b1 - b0 > 0x7fffffff || g.rows > 65535) return set_error(FATHOM_EINVAL, "append too large for one launch");
+  cudaStream_t st = as_stream(stream);
+  int* err = static_cast<int*>(const_cast<void*>(dW));
+  FATHOM_TRY_CUDA(cudaMemsetAsync(err, 0, sizeof(int), st));
+  const int64_t t0 = b0 * kBlock;  // K_tail holds tokens t0 .. n-1 of every row
+  pack_quant_kernel<<<dim3(unsigned(b1 - b0), unsigned(g.rows)), kD, 0, st>>>(
+      dK, k_dtype, g.n, g.nblk, g.nsb, g.log2S, b0, g.n - t0, t0, (uint32_t*)dP, (__half2*)dM, nullptr, err);
+  FATHOM_TRY_CUDA(cudaGetLastError());
+  int herr = 0;
+  FATHOM_TRY_CUDA(cudaMemcpyAsync(&herr, err, sizeof(int), cudaMemcpyDeviceToHost, st));
+  FATHOM_TRY_CUDA(cudaStreamSynchronize(st));
+  if (herr & kErrRange) return set_error(FATHOM_EDATA, "K_tail holds a non-finite value or one outside the fp16 range");
   return FATHOM_OK;
 }
 

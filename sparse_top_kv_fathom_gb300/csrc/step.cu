@@ -116,7 +116,7 @@ int fathom_decode_step(const fathom_step_desc* s, void* workspace, size_t ws_byt
                                      s->kv_dtype, s->kv_stride, (const int32_t*)dI, (float*)dO, (uint16_t*)dB, st,
                                      gqa == FATHOM_GQA_PER_HEAD));
     else
-      FATHOM_TRY_CUDA(launch_attn(g.rows, s->group, g.n, s->k, dq, s->q_dtype, dK, dV, s->kv_dtype, s->kv_stride,
+      FATHOM_TRY_CUDA(launch_attn(g.rows, s->group, g.cap, s->k, dq, s->q_dtype, dK, dV, s->kv_dtype, s->kv_stride,
                                   (const int32_t*)dI, (float*)dO, (uint16_t*)dB, w.attn, st,
                                   gqa == FATHOM_GQA_PER_HEAD));
     return FATHOM_OK;
@@ -136,7 +136,7 @@ int fathom_decode_step(const fathom_step_desc* s, void* workspace, size_t ws_byt
     FATHOM_TRY_CUDA(launch_attn_q4(g, s->group, s->k, dq, s->q_dtype, (const uint32_t*)dP, (const __half2*)dM, dV,
                                    s->kv_dtype, s->kv_stride, (const int32_t*)dI, (float*)dO, (uint16_t*)dB, st));
   else
-    FATHOM_TRY_CUDA(launch_attn(g.rows, s->group, g.n, s->k, dq, s->q_dtype, dK, dV, s->kv_dtype, s->kv_stride,
+    FATHOM_TRY_CUDA(launch_attn(g.rows, s->group, g.cap, s->k, dq, s->q_dtype, dK, dV, s->kv_dtype, s->kv_stride,
                                 (const int32_t*)dI, (float*)dO, (uint16_t*)dB, w.attn, st));
   return FATHOM_OK;
 }

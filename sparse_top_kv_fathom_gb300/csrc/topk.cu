@@ -31,7 +31,7 @@ constexpr int kBitmapWords = 32768;  // n <= 2^20: the chosen indices leave the 
 constexpr int kRegionA = kBitmapWords > kSortMax ? kBitmapWords : kSortMax;  // bitmap or sort buffer (words)
 constexpr int kPassThreads = 256;
 constexpr int kPassItems = 16;  // items per thread in the histogram / compaction passes
-constexpr int kCompactCtasPerSm = 3;  // resident CTAs per SM of the persistent compaction pass
+constexpr int kCompactCtasPerSm = 3;  // resident CTAs per SM of the candidate pass
 
 struct RowState {
   uint32_t b1;      // bin (top 12 key bits) holding the k-th largest key
@@ -183,39 +183,6 @@ __global__ void __launch_bounds__(kFinThreads) topk_bin_kernel(int64_t k, const 
   }
 }
 
-// Candidate pass over all (row, tile) pairs, each CTA a contiguous range of
-// them: keys in bins above b1 go to the row's sure list, keys in b1 to its
-// candidate list.  Per tile every thread counts its hits, one block scan of the
-// packed counts gives each thread its slots, and the next tile's scores are in
-// flight meanwhile.
-template <bool kVec>
-struct CompactTile {
-  static constexpr int kItems = kPassItems;
-  static constexpr int kTile = kPassThreads * kItems;
-  // position of a thread's item i inside the tile
-  __device__ static int pos(int i) {
-    return kVec ? 4 * ((i >> 2) * kPassThreads + int(threadIdx.x)) + (i & 3) : i * kPassThreads + int(threadIdx.x);
-  }
-  __device__ static void load(const float* __restrict__ s, int64_t n, int64_t t0, float (&v)[kItems]) {
-    if (kVec && t0 + kTile <= n) {
-#pragma unroll
-      for (int j = 0; j < kItems / 4; ++j) {
-        const float4 x = __ldg(reinterpret_cast<const float4*>(s + t0) + j * kPassThreads + threadIdx.x);
-        v[4 * j] = x.x;
-        v[4 * j + 1] = x.y;
-        v[4 * j + 2] = x.z;
-        v[4 * j + 3] = x.w;
-      }
-    } else {
-#pragma unroll
-      for (int i = 0; i < kItems; ++i) {
-        const int64_t t = t0 + pos(i);
-        v[i] = t < n ? __ldg(s + t) : 0.0f;
-      }
-    }
-  }
-};
-
 // Key of a score without branches: sign-dependent flip, -0.0 moved onto +0.0's key
 // (the same map as score_key).
 __device__ __forceinline__ uint32_t score_key_fast(float v) {
@@ -224,24 +191,60 @@ __device__ __forceinline__ uint32_t score_key_fast(float v) {
   return k + uint32_t(u == 0x80000000u);
 }
 
-// Hits of a CTA are staged in shared memory across its tiles and written out
-// (one slot reservation per list) when the row changes, the stage would
-// overflow, or the CTA is done; a tile with more hits than the stage holds is
-// written straight to the global lists.  The same-address atomics on the
-// row counters are thus about one per CTA instead of two per tile.
-constexpr int kStage = 1024;
+// Candidate pass: keys in bins above b1 go to the row's sure list, keys in b1
+// to its candidate list.  Every warp works on its own: it streams a contiguous
+// run of 512-score chunks (the next chunk in flight while the current one is
+// classified), counts its lanes' hits, and stages them in a private 64-entry
+// buffer in shared memory, which it writes out (one atomic per list reserves
+// the slots) when it would overflow, when the row changes, and at the end.  No
+// block barrier anywhere; a chunk with more hits than the buffer holds is
+// written straight to the global lists.
+constexpr int kChunk = 32 * kPassItems;  // scores per warp chunk
+constexpr int kWStage = 64;              // staged entries per warp and list
 
-__device__ __forceinline__ void stage_flush(int64_t row, int ns, int nc, int64_t bs, int64_t bc, int64_t k,
-                                            int64_t cap, const int32_t* st_si, const uint32_t* st_ck,
-                                            const int32_t* st_ci, int32_t* sure, uint32_t* cand_key,
-                                            int32_t* cand_idx) {
-  for (int i = threadIdx.x; i < ns; i += kPassThreads)
-    if (bs + i < k) sure[row * k + bs + i] = st_si[i];
-  for (int i = threadIdx.x; i < nc; i += kPassThreads)
-    if (bc + i < cap) {
-      cand_key[row * cap + bc + i] = st_ck[i];
-      cand_idx[row * cap + bc + i] = st_ci[i];
+template <bool kVec>
+struct WarpChunk {
+  // position of lane's item i inside the chunk
+  __device__ static int pos(int i, int lane) { return kVec ? 4 * ((i >> 2) * 32 + lane) + (i & 3) : i * 32 + lane; }
+  __device__ static void load(const float* __restrict__ s, int64_t n, int64_t t0, int lane, float (&v)[kPassItems]) {
+    if (kVec && t0 + kChunk <= n) {
+#pragma unroll
+      for (int j = 0; j < kPassItems / 4; ++j) {
+        const float4 x = __ldg(reinterpret_cast<const float4*>(s + t0) + j * 32 + lane);
+        v[4 * j] = x.x;
+        v[4 * j + 1] = x.y;
+        v[4 * j + 2] = x.z;
+        v[4 * j + 3] = x.w;
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < kPassItems; ++i) {
+        const int64_t t = t0 + pos(i, lane);
+        v[i] = t < n ? __ldg(s + t) : 0.0f;
+      }
     }
+  }
+};
+
+// Write out a warp's staged hits of `row` (ns sure, nc candidates).
+__device__ __forceinline__ void warp_flush(int64_t row, int ns, int nc, int lane, RowState* state, int64_t k,
+                                           int64_t cap, const int32_t* si, const uint32_t* ck, const int32_t* ci,
+                                           int32_t* sure, uint32_t* cand_key, int32_t* cand_idx) {
+  int bs = 0, bc = 0;
+  if (lane == 0) {
+    bs = ns ? atomicAdd(&state[row].sure_cnt, ns) : 0;
+    bc = nc ? atomicAdd(&state[row].cand_cnt, nc) : 0;
+  }
+  bs = __shfl_sync(0xffffffffu, bs, 0);
+  bc = __shfl_sync(0xffffffffu, bc, 0);
+  for (int i = lane; i < ns; i += 32)
+    if (int64_t(bs) + i < k) sure[row * k + bs + i] = si[i];
+  for (int i = lane; i < nc; i += 32)
+    if (int64_t(bc) + i < cap) {
+      cand_key[row * cap + bc + i] = ck[i];
+      cand_idx[row * cap + bc + i] = ci[i];
+    }
+  __syncwarp();  // the buffer is free again
 }
 
 template <bool kVec>
@@ -251,129 +254,110 @@ __global__ void __launch_bounds__(kPassThreads, kCompactCtasPerSm) topk_compact_
                                                                     int32_t* __restrict__ sure,
                                                                     uint32_t* __restrict__ cand_key,
                                                                     int32_t* __restrict__ cand_idx) {
-  using C = CompactTile<kVec>;
-  static_assert(C::kItems <= 16 && C::kTile < 65536, "packed 16-bit counts");
+  using C = WarpChunk<kVec>;
   constexpr int kWarps = kPassThreads / 32;
-  __shared__ uint32_t s_warp[kWarps];  // inclusive scan of the warps' packed counts
-  __shared__ int32_t st_si[kStage];    // staged sure winners
-  __shared__ uint32_t st_ck[kStage];   // staged candidates (key, index)
-  __shared__ int32_t st_ci[kStage];
-  // Per tile, written by the control thread (warp 0, lane kWarps-1) between the tile's first two
-  // barriers and read by all after them: [0], [1] stage offsets of this tile's sure / candidate
-  // hits, [2] flush the stage first?, [3] this tile direct to global?, [4], [5] slot bases of the
-  // flushed hits, [6], [7] slot bases of a direct tile, [8] row, [9], [10] counts of the flushed
-  // stage.  The stage's own state (row, counts) is touched by the control thread only until the
-  // last tile is done.
-  __shared__ int64_t s_ctl[11];
-  __shared__ int64_t s_row;
-  __shared__ int s_ns, s_nc;
-  const int64_t tiles_row = (n + C::kTile - 1) / C::kTile;
-  const int64_t total = tiles_row * rows;
+  static_assert(kPassItems <= 16, "packed 16-bit counts");
+  __shared__ int32_t st_si[kWarps][kWStage];
+  __shared__ uint32_t st_ck[kWarps][kWStage];
+  __shared__ int32_t st_ci[kWarps][kWStage];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  // a contiguous range of (row, tile) pairs per CTA: a CTA's tiles mostly share one row
-  const int64_t per = (total + gridDim.x - 1) / gridDim.x;
-  const int64_t g0 = int64_t(blockIdx.x) * per, g1 = g0 + per < total ? g0 + per : total;
-  if (g0 >= g1) return;
-  if (threadIdx.x == 0) {
-    s_row = g0 / tiles_row;
-    s_ns = s_nc = 0;
-  }
-  float cur[C::kItems];
-  C::load(scores + (g0 / tiles_row) * n, n, (g0 % tiles_row) * C::kTile, cur);
-  for (int64_t g = g0; g < g1; ++g) {
-    const int64_t r = g / tiles_row;
-    const int64_t t0 = (g % tiles_row) * C::kTile;
-    float nxt[C::kItems];
-    if (g + 1 < g1) C::load(scores + ((g + 1) / tiles_row) * n, n, ((g + 1) % tiles_row) * C::kTile, nxt);
+  int32_t* si = st_si[warp];
+  uint32_t* ck = st_ck[warp];
+  int32_t* ci = st_ci[warp];
+  const int64_t chunks_row = (n + kChunk - 1) / kChunk;
+  const int64_t total = chunks_row * rows;
+  const int64_t nw = int64_t(gridDim.x) * kWarps;
+  const int64_t per = (total + nw - 1) / nw;
+  const int64_t c0 = (int64_t(blockIdx.x) * kWarps + warp) * per;
+  const int64_t c1 = c0 + per < total ? c0 + per : total;
+  if (c0 >= c1) return;  // whole warps only: no block barrier follows
+  int ns_st = 0, nc_st = 0;  // staged counts (warp-uniform)
+  // (row, first token) of the current chunk and of the next one, stepped without divisions
+  int64_t r = c0 / chunks_row, t0 = (c0 % chunks_row) * kChunk;
+  int64_t rn = t0 + kChunk < n ? r : r + 1, tn = t0 + kChunk < n ? t0 + kChunk : 0;
+  int64_t row_st = r;
+  float cur[kPassItems];
+  C::load(scores + r * n, n, t0, lane, cur);
+  for (int64_t c = c0; c < c1; ++c) {
+    float nxt[kPassItems];
+    if (c + 1 < c1) C::load(scores + rn * n, n, tn, lane, nxt);
     // keys in (khi, ~0] are sure, keys in [klo, khi] candidates
     const uint32_t b1 = __ldg(&state[r].b1);
-    const uint32_t klo = b1 << (32 - kHistBits), khi = klo | ((1u << (32 - kHistBits)) - 1u);
-    const int lim = n - t0 < C::kTile ? int(n - t0) : C::kTile;  // items of this tile inside the row
-    uint32_t ns = 0u, nc = 0u;
-    if (lim == C::kTile) {
+    constexpr uint32_t kSpan = (1u << (32 - kHistBits)) - 1u;
+    const uint32_t klo = b1 << (32 - kHistBits), khi = klo | kSpan;
+    const int lim = n - t0 < kChunk ? int(n - t0) : kChunk;  // items of this chunk inside the row
+    uint32_t ms = 0u, mc = 0u;  // bit i: this lane's item i is a sure winner / a candidate
 #pragma unroll
-      for (int i = 0; i < C::kItems; ++i) {
-        const uint32_t key = score_key_fast(cur[i]);
-        ns += key > khi;
-        nc += key >= klo && key <= khi;
-      }
-    } else {
-#pragma unroll
-      for (int i = 0; i < C::kItems; ++i) {
-        const uint32_t key = score_key_fast(cur[i]);
-        const bool in = C::pos(i) < lim;
-        ns += in && key > khi;
-        nc += in && key >= klo && key <= khi;
-      }
+    for (int i = 0; i < kPassItems; ++i) {
+      const uint32_t key = score_key_fast(cur[i]);
+      ms |= uint32_t(key > khi) << i;
+      mc |= uint32_t(key - klo <= kSpan) << i;
     }
-    const uint32_t mine = ns | (nc << 16);
+    if (lim < kChunk) {  // the row's last chunk: drop items past n
+      uint32_t vm = 0u;
+#pragma unroll
+      for (int i = 0; i < kPassItems; ++i) vm |= uint32_t(C::pos(i, lane) < lim) << i;
+      ms &= vm;
+      mc &= vm;
+    }
+    const uint32_t mine = uint32_t(__popc(ms)) | (uint32_t(__popc(mc)) << 16);
     uint32_t x = mine;  // inclusive warp scan of the packed (sure, candidate) counts
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
       if (lane >= o) x += y;
     }
-    if (lane == 31) s_warp[warp] = x;
-    __syncthreads();
-    if (warp == 0) {
-      uint32_t v = lane < kWarps ? s_warp[lane] : 0u;
+    const uint32_t tot = __shfl_sync(0xffffffffu, x, 31);
+    const int ts = int(tot & 0xFFFFu), tc = int(tot >> 16);
+    if (ts == 0 && tc == 0) {
+      if (c + 1 < c1) {
 #pragma unroll
-      for (int o = 1; o < kWarps; o <<= 1) {
-        const uint32_t y = __shfl_up_sync(0xffffffffu, v, o);
-        if (lane >= o) v += y;
+        for (int i = 0; i < kPassItems; ++i) cur[i] = nxt[i];
       }
-      if (lane < kWarps) s_warp[lane] = v;
-      if (lane == kWarps - 1) {  // the control thread
-        const int ts = int(v & 0xFFFFu), tc = int(v >> 16);
-        const bool direct = ts > kStage || tc > kStage;
-        const bool flush = s_ns + s_nc > 0 && (s_row != r || direct || s_ns + ts > kStage || s_nc + tc > kStage);
-        s_ctl[2] = flush;
-        s_ctl[3] = direct;
-        if (flush) {  // reserve the staged hits' slots in their row's lists
-          s_ctl[4] = s_ns ? atomicAdd(&state[s_row].sure_cnt, s_ns) : 0;
-          s_ctl[5] = s_nc ? atomicAdd(&state[s_row].cand_cnt, s_nc) : 0;
-          s_ctl[8] = s_row;
-          s_ctl[9] = s_ns;
-          s_ctl[10] = s_nc;
-          s_ns = s_nc = 0;
-        }
-        if (direct) {  // this tile's own hits go straight to the global lists
-          s_ctl[6] = ts ? atomicAdd(&state[r].sure_cnt, ts) : 0;
-          s_ctl[7] = tc ? atomicAdd(&state[r].cand_cnt, tc) : 0;
-        } else {
-          s_ctl[0] = s_ns;
-          s_ctl[1] = s_nc;
-          s_ns += ts;
-          s_nc += tc;
-          s_row = r;
-        }
+      r = rn;
+      t0 = tn;
+      if (tn + kChunk < n) {
+        tn += kChunk;
+      } else {
+        ++rn;
+        tn = 0;
       }
+      continue;
     }
-    __syncthreads();
-    if (s_ctl[2]) {  // rare: write out the stage before this tile's hits land in it
-      stage_flush(s_ctl[8], int(s_ctl[9]), int(s_ctl[10]), s_ctl[4], s_ctl[5], k, cap, st_si, st_ck, st_ci, sure,
-                  cand_key, cand_idx);
-      __syncthreads();
+    const bool direct = ts > kWStage || tc > kWStage;
+    if (ns_st + nc_st > 0 && (row_st != r || direct || ns_st + ts > kWStage || nc_st + tc > kWStage)) {
+      warp_flush(row_st, ns_st, nc_st, lane, state, k, cap, si, ck, ci, sure, cand_key, cand_idx);
+      ns_st = nc_st = 0;
     }
-    const bool direct = s_ctl[3] != 0;
-    if (mine) {  // this thread holds hits: find them again and place them
-      const uint32_t excl = x - mine + (warp ? s_warp[warp - 1] : 0u);
-      int64_t ps = int64_t(excl & 0xFFFFu) + (direct ? s_ctl[6] : s_ctl[0]);
-      int64_t pc = int64_t(excl >> 16) + (direct ? s_ctl[7] : s_ctl[1]);
+    int64_t ps, pc;  // this lane's first slot in each list (stage or global)
+    const uint32_t excl = x - mine;
+    if (direct) {
+      int bs = 0, bc = 0;
+      if (lane == 0) {
+        bs = ts ? atomicAdd(&state[r].sure_cnt, ts) : 0;
+        bc = tc ? atomicAdd(&state[r].cand_cnt, tc) : 0;
+      }
+      ps = int64_t(__shfl_sync(0xffffffffu, bs, 0)) + (excl & 0xFFFFu);
+      pc = int64_t(__shfl_sync(0xffffffffu, bc, 0)) + (excl >> 16);
+    } else {
+      ps = ns_st + (excl & 0xFFFFu);
+      pc = nc_st + (excl >> 16);
+    }
+    if (mine) {  // this lane holds hits: place them, visiting only the marked items
+      const uint32_t hit = ms | mc;
 #pragma unroll
-      for (int i = 0; i < C::kItems; ++i) {
-        const uint32_t key = score_key_fast(cur[i]);
-        const int p = C::pos(i);
-        if (p >= lim) continue;
-        const int32_t t = int32_t(t0 + p);
-        if (key > khi) {
-          if (!direct) st_si[ps] = t;
+      for (int i = 0; i < kPassItems; ++i) {
+        if (!((hit >> i) & 1u)) continue;
+        const int32_t t = int32_t(t0 + C::pos(i, lane));
+        if ((ms >> i) & 1u) {
+          if (!direct) si[ps] = t;
           else if (ps < k) sure[r * k + ps] = t;
           ++ps;
-        } else if (key >= klo) {
+        } else {
+          const uint32_t key = score_key_fast(cur[i]);
           if (!direct) {
-            st_ck[pc] = key;
-            st_ci[pc] = t;
+            ck[pc] = key;
+            ci[pc] = t;
           } else if (pc < cap) {
             cand_key[r * cap + pc] = key;
             cand_idx[r * cap + pc] = t;
@@ -382,21 +366,26 @@ __global__ void __launch_bounds__(kPassThreads, kCompactCtasPerSm) topk_compact_
         }
       }
     }
-    __syncthreads();  // stage writes and s_warp / s_ctl reads done before the next tile
-    if (g + 1 < g1) {
+    __syncwarp();  // staged entries visible to the whole warp
+    if (!direct) {
+      ns_st += ts;
+      nc_st += tc;
+      row_st = r;
+    }
+    if (c + 1 < c1) {
 #pragma unroll
-      for (int i = 0; i < C::kItems; ++i) cur[i] = nxt[i];
+      for (int i = 0; i < kPassItems; ++i) cur[i] = nxt[i];
+    }
+    r = rn;
+    t0 = tn;
+    if (tn + kChunk < n) {
+      tn += kChunk;
+    } else {
+      ++rn;
+      tn = 0;
     }
   }
-  // the control thread's last update of the stage state is visible after the loop's last barrier
-  if (s_ns + s_nc > 0) {
-    if (threadIdx.x == 0) {
-      s_ctl[4] = s_ns ? atomicAdd(&state[s_row].sure_cnt, s_ns) : 0;
-      s_ctl[5] = s_nc ? atomicAdd(&state[s_row].cand_cnt, s_nc) : 0;
-    }
-    __syncthreads();
-    stage_flush(s_row, s_ns, s_nc, s_ctl[4], s_ctl[5], k, cap, st_si, st_ck, st_ci, sure, cand_key, cand_idx);
-  }
+  if (ns_st + nc_st > 0) warp_flush(row_st, ns_st, nc_st, lane, state, k, cap, si, ck, ci, sure, cand_key, cand_idx);
 }
 
 // Bitonic sort (ascending) of s[0..m) in shared memory, m a power of two.

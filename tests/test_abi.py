@@ -109,3 +109,20 @@ def test_no_oracle_in_product_path():
         if f.endswith((".py", ".c")):
             text = open(os.path.join(ROOT, "oracle", f)).read()
             assert "sparse_top_kv_fathom_gb300" not in text and "fathom.h" not in text, f
+
+
+def test_index_capacity_sets_the_layout_strides():
+    """capacity (0 = n) fixes the per-row strides; below n it is rejected (host-only queries)."""
+    from sparse_top_kv_fathom_gb300 import _native as N
+    L = N.load()
+    pb, mb = ctypes.c_size_t(), ctypes.c_size_t()
+    n, S = 5000, 1024
+    d0 = N.IndexDesc(n, 2, 128, 128, S, 0)
+    assert L.fathom_index_bytes(ctypes.byref(d0), ctypes.byref(pb), ctypes.byref(mb)) == 0
+    assert (pb.value, mb.value) == (2 * 5 * 128 * 4 * (S // 32) * 4, 2 * 128 * 40 * 4)
+    d1 = N.IndexDesc(n, 2, 128, 128, S, 9000)
+    assert L.fathom_index_bytes(ctypes.byref(d1), ctypes.byref(pb), ctypes.byref(mb)) == 0
+    assert (pb.value, mb.value) == (2 * 9 * 128 * 4 * (S // 32) * 4, 2 * 128 * 71 * 4)
+    bad = N.IndexDesc(n, 2, 128, 128, S, n - 1)
+    assert L.fathom_index_bytes(ctypes.byref(bad), ctypes.byref(pb), ctypes.byref(mb)) == 1
+    assert b"capacity" in L.fathom_last_error()

@@ -372,3 +372,58 @@ def test_decode_step_with_keys_from_the_index(case, gpu_lib, gqa):
         ref = oracle.sparse_attn_q4(case["planes"], case["meta"], f32(case["q"]), f32(case["V"]), gi, w.group, w.n,
                                     case["S"])
     check_attn(out.cpu().numpy(), outb, ref)
+
+
+# ------------------------------------------------- capacity and streaming append ---
+def _relayout(planes_cap, meta_cap, n, S):
+    """The live part of a capacity-laid-out index in the compact layout of n tokens."""
+    nsb, nblk = -(-n // S), -(-n // 128)
+    return planes_cap[:, :nsb], meta_cap[:, :, :nblk]
+
+
+def test_pack_with_capacity_is_the_compact_pack_relaid(case, gpu_lib):
+    F, w = gpu_lib, case["w"]
+    cap = w.n + 3 * case["S"] + 77
+    ix = F.pack(case["Kd"], case["S"], capacity=cap)
+    P, M = ix.planes.cpu().numpy().view(np.uint32), ix.meta.cpu().numpy().view(np.uint16)
+    p, m = _relayout(P, M, w.n, case["S"])
+    assert np.array_equal(p, case["planes"]) and np.array_equal(m, case["meta"])
+    assert not P[:, p.shape[1]:].any() and not M[:, :, m.shape[2]:].any()  # storage past n is zero
+    assert np.array_equal(ix.var.cpu().numpy().view(np.uint32), case["var"].view(np.uint32))
+    # the scan and the step see the same first n tokens: identical results
+    bits, qbar = F.allocate(case["qd"], ix.var, 92, w.group)
+    assert torch.equal(F.scan(ix, bits, qbar), F.scan(case["index"], bits, qbar))
+    Kc = torch.zeros((w.rows, cap, 128), dtype=case["Kd"].dtype, device="cuda")
+    Vc = torch.zeros_like(Kc)
+    Kc[:, :w.n], Vc[:, :w.n] = case["Kd"], case["Vd"]  # K/V rows are `capacity` tokens long too
+    k = min(w.k, w.n)
+    a = F.decode_step(case["index"], case["qd"], case["Kd"], case["Vd"], k, w.group, 92)
+    b = F.decode_step(ix, case["qd"], Kc, Vc, k, w.group, 92)
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+
+
+def test_streaming_append_equals_packing_everything(case, gpu_lib):
+    """pack the first n1 tokens, append in steps (partial blocks, superblock boundaries): the planes
+    and meta are bit-identical to packing all n tokens at once with the same capacity."""
+    F, w = gpu_lib, case["w"]
+    S, n = case["S"], w.n
+    cap = n + 200
+    K = case["Kd"]
+    full = F.pack(K, S, capacity=cap)
+    n1 = max(1, n // 3 + 5)
+    ix = F.pack(K[:, :n1].contiguous(), S, capacity=cap)
+    var1 = ix.var.clone()
+    for n_new in sorted({min(n, n1 + 1), min(n, n1 + 130), min(n, 2 * n // 3 + 7), n}):
+        if n_new <= ix.n:
+            continue
+        t0 = 128 * (ix.n // 128)
+        ix = F.pack_append(ix, K[:, t0:n_new].contiguous(), n_new)
+    assert ix.n == n
+    assert torch.equal(ix.planes, full.planes) and torch.equal(ix.meta, full.meta)
+    assert torch.equal(ix.var, var1)  # the append leaves the variance as packed
+    # out-of-range keys in an append are reported
+    bad = K[:, 128 * (n1 // 128):n1 + 1].float().contiguous()
+    bad[0, -1, 3] = float("inf")
+    ix2 = F.pack(K[:, :n1].contiguous(), S, capacity=cap)
+    with pytest.raises(Exception, match="fp16 range"):
+        F.pack_append(ix2, bad, n1 + 1)
