@@ -59,6 +59,8 @@ def parse():
     p.add_argument("--layers", type=int, default=None, help="override layer count (smaller runs)")
     p.add_argument("--n", type=int, default=None, help="override tokens per row (smaller runs)")
     p.add_argument("--profile", action="store_true", help="few launches, for ncu")
+    p.add_argument("--filter", action="store_true",
+                   help="time the step with the fused scan -> top-k filter (hints carried between steps)")
     return p.parse_args()
 
 
@@ -195,7 +197,7 @@ class Model:
         return self.F.BitPlaneIndex(store["planes"][r0:r1], store["meta"][r0:r1], self.var[r0:r1], self.w.n,
                                     r1 - r0, self.S)
 
-    def steps(self, store, q, out, idx, ws=None, sparq_r=0, k_source="rows"):
+    def steps(self, store, q, out, idx, ws=None, sparq_r=0, k_source="rows", hint=False):
         """DecodeStep objects sharing one workspace; outputs are views of out/idx.  Layers of one
         model run one after the other (a layer's query depends on the previous layer); independent
         sessions run as one batched step over all their rows."""
@@ -215,7 +217,7 @@ class Model:
             res.append(F.DecodeStep(ixs[i], store["K"][k0:k1], store["V"][k0:k1],
                                     q[r0 * G:r1 * G], w.k, G, budget, workspace=ws,
                                     idx=idx[r0:r1], out=out[r0 * G:r1 * G], out_bf16=out_b[r0 * G:r1 * G],
-                                    sparq_r=sparq_r, k_source=k_source))
+                                    sparq_r=sparq_r, k_source=k_source, hint=True if hint else None))
         return res
 
     def comparator_steps(self, store, q, out, idx):
@@ -266,6 +268,26 @@ def time_graph(g, steps, warmup, stream, clocks=None):
         ck = clocks.stop() if clocks else None
     per = [ev[i].elapsed_time(ev[i + 1]) for i in range(steps)]
     return ev[0].elapsed_time(ev[-1]), per, ck
+
+
+def time_graph_rotating(g, q, qsets, steps, warmup, stream):
+    """Like time_graph, but each step first copies the next of `qsets` into the step's queries
+    (device to device, inside the timed region): a new query every step."""
+    with torch.cuda.stream(stream):
+        for i in range(warmup):
+            q.copy_(qsets[i % len(qsets)], non_blocking=True)
+            g.replay()
+        torch.cuda.synchronize()
+        barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(steps):
+            q.copy_(qsets[(warmup + i) % len(qsets)], non_blocking=True)
+            g.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+    return e0.elapsed_time(e1)
 
 
 def barrier():
@@ -539,7 +561,7 @@ def main():
         q = model.q
         out = torch.empty((w.rows * w.group, D), dtype=torch.float32, device="cuda")
         idx = torch.empty((w.rows, w.k), dtype=torch.int32, device="cuda")
-        steps = model.steps(store, q, out, idx)
+        steps = model.steps(store, q, out, idx, hint=args.filter)
         g = capture(steps, stream)
         clocks = Clocks(local) if res == primary else None
         total, per, ck = time_graph(g, args.steps, args.warmup, stream, clocks)
@@ -567,6 +589,20 @@ def main():
                 r["sparq"]["r%d" % rr] = {"ms_per_step": max_over_ranks(stot) / args.steps,
                                           "bits_per_key_read": 4 * rr + 32 * rr / 128}
                 del sg
+            # fused scan -> top-k filter, with a new query every step (hints carried from the last one)
+            qsets = [torch.cat([synth.queries(w, l, "cuda", step=st_) for l in range(w.layers)]).contiguous()
+                     for st_ in range(1, 5)]
+            q_keep = q.clone()
+            pg = capture(model.steps(store, q, cout, cidx), stream)
+            ptot = time_graph_rotating(pg, q, qsets, args.steps, args.warmup, stream)
+            del pg
+            fg = capture(model.steps(store, q, cout, cidx, hint=True), stream)
+            ftot = time_graph_rotating(fg, q, qsets, args.steps, args.warmup, stream)
+            del fg
+            q.copy_(q_keep)
+            r["fused_filter"] = {"ms_per_step": max_over_ranks(ftot) / args.steps,
+                                 "plain_ms_per_step": max_over_ranks(ptot) / args.steps,
+                                 "queries": "4 query sets in rotation, a new one every step (copied in, timed)"}
             # unified 4-bit store: attention reads the winners' keys back from the bit-plane index
             ug = capture(model.steps(store, q, cout, cidx, k_source="index"), stream)
             utot, _, _ = time_graph(ug, args.steps, args.warmup, stream)
@@ -648,10 +684,12 @@ def main():
         line["comparator"] = {"index": "fixed 136-bit (32 channels x 4 bit + 8-bit scale)",
                               "ms_per_step": p.get("comparator_ms_per_step"),
                               "fathom_speedup": p.get("comparator_ms_per_step", 0) / p["ms_per_step"],
-                              "sparq": p.get("sparq"), "unified_store": p.get("unified_store")}
+                              "sparq": p.get("sparq"), "unified_store": p.get("unified_store"),
+                              "fused_filter": p.get("fused_filter")}
         if "device" in result and "hbm_resident" in line:
             line["hbm_resident"]["sparq"] = result["device"].get("sparq")
             line["hbm_resident"]["unified_store"] = result["device"].get("unified_store")
+            line["hbm_resident"]["fused_filter"] = result["device"].get("fused_filter")
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(model, model.h if model.h else model.d, log)
     if rank == 0:

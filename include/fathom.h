@@ -321,6 +321,15 @@ typedef struct fathom_step_desc {
   float* out;               /* device [rows*group][128] out */
   uint16_t* out_bf16;       /* device [rows*group][128] out or NULL */
   int32_t* status;          /* device int32 or NULL (FATHOM_STATUS_* bits) */
+  uint32_t* hint;           /* device uint32 [rows] or NULL: the fused scan -> top-k filter (with
+                               FATHOM_GQA_SUM; ignored otherwise).  hint[r] is a score key (the
+                               order-preserving map of the fp32 score, -0.0 as +0.0); the scan lists
+                               every key at or above it as a top-k candidate, and a row whose list
+                               holds at least k and at most the list's capacity keys skips the
+                               top-k's pass over all its scores.  The result is the same either way.
+                               Each step rewrites hint[r] for the next step of the same rows: the
+                               first key of the bin below the k-th key's 12-bit bin.  Keep one
+                               array per set of rows (per layer); 0 lists every key (no saving). */
 } fathom_step_desc;
 
 int fathom_decode_step_workspace_bytes(const fathom_step_desc* step, size_t* bytes);

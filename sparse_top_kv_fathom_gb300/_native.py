@@ -23,7 +23,7 @@ class StepDesc(ctypes.Structure):
                 ("kv_stride", ctypes.c_int64), ("sparq_r", ctypes.c_int32), ("gqa_mode", ctypes.c_int32),
                 ("k_source", ctypes.c_int32), ("reserved", ctypes.c_int32),
                 ("planes", P), ("meta", P), ("var", P), ("budgets", P), ("q", P), ("K", P), ("V", P),
-                ("idx", P), ("out", P), ("out_bf16", P), ("status", P)]
+                ("idx", P), ("out", P), ("out_bf16", P), ("status", P), ("hint", P)]
 
 
 class Fixed136StepDesc(ctypes.Structure):

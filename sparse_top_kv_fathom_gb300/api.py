@@ -257,7 +257,7 @@ class DecodeStep:
     K, V:  [rows][n][128] (device or pinned host), q: [rows*group][128] (device)."""
 
     def __init__(self, index, K, V, q, k, group, budget, status=None, device=None, workspace=None, idx=None,
-                 out=None, out_bf16=None, sparq_r=0, gqa="sum", k_source="rows"):
+                 out=None, out_bf16=None, sparq_r=0, gqa="sum", k_source="rows", hint=None):
         self.L = lib()
         self.index, self.K, self.V, self.q = index, K, V, q
         dev = device if device is not None else q.device
@@ -270,6 +270,10 @@ class DecodeStep:
                          torch.empty((rows * group, D), dtype=torch.bfloat16, device=dev))
         self.budgets = budget if isinstance(budget, torch.Tensor) else None
         self.status = status
+        # fused scan -> top-k filter: True gives this step its own per-row hints (start: 0 = every key)
+        if hint is True:
+            hint = torch.zeros(rows, dtype=torch.int32, device=dev)
+        self.hint = hint
         self.desc = N.StepDesc()
         self.desc.index = index.desc
         self.desc.group = group
@@ -309,6 +313,7 @@ class DecodeStep:
         d.K = self.K.data_ptr() if self.K is not None else None
         d.idx, d.out, d.out_bf16 = self.idx.data_ptr(), self.out.data_ptr(), self.out_bf16.data_ptr()
         d.status = self.status.data_ptr() if self.status is not None else None
+        d.hint = self.hint.data_ptr() if self.hint is not None else None
 
     def __call__(self, stream=None):
         N.check(self.L.fathom_decode_step(ctypes.byref(self.desc), _ptr(self.ws), self.ws_bytes, _stream(stream)))

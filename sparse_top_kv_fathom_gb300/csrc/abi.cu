@@ -98,7 +98,7 @@ extern "C" {
 
 const char* fathom_last_error(void) { return g_err; }
 
-int fathom_abi_version(void) { return 3; }
+int fathom_abi_version(void) { return 4; }
 
 int fathom_index_bytes(const fathom_index_desc* desc, size_t* plane_bytes, size_t* meta_bytes) {
   IndexGeom g;

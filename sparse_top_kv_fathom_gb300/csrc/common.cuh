@@ -95,6 +95,21 @@ int index_geom(const fathom_index_desc* d, IndexGeom* g);
 size_t topk_ws_bytes(int rows, int64_t n, int64_t k);
 size_t attn_ws_bytes(int rows, int group, int64_t k);
 
+// The scan's fused top-k filter: every key at or above the row's hint is appended
+// (key, index) to the row's candidate list and counted; the top-k then skips its
+// candidate pass for rows whose filter kept at least k and at most cap keys.
+struct ScanFilter {
+  const uint32_t* hint;  // [rows] key threshold per row
+  uint32_t* cand_key;    // [rows][cap]
+  int32_t* cand_idx;     // [rows][cap]
+  int64_t cap;
+  int32_t* cnt;          // row r's counter at cnt[r * cnt_stride] (zeroed before the scan)
+  int cnt_stride;
+};
+ScanFilter topk_scan_filter(void* ws, int rows, int64_t n, int64_t k, const uint32_t* hint);
+// bytes from the top-k histogram to the end of the row states (one memset clears both)
+size_t topk_state_clear_bytes(int rows);
+
 // launchers used by the step functions (arguments already validated)
 cudaError_t launch_allocate(int rows, int group, const void* q, int q_dtype, const float* var, const uint16_t* budgets,
                             int budget, uint8_t* bits, float* qbar, int32_t* status, cudaStream_t st);
@@ -107,9 +122,11 @@ cudaError_t launch_qbar(int rows, int group, const void* q, int q_dtype, float* 
 cudaError_t launch_allocate_sparq(int rows, int group, const void* q, int q_dtype, int r_channels, uint8_t* bits,
                                   float* qbar, int32_t* status, cudaStream_t st);
 cudaError_t launch_scan(const IndexGeom& g, const uint32_t* planes, const __half2* meta, const uint8_t* bits,
-                        const float* qbar, float* scores, uint32_t* hist, cudaStream_t st);
+                        const float* qbar, float* scores, uint32_t* hist, cudaStream_t st,
+                        const ScanFilter* filter = nullptr);
+// hint: the fused filter's per-row hints (read, and rewritten for the next step), or NULL
 cudaError_t launch_topk(int rows, int64_t n, int64_t k, const float* scores, int32_t* idx, float* vals, void* ws,
-                        bool hist_ready, cudaStream_t st);
+                        bool hist_ready, cudaStream_t st, uint32_t* hint = nullptr);
 // per_head: idx holds one winner set per query head ([rows*group][k]), each head attends over its own
 cudaError_t launch_attn(int rows, int group, int64_t n, int64_t k, const void* q, int q_dtype, const void* K,
                         const void* V, int kv_dtype, int64_t kv_stride, const int32_t* idx, float* out, uint16_t* out_bf16, void* ws,

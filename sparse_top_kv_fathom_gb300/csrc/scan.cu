@@ -29,7 +29,9 @@
 //     two tokens at a time (packed f32x2), so each term carries only a few ulps
 //     of |qbar_c * x_c| of error.
 // Inside the decode step the kernel also builds the 12-bit first-digit
-// histogram of its scores for the top-k.
+// histogram of its scores for the top-k, and, with the step's fused filter,
+// lists every key at or above the row's hint (the previous step's k-th key,
+// one histogram bin lower) as a top-k candidate.
 #include "bitplane.cuh"
 #include "common.cuh"
 
@@ -87,14 +89,15 @@ __device__ __forceinline__ void channel_terms(float2* acc, uint32_t w0, uint32_t
   }
 }
 
-template <int TOK, bool kHist>
+template <int TOK, bool kHist, bool kFilter>
 __global__ void __launch_bounds__(ScanCfg<TOK>::kThreads, 4) scan_kernel(const uint32_t* __restrict__ planes,
                                                                          const __half2* __restrict__ meta,
                                                                          const uint8_t* __restrict__ bits,
                                                                          const float* __restrict__ qbar,
                                                                          float* __restrict__ scores,
                                                                          uint32_t* __restrict__ hist, int64_t n,
-                                                                         int64_t nsb, int log2S, int64_t nblk) {
+                                                                         int64_t nsb, int log2S, int64_t nblk,
+                                                                         const ScanFilter flt) {
   constexpr int T = ScanCfg<TOK>::kThreads;
   constexpr int W = ScanCfg<TOK>::kWords;
   using PW = PlaneWords<W>;
@@ -105,6 +108,7 @@ __global__ void __launch_bounds__(ScanCfg<TOK>::kThreads, 4) scan_kernel(const u
   __shared__ typename PW::T s_w[kStages][kPlanes][T];
   __shared__ __half2 s_m[kStages][T];
   __shared__ uint32_t s_hist[kHist ? kHistBins : 1];
+  __shared__ int s_fcnt, s_fbase;  // the CTA's filter candidates, and their first slot in the row's list
 
   const int r = blockIdx.y;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -122,6 +126,7 @@ __global__ void __launch_bounds__(ScanCfg<TOK>::kThreads, 4) scan_kernel(const u
   if constexpr (kHist) {
     for (int i = tid; i < kHistBins; i += T) s_hist[i] = 0u;
   }
+  if (tid == 0) s_fcnt = 0;
   __syncthreads();
   int nact = 0;
 #pragma unroll
@@ -248,6 +253,54 @@ __global__ void __launch_bounds__(ScanCfg<TOK>::kThreads, 4) scan_kernel(const u
       }
     }
   }
+  if constexpr (kFilter) {
+    // fused top-k filter: append (key, index) of every key at or above the row's hint
+    const uint32_t tau = __ldg(flt.hint + r);
+    uint32_t mk[W];  // bit b of mk[w]: token t0 + 32w + b is at or above the hint
+    int cnt = 0;
+#pragma unroll
+    for (int w = 0; w < W; ++w) {
+      mk[w] = 0u;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        mk[w] |= uint32_t(valid && t0 + 32 * w + i < n && score_key(acc[16 * w + i].x) >= tau) << i;
+        mk[w] |= uint32_t(valid && t0 + 32 * w + 16 + i < n && score_key(acc[16 * w + i].y) >= tau) << (16 + i);
+      }
+      cnt += __popc(mk[w]);
+    }
+    int x = cnt;  // inclusive warp scan of the counts
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    // slots: warp offset inside the CTA (shared counter), then one global reservation per CTA
+    int wbase = 0;
+    if (lane == 31 && x) wbase = atomicAdd(&s_fcnt, x);
+    wbase = __shfl_sync(0xffffffffu, wbase, 31);
+    __syncthreads();
+    if (tid == 0) s_fbase = s_fcnt ? atomicAdd(flt.cnt + int64_t(r) * flt.cnt_stride, s_fcnt) : 0;
+    __syncthreads();
+    const int base = s_fbase + wbase;
+    if (cnt && base < flt.cap) {  // once the row's list is full the row falls back: stop writing
+      int64_t slot = int64_t(base) + x - cnt;
+      uint32_t* ck = flt.cand_key + int64_t(r) * flt.cap;
+      int32_t* ci = flt.cand_idx + int64_t(r) * flt.cap;
+#pragma unroll
+      for (int w = 0; w < W; ++w) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          if (!((mk[w] >> i) & 1u)) continue;
+          const float v = i < 16 ? acc[16 * w + i].x : acc[16 * w + i - 16].y;
+          if (slot < flt.cap) {
+            ck[slot] = score_key(v);
+            ci[slot] = int32_t(t0 + 32 * w + i);
+          }
+          ++slot;
+        }
+      }
+    }
+  }
   if constexpr (kHist) {
     __syncthreads();
     uint32_t* gh = hist + int64_t(r) * kHistBins;
@@ -260,26 +313,31 @@ __global__ void __launch_bounds__(ScanCfg<TOK>::kThreads, 4) scan_kernel(const u
 
 template <int TOK>
 cudaError_t launch_scan_t(const IndexGeom& g, const uint32_t* planes, const __half2* meta, const uint8_t* bits,
-                          const float* qbar, float* scores, uint32_t* hist, cudaStream_t st) {
+                          const float* qbar, float* scores, uint32_t* hist, cudaStream_t st, const ScanFilter* f) {
   const int64_t tiles = (g.n + kScanTile - 1) / kScanTile;
   const dim3 grid{unsigned(tiles), unsigned(g.rows), 1u};
   constexpr int T = ScanCfg<TOK>::kThreads;
-  if (hist)
-    scan_kernel<TOK, true><<<grid, T, 0, st>>>(planes, meta, bits, qbar, scores, hist, g.n, g.nsb, g.log2S, g.nblk);
+  const ScanFilter none{};
+  if (hist && f)
+    scan_kernel<TOK, true, true><<<grid, T, 0, st>>>(planes, meta, bits, qbar, scores, hist, g.n, g.nsb, g.log2S,
+                                                     g.nblk, *f);
+  else if (hist)
+    scan_kernel<TOK, true, false><<<grid, T, 0, st>>>(planes, meta, bits, qbar, scores, hist, g.n, g.nsb, g.log2S,
+                                                      g.nblk, none);
   else
-    scan_kernel<TOK, false><<<grid, T, 0, st>>>(planes, meta, bits, qbar, scores, nullptr, g.n, g.nsb, g.log2S,
-                                                g.nblk);
+    scan_kernel<TOK, false, false><<<grid, T, 0, st>>>(planes, meta, bits, qbar, scores, nullptr, g.n, g.nsb,
+                                                       g.log2S, g.nblk, none);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_scan(const IndexGeom& g, const uint32_t* planes, const __half2* meta, const uint8_t* bits,
-                        const float* qbar, float* scores, uint32_t* hist, cudaStream_t st) {
+                        const float* qbar, float* scores, uint32_t* hist, cudaStream_t st, const ScanFilter* f) {
   // two plane words per thread need 8-byte aligned planes (every run of S >= 128 tokens is)
   if ((reinterpret_cast<uintptr_t>(planes) & 7) == 0)
-    return launch_scan_t<64>(g, planes, meta, bits, qbar, scores, hist, st);
-  return launch_scan_t<32>(g, planes, meta, bits, qbar, scores, hist, st);
+    return launch_scan_t<64>(g, planes, meta, bits, qbar, scores, hist, st, f);
+  return launch_scan_t<32>(g, planes, meta, bits, qbar, scores, hist, st, f);
 }
 
 }  // namespace fathom

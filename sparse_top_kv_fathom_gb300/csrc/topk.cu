@@ -37,9 +37,11 @@ struct RowState {
   uint32_t b1;      // bin (top 12 key bits) holding the k-th largest key
   int32_t above;    // keys in bins above b1
   int32_t sure_cnt;
-  int32_t cand_cnt;
-  int32_t pad[4];
+  int32_t cand_cnt; // candidates listed (with the scan's filter: keys at or above the row's hint)
+  int32_t fast;     // 1: the filter's candidates hold the top k, the candidate pass is skipped
+  int32_t pad[3];
 };
+static_assert(sizeof(RowState) == 32, "RowState layout");
 
 struct TopkWs {
   uint32_t* hist;
@@ -152,12 +154,37 @@ __global__ void __launch_bounds__(kPassThreads) topk_hist_kernel(int64_t n, cons
     if (h[i]) atomicAdd(hist + int64_t(r) * kHistBins + i, h[i]);
 }
 
-// One CTA (1024 threads) per row: locate the bin of the k-th largest key.
-__global__ void __launch_bounds__(kFinThreads) topk_bin_kernel(int64_t k, const uint32_t* __restrict__ hist,
+// The filter hint left for the row's next step: the first key of the bin below
+// the k-th largest key's bin (the next query's k-th key may drift down by up to
+// one bin, 1/8 of an octave -- at least 8 % in score -- and the top k still
+// clear the hint, while the list stays near twice k).
+__device__ __forceinline__ uint32_t next_hint(uint32_t T) {
+  const uint32_t b = T >> (32 - kHistBits);
+  return b >= 1u ? (b - 1u) << (32 - kHistBits) : 0u;
+}
+
+// One CTA (1024 threads) per row: locate the bin of the k-th largest key.  With
+// the scan's filter (hint != NULL), a row whose filter kept at least k and at
+// most cap keys is marked fast instead: its top k are among those candidates.
+__global__ void __launch_bounds__(kFinThreads) topk_bin_kernel(int64_t k, int64_t cap,
+                                                               const uint32_t* __restrict__ hint,
+                                                               const uint32_t* __restrict__ hist,
                                                                RowState* __restrict__ state) {
   __shared__ uint32_t h[kFinThreads];
   __shared__ int s_out[2];
   const int r = blockIdx.x;
+  if (hint) {
+    const int32_t cnt = state[r].cand_cnt;  // keys at or above the hint, counted by the scan
+    if (cnt >= k && cnt <= cap) {           // uniform across the CTA
+      __syncthreads();                      // every thread has read cand_cnt
+      if (threadIdx.x == 0) {
+        state[r].fast = 1;
+        state[r].above = 0;
+        state[r].sure_cnt = 0;
+      }
+      return;
+    }
+  }
   // fold the 4096 bins into 1024 groups of 4 (from the top), then refine inside the group
   const uint32_t* hr = hist + int64_t(r) * kHistBins;
   const int g = threadIdx.x;
@@ -178,7 +205,8 @@ __global__ void __launch_bounds__(kFinThreads) topk_bin_kernel(int64_t k, const 
     st.above = before;
     st.sure_cnt = 0;
     st.cand_cnt = 0;
-    st.pad[0] = st.pad[1] = st.pad[2] = st.pad[3] = 0;
+    st.fast = 0;
+    st.pad[0] = st.pad[1] = st.pad[2] = 0;
     state[r] = st;
   }
 }
@@ -277,11 +305,26 @@ __global__ void __launch_bounds__(kPassThreads, kCompactCtasPerSm) topk_compact_
   int64_t rn = t0 + kChunk < n ? r : r + 1, tn = t0 + kChunk < n ? t0 + kChunk : 0;
   int64_t row_st = r;
   float cur[kPassItems];
-  C::load(scores + r * n, n, t0, lane, cur);
+  if (!__ldg(&state[r].fast)) C::load(scores + r * n, n, t0, lane, cur);
   for (int64_t c = c0; c < c1; ++c) {
     float nxt[kPassItems];
-    if (c + 1 < c1) C::load(scores + rn * n, n, tn, lane, nxt);
+    if (c + 1 < c1 && !__ldg(&state[rn].fast)) C::load(scores + rn * n, n, tn, lane, nxt);
     // keys in (khi, ~0] are sure, keys in [klo, khi] candidates
+    if (__ldg(&state[r].fast)) {  // the scan's filter already listed this row's candidates
+      if (c + 1 < c1) {
+#pragma unroll
+        for (int i = 0; i < kPassItems; ++i) cur[i] = nxt[i];
+      }
+      r = rn;
+      t0 = tn;
+      if (tn + kChunk < n) {
+        tn += kChunk;
+      } else {
+        ++rn;
+        tn = 0;
+      }
+      continue;
+    }
     const uint32_t b1 = __ldg(&state[r].b1);
     constexpr uint32_t kSpan = (1u << (32 - kHistBits)) - 1u;
     const uint32_t klo = b1 << (32 - kHistBits), khi = klo | kSpan;
@@ -416,7 +459,7 @@ __device__ void bitonic_sort(int32_t* s, int m) {
 // Exact select directly over the row's n scores (one CTA): threshold key T, the
 // index cut among keys equal to T, then ordered output.
 __device__ void select_row_direct(int64_t n, int64_t k, const float* s, int32_t* out_idx, float* out_vals,
-                                  uint32_t* h, int* s_out) {
+                                  uint32_t* h, int* s_out, uint32_t* hint_out) {
   const int tid = threadIdx.x;
   // --- threshold key by three digits: 12 bits (in 4 folds of 1024), 10, 10
   uint32_t prefix = 0u, pmask = 0u;
@@ -464,6 +507,7 @@ __device__ void select_row_direct(int64_t n, int64_t k, const float* s, int32_t*
     __syncthreads();
   }
   const uint32_t T = prefix;  // keys > T all taken; `need` keys equal to T taken, lowest indices first
+  if (hint_out && tid == 0) *hint_out = next_hint(T);
   // --- index cut: the need-th key equal to T in index order
   const int64_t chunk = (n + blockDim.x - 1) / blockDim.x;
   const int64_t c0 = int64_t(tid) * chunk, c1 = (c0 + chunk < n) ? c0 + chunk : n;
@@ -511,7 +555,8 @@ __global__ void __launch_bounds__(kFinThreads) topk_final_kernel(int64_t n, int6
                                                                  const int32_t* __restrict__ sure,
                                                                  const uint32_t* __restrict__ cand_key,
                                                                  const int32_t* __restrict__ cand_idx,
-                                                                 int32_t* __restrict__ idx, float* __restrict__ vals) {
+                                                                 int32_t* __restrict__ idx, float* __restrict__ vals,
+                                                                 uint32_t* __restrict__ hint) {
   extern __shared__ int32_t s_dyn[];  // region A (sort buffer or bitmap), then kCandSmem keys and indices
   int32_t* s_sel = s_dyn;
   uint32_t* s_ck = reinterpret_cast<uint32_t*>(s_dyn + kRegionA);
@@ -527,8 +572,9 @@ __global__ void __launch_bounds__(kFinThreads) topk_final_kernel(int64_t n, int6
   float* ov = vals ? vals + int64_t(r) * k : nullptr;
   const int m = st.cand_cnt;
   const int64_t words = (n + 31) >> 5;
+  uint32_t* hint_out = hint ? hint + r : nullptr;
   if (m > cap || (k > kSortMax && words > kBitmapWords)) {
-    select_row_direct(n, k, s, oi, ov, h, s_out);
+    select_row_direct(n, k, s, oi, ov, h, s_out, hint_out);
     return;
   }
   const uint32_t* ck = cand_key + int64_t(r) * cap;
@@ -557,9 +603,41 @@ __global__ void __launch_bounds__(kFinThreads) topk_final_kernel(int64_t n, int6
     ck = s_ck;
     ci = s_ci;
   }
-  int need = int(k) - st.above;  // >= 1
+  uint32_t b1 = st.b1;
+  int above = st.above;  // keys in bins above b1
+  int nsure = st.above;  // of them, listed in `sure` (none for a fast row: its candidates hold them)
+  if (st.fast) {
+    // the scan's filter listed every key at or above the hint, at least k of them: find the
+    // bin of the k-th largest among them from their own 4096-bin histogram
+    uint32_t* h12 = reinterpret_cast<uint32_t*>(s_dyn);  // region A, reused by the bitmap later
+    for (int i = tid; i < kHistBins; i += kFinThreads) h12[i] = 0u;
+    __syncthreads();
+    for (int i = tid; i < m; i += kFinThreads) atomicAdd(&h12[ck[i] >> (32 - kHistBits)], 1u);
+    __syncthreads();
+    h[tid] = h12[4 * tid] + h12[4 * tid + 1] + h12[4 * tid + 2] + h12[4 * tid + 3];
+    __syncthreads();
+    find_digit(h, int(k), true, s_out);
+    __shared__ int s_b1[2];
+    if (tid == 0) {
+      const int grp = s_out[0];
+      int before = s_out[1];
+      int b = 4 * grp + 3;
+      for (; b > 4 * grp; --b) {
+        const int c = int(h12[b]);
+        if (before + c >= int(k)) break;
+        before += c;
+      }
+      s_b1[0] = b;
+      s_b1[1] = before;
+    }
+    __syncthreads();
+    b1 = uint32_t(s_b1[0]);
+    above = s_b1[1];
+    nsure = 0;
+  }
+  int need = int(k) - above;  // >= 1
   // --- digits 2 and 3 (bits 19..10 and 9..0) among the candidates
-  uint32_t prefix = st.b1 << 20, pmask = 0xFFF00000u;
+  uint32_t prefix = b1 << 20, pmask = 0xFFF00000u;
   for (int sh = 10; sh >= 0; sh -= 10) {
     h[tid] = 0u;
     __syncthreads();
@@ -575,6 +653,7 @@ __global__ void __launch_bounds__(kFinThreads) topk_final_kernel(int64_t n, int6
     __syncthreads();
   }
   const uint32_t T = prefix;
+  if (hint_out && tid == 0) *hint_out = next_hint(T);
   // --- among candidates equal to T, the `need` lowest indices: radix select on the index
   int32_t cut = 0x7fffffff;
   {
@@ -639,7 +718,7 @@ __global__ void __launch_bounds__(kFinThreads) topk_final_kernel(int64_t n, int6
     for (int64_t i = tid; i < words4; i += kFinThreads) reinterpret_cast<uint4*>(bm)[i] = make_uint4(0u, 0u, 0u, 0u);
     touch[tid] = 0u;
     __syncthreads();
-    for (int i = tid; i < st.above; i += kFinThreads) {
+    for (int i = tid; i < nsure; i += kFinThreads) {
       const int32_t t = sure[int64_t(r) * k + i];
       if (uint32_t(t) < uint32_t(n)) {
         atomicOr(&bm[t >> 5], 1u << (t & 31));
@@ -691,8 +770,8 @@ __global__ void __launch_bounds__(kFinThreads) topk_final_kernel(int64_t n, int6
   for (int i = tid; i < pow2; i += kFinThreads) s_sel[i] = 0x7fffffff;
   if (tid == 0) s_fill = 0;
   __syncthreads();
-  for (int i = tid; i < st.above; i += kFinThreads) s_sel[i] = sure[int64_t(r) * k + i];
-  if (tid == 0) s_fill = st.above;
+  for (int i = tid; i < nsure; i += kFinThreads) s_sel[i] = sure[int64_t(r) * k + i];
+  if (tid == 0) s_fill = nsure;
   __syncthreads();
   for (int i0 = 0; i0 < m; i0 += kFinThreads) {  // whole warps: one shared atomic per warp
     const int i = i0 + tid;
@@ -720,7 +799,7 @@ size_t topk_ws_bytes(int rows, int64_t n, int64_t k) {
 uint32_t* topk_hist_ptr(void* ws, int rows, int64_t n, int64_t k) { return carve_topk(ws, rows, n, k).hist; }
 
 cudaError_t launch_topk(int rows, int64_t n, int64_t k, const float* scores, int32_t* idx, float* vals, void* ws,
-                        bool hist_ready, cudaStream_t st) {
+                        bool hist_ready, cudaStream_t st, uint32_t* hint) {
   if (k >= n) {
     dim3 grid(unsigned((k + 255) / 256 < 1024 ? (k + 255) / 256 : 1024), unsigned(rows));
     topk_all_kernel<<<grid, 256, 0, st>>>(n, k, scores, idx, vals);
@@ -736,7 +815,7 @@ cudaError_t launch_topk(int rows, int64_t n, int64_t k, const float* scores, int
     topk_hist_kernel<<<pgrid, kPassThreads, 0, st>>>(n, scores, w.hist);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
-  topk_bin_kernel<<<rows, kFinThreads, 0, st>>>(k, w.hist, w.state);
+  topk_bin_kernel<<<rows, kFinThreads, 0, st>>>(k, w.cap, hint, w.hist, w.state);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   {
     const int64_t ctiles = tiles * rows;
@@ -758,8 +837,24 @@ cudaError_t launch_topk(int rows, int64_t n, int64_t k, const float* scores, int
     attr_set = true;
   }
   topk_final_kernel<<<rows, kFinThreads, smem, st>>>(n, k, w.cap, scores, w.state, w.sure, w.cand_key, w.cand_idx,
-                                                     idx, vals);
+                                                     idx, vals, hint);
   return cudaGetLastError();
+}
+
+ScanFilter topk_scan_filter(void* ws, int rows, int64_t n, int64_t k, const uint32_t* hint) {
+  TopkWs w = carve_topk(ws, rows, n, k);
+  ScanFilter f;
+  f.hint = hint;
+  f.cand_key = w.cand_key;
+  f.cand_idx = w.cand_idx;
+  f.cap = w.cap;
+  f.cnt = &w.state[0].cand_cnt;
+  f.cnt_stride = int(sizeof(RowState) / sizeof(int32_t));
+  return f;
+}
+
+size_t topk_state_clear_bytes(int rows) {
+  return size_t(rows) * kHistBins * sizeof(uint32_t) + size_t(rows) * sizeof(RowState);
 }
 
 }  // namespace fathom

@@ -427,3 +427,44 @@ def test_streaming_append_equals_packing_everything(case, gpu_lib):
     ix2 = F.pack(K[:, :n1].contiguous(), S, capacity=cap)
     with pytest.raises(Exception, match="fp16 range"):
         F.pack_append(ix2, bad, n1 + 1)
+
+
+# ------------------------------------------------------- fused scan -> top-k filter ---
+def _score_keys(s):
+    u = s.astype(np.float32).view(np.uint32)
+    k = np.where(u & np.uint32(0x80000000), ~u, u | np.uint32(0x80000000))
+    return np.where(u == np.uint32(0x80000000), np.uint32(0x80000000), k).astype(np.uint32)
+
+
+def _next_hint(T):
+    b = int(T) >> 20
+    return (b - 1) << 20 if b >= 1 else 0
+
+
+def test_fused_filter_gives_the_same_steps(case, gpu_lib):
+    """Steps with the fused filter (hints carried from step to step, queries changing) equal the
+    plain steps bit for bit, whichever route each row takes; the hint left behind follows the rule."""
+    F, w = gpu_lib, case["w"]
+    B, k = w.budgets[len(w.budgets) // 2], min(w.k, w.n)
+    nl = max(1, w.rows // w.kv_heads)
+    qs = [torch.cat([synth.queries(w, l, "cpu", step=s) for l in range(nl)])[: w.rows * w.group].cuda()
+          for s in range(4)]
+    qbuf = qs[0].clone()
+    plain = F.DecodeStep(case["index"], case["Kd"], case["Vd"], qbuf, k, w.group, B)
+    filt = F.DecodeStep(case["index"], case["Kd"], case["Vd"], qbuf, k, w.group, B, hint=True)
+    for s in [0, 0, 1, 1, 2, 3, 0]:
+        qbuf.copy_(qs[s])
+        a = [t.clone() for t in plain()]
+        b = filt()
+        assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1]), s
+        if k < w.n:
+            bits, qbar = F.allocate(qbuf, case["index"].var, B, w.group)
+            keys = _score_keys(F.scan(case["index"], bits, qbar).cpu().numpy())
+            want = [_next_hint(np.sort(keys[r])[::-1][k - 1]) for r in range(w.rows)]
+            assert filt.hint.cpu().numpy().view(np.uint32).tolist() == want
+    # hints that force each route: above every key (too few listed) and 0 (every key listed)
+    for hv in (-1, 0):
+        filt.hint.fill_(hv)
+        a = [t.clone() for t in plain()]
+        b = filt()
+        assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1]), hv
