@@ -95,18 +95,31 @@ int index_geom(const fathom_index_desc* d, IndexGeom* g);
 size_t topk_ws_bytes(int rows, int64_t n, int64_t k);
 size_t attn_ws_bytes(int rows, int group, int64_t k);
 
-// The scan's fused top-k filter: every key at or above the row's hint is appended
-// (key, index) to the row's candidate list and counted; the top-k then skips its
-// candidate pass for rows whose filter kept at least k and at most cap keys.
-struct ScanFilter {
-  const uint32_t* hint;  // [rows] key threshold per row
+// Per-row state of the top-k radix select (topk.cu), also finished by the scan
+// inside the decode step.
+struct TopkRowState {
+  uint32_t b1;       // bin (top 12 key bits) holding the k-th largest key
+  int32_t above;     // keys in bins above b1
+  int32_t sure_cnt;  // keys listed as sure winners (bins above b1)
+  int32_t cand_cnt;  // candidates listed (with the scan's filter: keys at or above the row's hint)
+  int32_t fast;      // 1: the filter's candidates hold the top k, the candidate pass is skipped
+  int32_t spill;     // the filter's staging overflowed in some CTA: the row's list is incomplete
+  int32_t pad[2];
+};
+
+// The scan's fused top-k filter (decode step): with a hint, every key at or
+// above it is listed (key, index) as a candidate of its row and counted in the
+// row state (zeroed before the scan); the top-k then marks a row whose list
+// holds at least k and at most cap keys fast.
+struct ScanTopk {
+  TopkRowState* state;   // [rows]
+  int64_t k;
+  const uint32_t* hint;  // [rows] key thresholds, or nullptr (no filter)
   uint32_t* cand_key;    // [rows][cap]
   int32_t* cand_idx;     // [rows][cap]
   int64_t cap;
-  int32_t* cnt;          // row r's counter at cnt[r * cnt_stride] (zeroed before the scan)
-  int cnt_stride;
 };
-ScanFilter topk_scan_filter(void* ws, int rows, int64_t n, int64_t k, const uint32_t* hint);
+ScanTopk topk_scan_side(void* ws, int rows, int64_t n, int64_t k, const uint32_t* hint);
 // bytes from the top-k histogram to the end of the row states (one memset clears both)
 size_t topk_state_clear_bytes(int rows);
 
@@ -123,8 +136,9 @@ cudaError_t launch_allocate_sparq(int rows, int group, const void* q, int q_dtyp
                                   float* qbar, int32_t* status, cudaStream_t st);
 cudaError_t launch_scan(const IndexGeom& g, const uint32_t* planes, const __half2* meta, const uint8_t* bits,
                         const float* qbar, float* scores, uint32_t* hist, cudaStream_t st,
-                        const ScanFilter* filter = nullptr);
-// hint: the fused filter's per-row hints (read, and rewritten for the next step), or NULL
+                        const ScanTopk* topk = nullptr);
+// hist_ready: the histogram is built; hint: the fused filter's per-row hints (read, and
+// rewritten for the next step), or NULL
 cudaError_t launch_topk(int rows, int64_t n, int64_t k, const float* scores, int32_t* idx, float* vals, void* ws,
                         bool hist_ready, cudaStream_t st, uint32_t* hint = nullptr);
 // per_head: idx holds one winner set per query head ([rows*group][k]), each head attends over its own

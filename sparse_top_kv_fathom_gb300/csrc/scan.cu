@@ -42,6 +42,7 @@ using namespace bitplane;
 
 constexpr int kScanTile = 8192;  // tokens per CTA
 constexpr int kStages = 4;
+constexpr int kFStage = 512;     // filter candidates a CTA stages in shared memory
 
 // TOK tokens per thread = TOK/32 words of every plane
 template <int TOK>
@@ -97,7 +98,7 @@ __global__ void __launch_bounds__(ScanCfg<TOK>::kThreads, 4) scan_kernel(const u
                                                                          float* __restrict__ scores,
                                                                          uint32_t* __restrict__ hist, int64_t n,
                                                                          int64_t nsb, int log2S, int64_t nblk,
-                                                                         const ScanFilter flt) {
+                                                                         const ScanTopk tk) {
   constexpr int T = ScanCfg<TOK>::kThreads;
   constexpr int W = ScanCfg<TOK>::kWords;
   using PW = PlaneWords<W>;
@@ -109,6 +110,8 @@ __global__ void __launch_bounds__(ScanCfg<TOK>::kThreads, 4) scan_kernel(const u
   __shared__ __half2 s_m[kStages][T];
   __shared__ uint32_t s_hist[kHist ? kHistBins : 1];
   __shared__ int s_fcnt, s_fbase;  // the CTA's filter candidates, and their first slot in the row's list
+  __shared__ uint32_t s_fk[kFilter ? kFStage : 1];  // the CTA's filter candidates (key, index)
+  __shared__ int32_t s_fi[kFilter ? kFStage : 1];
 
   const int r = blockIdx.y;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -242,61 +245,26 @@ __global__ void __launch_bounds__(ScanCfg<TOK>::kThreads, 4) scan_kernel(const u
       }
     }
     if constexpr (kHist) {
+      const uint32_t tau = kFilter ? __ldg(tk.hint + r) : 0u;
+      auto count = [&](float v, int64_t t) {
+        const uint32_t key = score_key(v);
+        atomicAdd(&s_hist[key >> (32 - kHistBits)], 1u);
+        if constexpr (kFilter) {
+          if (key >= tau) {  // rare: a filter candidate
+            const int sl = atomicAdd(&s_fcnt, 1);
+            if (sl < kFStage) {
+              s_fk[sl] = key;
+              s_fi[sl] = int32_t(t);
+            }
+          }
+        }
+      };
 #pragma unroll
       for (int w = 0; w < W; ++w) {
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          if (t0 + 32 * w + i < n) atomicAdd(&s_hist[score_key(acc[16 * w + i].x) >> (32 - kHistBits)], 1u);
-          if (t0 + 32 * w + 16 + i < n)
-            atomicAdd(&s_hist[score_key(acc[16 * w + i].y) >> (32 - kHistBits)], 1u);
-        }
-      }
-    }
-  }
-  if constexpr (kFilter) {
-    // fused top-k filter: append (key, index) of every key at or above the row's hint
-    const uint32_t tau = __ldg(flt.hint + r);
-    uint32_t mk[W];  // bit b of mk[w]: token t0 + 32w + b is at or above the hint
-    int cnt = 0;
-#pragma unroll
-    for (int w = 0; w < W; ++w) {
-      mk[w] = 0u;
-#pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        mk[w] |= uint32_t(valid && t0 + 32 * w + i < n && score_key(acc[16 * w + i].x) >= tau) << i;
-        mk[w] |= uint32_t(valid && t0 + 32 * w + 16 + i < n && score_key(acc[16 * w + i].y) >= tau) << (16 + i);
-      }
-      cnt += __popc(mk[w]);
-    }
-    int x = cnt;  // inclusive warp scan of the counts
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, x, o);
-      if (lane >= o) x += y;
-    }
-    // slots: warp offset inside the CTA (shared counter), then one global reservation per CTA
-    int wbase = 0;
-    if (lane == 31 && x) wbase = atomicAdd(&s_fcnt, x);
-    wbase = __shfl_sync(0xffffffffu, wbase, 31);
-    __syncthreads();
-    if (tid == 0) s_fbase = s_fcnt ? atomicAdd(flt.cnt + int64_t(r) * flt.cnt_stride, s_fcnt) : 0;
-    __syncthreads();
-    const int base = s_fbase + wbase;
-    if (cnt && base < flt.cap) {  // once the row's list is full the row falls back: stop writing
-      int64_t slot = int64_t(base) + x - cnt;
-      uint32_t* ck = flt.cand_key + int64_t(r) * flt.cap;
-      int32_t* ci = flt.cand_idx + int64_t(r) * flt.cap;
-#pragma unroll
-      for (int w = 0; w < W; ++w) {
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          if (!((mk[w] >> i) & 1u)) continue;
-          const float v = i < 16 ? acc[16 * w + i].x : acc[16 * w + i - 16].y;
-          if (slot < flt.cap) {
-            ck[slot] = score_key(v);
-            ci[slot] = int32_t(t0 + 32 * w + i);
-          }
-          ++slot;
+          if (t0 + 32 * w + i < n) count(acc[16 * w + i].x, t0 + 32 * w + i);
+          if (t0 + 32 * w + 16 + i < n) count(acc[16 * w + i].y, t0 + 32 * w + 16 + i);
         }
       }
     }
@@ -308,19 +276,39 @@ __global__ void __launch_bounds__(ScanCfg<TOK>::kThreads, 4) scan_kernel(const u
       const uint32_t v = s_hist[i];
       if (v) atomicAdd(gh + i, v);
     }
+    if constexpr (kFilter) {
+      TopkRowState* srow = tk.state + r;
+      // the CTA's candidates: one reservation in the row's list, then a coalesced copy; a CTA
+      // whose stage overflowed marks the row's list incomplete (the row falls back)
+      if (tid == 0) {
+        const int nc = s_fcnt;
+        if (nc > kFStage) atomicOr(&srow->spill, 1);
+        s_fbase = nc ? atomicAdd(&srow->cand_cnt, nc) : 0;
+      }
+      __syncthreads();
+      const int nc = s_fcnt < kFStage ? s_fcnt : kFStage;
+      for (int i = tid; i < nc; i += T) {
+        const int64_t slot = int64_t(s_fbase) + i;
+        if (slot < tk.cap) {
+          tk.cand_key[int64_t(r) * tk.cap + slot] = s_fk[i];
+          tk.cand_idx[int64_t(r) * tk.cap + slot] = s_fi[i];
+        }
+      }
+    }
   }
 }
 
 template <int TOK>
 cudaError_t launch_scan_t(const IndexGeom& g, const uint32_t* planes, const __half2* meta, const uint8_t* bits,
-                          const float* qbar, float* scores, uint32_t* hist, cudaStream_t st, const ScanFilter* f) {
+                          const float* qbar, float* scores, uint32_t* hist, cudaStream_t st, const ScanTopk* tk) {
   const int64_t tiles = (g.n + kScanTile - 1) / kScanTile;
   const dim3 grid{unsigned(tiles), unsigned(g.rows), 1u};
   constexpr int T = ScanCfg<TOK>::kThreads;
-  const ScanFilter none{};
-  if (hist && f)
+  const ScanTopk none{};
+  if (hist && tk && tk->hint && !tk->state) return cudaErrorInvalidValue;
+  if (hist && tk && tk->hint)
     scan_kernel<TOK, true, true><<<grid, T, 0, st>>>(planes, meta, bits, qbar, scores, hist, g.n, g.nsb, g.log2S,
-                                                     g.nblk, *f);
+                                                     g.nblk, *tk);
   else if (hist)
     scan_kernel<TOK, true, false><<<grid, T, 0, st>>>(planes, meta, bits, qbar, scores, hist, g.n, g.nsb, g.log2S,
                                                       g.nblk, none);
@@ -333,11 +321,11 @@ cudaError_t launch_scan_t(const IndexGeom& g, const uint32_t* planes, const __ha
 }  // namespace
 
 cudaError_t launch_scan(const IndexGeom& g, const uint32_t* planes, const __half2* meta, const uint8_t* bits,
-                        const float* qbar, float* scores, uint32_t* hist, cudaStream_t st, const ScanFilter* f) {
+                        const float* qbar, float* scores, uint32_t* hist, cudaStream_t st, const ScanTopk* tk) {
   // two plane words per thread need 8-byte aligned planes (every run of S >= 128 tokens is)
   if ((reinterpret_cast<uintptr_t>(planes) & 7) == 0)
-    return launch_scan_t<64>(g, planes, meta, bits, qbar, scores, hist, st, f);
-  return launch_scan_t<32>(g, planes, meta, bits, qbar, scores, hist, st, f);
+    return launch_scan_t<64>(g, planes, meta, bits, qbar, scores, hist, st, tk);
+  return launch_scan_t<32>(g, planes, meta, bits, qbar, scores, hist, st, tk);
 }
 
 }  // namespace fathom

@@ -126,11 +126,11 @@ int fathom_decode_step(const fathom_step_desc* s, void* workspace, size_t ws_byt
   const void* dH = nullptr;
   FATHOM_TRY(device_view(s->hint, "hint", &dH, true));
   uint32_t* hint = use_hist ? (uint32_t*)dH : nullptr;  // the fused filter (k < n only)
-  // the histogram, and with the filter also the row states whose candidate counters the scan bumps
+  // the histogram, and with the filter the row states whose candidate counters the scan bumps
   if (hist)
     FATHOM_TRY_CUDA(cudaMemsetAsync(hist, 0, hint ? topk_state_clear_bytes(g.rows)
                                                     : size_t(g.rows) * kHistBins * sizeof(uint32_t), st));
-  const ScanFilter flt = hint ? topk_scan_filter(w.topk, g.rows, g.n, s->k, hint) : ScanFilter{};
+  const ScanTopk tk = topk_scan_side(w.topk, g.rows, g.n, s->k, hint);
   if (s->sparq_r > 0)
     FATHOM_TRY_CUDA(launch_allocate_sparq(g.rows, s->group, dq, s->q_dtype, s->sparq_r, w.bits, w.qbar,
                                           (int32_t*)dSt, st));
@@ -138,7 +138,7 @@ int fathom_decode_step(const fathom_step_desc* s, void* workspace, size_t ws_byt
     FATHOM_TRY_CUDA(launch_allocate(g.rows, s->group, dq, s->q_dtype, (const float*)dVar, (const uint16_t*)dBud,
                                     s->budget, w.bits, w.qbar, (int32_t*)dSt, st));
   FATHOM_TRY_CUDA(launch_scan(g, (const uint32_t*)dP, (const __half2*)dM, w.bits, w.qbar, w.scores, hist, st,
-                              hint ? &flt : nullptr));
+                              hint ? &tk : nullptr));
   FATHOM_TRY_CUDA(launch_topk(g.rows, g.n, s->k, w.scores, (int32_t*)dI, nullptr, w.topk, use_hist, st, hint));
   if (q4)
     FATHOM_TRY_CUDA(launch_attn_q4(g, s->group, s->k, dq, s->q_dtype, (const uint32_t*)dP, (const __half2*)dM, dV,

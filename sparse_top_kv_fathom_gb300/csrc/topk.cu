@@ -33,14 +33,7 @@ constexpr int kPassThreads = 256;
 constexpr int kPassItems = 16;  // items per thread in the histogram / compaction passes
 constexpr int kCompactCtasPerSm = 3;  // resident CTAs per SM of the candidate pass
 
-struct RowState {
-  uint32_t b1;      // bin (top 12 key bits) holding the k-th largest key
-  int32_t above;    // keys in bins above b1
-  int32_t sure_cnt;
-  int32_t cand_cnt; // candidates listed (with the scan's filter: keys at or above the row's hint)
-  int32_t fast;     // 1: the filter's candidates hold the top k, the candidate pass is skipped
-  int32_t pad[3];
-};
+using RowState = TopkRowState;
 static_assert(sizeof(RowState) == 32, "RowState layout");
 
 struct TopkWs {
@@ -173,18 +166,9 @@ __global__ void __launch_bounds__(kFinThreads) topk_bin_kernel(int64_t k, int64_
   __shared__ uint32_t h[kFinThreads];
   __shared__ int s_out[2];
   const int r = blockIdx.x;
-  if (hint) {
-    const int32_t cnt = state[r].cand_cnt;  // keys at or above the hint, counted by the scan
-    if (cnt >= k && cnt <= cap) {           // uniform across the CTA
-      __syncthreads();                      // every thread has read cand_cnt
-      if (threadIdx.x == 0) {
-        state[r].fast = 1;
-        state[r].above = 0;
-        state[r].sure_cnt = 0;
-      }
-      return;
-    }
-  }
+  // keys at or above the hint, counted by the scan (read before thread 0 rewrites the state)
+  const int32_t cnt = hint ? state[r].cand_cnt : 0;
+  const bool fast = hint && cnt >= k && cnt <= cap && !state[r].spill;
   // fold the 4096 bins into 1024 groups of 4 (from the top), then refine inside the group
   const uint32_t* hr = hist + int64_t(r) * kHistBins;
   const int g = threadIdx.x;
@@ -204,9 +188,10 @@ __global__ void __launch_bounds__(kFinThreads) topk_bin_kernel(int64_t k, int64_
     st.b1 = uint32_t(b);
     st.above = before;
     st.sure_cnt = 0;
-    st.cand_cnt = 0;
-    st.fast = 0;
-    st.pad[0] = st.pad[1] = st.pad[2] = 0;
+    st.cand_cnt = fast ? cnt : 0;
+    st.fast = fast;
+    st.spill = 0;
+    st.pad[0] = st.pad[1] = 0;
     state[r] = st;
   }
 }
@@ -606,35 +591,7 @@ __global__ void __launch_bounds__(kFinThreads) topk_final_kernel(int64_t n, int6
   uint32_t b1 = st.b1;
   int above = st.above;  // keys in bins above b1
   int nsure = st.above;  // of them, listed in `sure` (none for a fast row: its candidates hold them)
-  if (st.fast) {
-    // the scan's filter listed every key at or above the hint, at least k of them: find the
-    // bin of the k-th largest among them from their own 4096-bin histogram
-    uint32_t* h12 = reinterpret_cast<uint32_t*>(s_dyn);  // region A, reused by the bitmap later
-    for (int i = tid; i < kHistBins; i += kFinThreads) h12[i] = 0u;
-    __syncthreads();
-    for (int i = tid; i < m; i += kFinThreads) atomicAdd(&h12[ck[i] >> (32 - kHistBits)], 1u);
-    __syncthreads();
-    h[tid] = h12[4 * tid] + h12[4 * tid + 1] + h12[4 * tid + 2] + h12[4 * tid + 3];
-    __syncthreads();
-    find_digit(h, int(k), true, s_out);
-    __shared__ int s_b1[2];
-    if (tid == 0) {
-      const int grp = s_out[0];
-      int before = s_out[1];
-      int b = 4 * grp + 3;
-      for (; b > 4 * grp; --b) {
-        const int c = int(h12[b]);
-        if (before + c >= int(k)) break;
-        before += c;
-      }
-      s_b1[0] = b;
-      s_b1[1] = before;
-    }
-    __syncthreads();
-    b1 = uint32_t(s_b1[0]);
-    above = s_b1[1];
-    nsure = 0;
-  }
+  if (st.fast) nsure = 0;  // the filter's list holds the keys of the bins above b1 too
   int need = int(k) - above;  // >= 1
   // --- digits 2 and 3 (bits 19..10 and 9..0) among the candidates
   uint32_t prefix = b1 << 20, pmask = 0xFFF00000u;
@@ -841,16 +798,16 @@ cudaError_t launch_topk(int rows, int64_t n, int64_t k, const float* scores, int
   return cudaGetLastError();
 }
 
-ScanFilter topk_scan_filter(void* ws, int rows, int64_t n, int64_t k, const uint32_t* hint) {
+ScanTopk topk_scan_side(void* ws, int rows, int64_t n, int64_t k, const uint32_t* hint) {
   TopkWs w = carve_topk(ws, rows, n, k);
-  ScanFilter f;
-  f.hint = hint;
-  f.cand_key = w.cand_key;
-  f.cand_idx = w.cand_idx;
-  f.cap = w.cap;
-  f.cnt = &w.state[0].cand_cnt;
-  f.cnt_stride = int(sizeof(RowState) / sizeof(int32_t));
-  return f;
+  ScanTopk t;
+  t.state = w.state;
+  t.k = k;
+  t.hint = hint;
+  t.cand_key = w.cand_key;
+  t.cand_idx = w.cand_idx;
+  t.cap = w.cap;
+  return t;
 }
 
 size_t topk_state_clear_bytes(int rows) {
