@@ -48,7 +48,6 @@ constexpr int kFStage = 512;     // filter candidates a CTA stages in shared mem
 template <int TOK>
 struct ScanCfg {
   static constexpr int kWords = TOK / 32;
-  static constexpr int kThreads = kScanTile / TOK;
 };
 template <int W>
 struct PlaneWords;
@@ -90,8 +89,9 @@ __device__ __forceinline__ void channel_terms(float2* acc, uint32_t w0, uint32_t
   }
 }
 
-template <int TOK, bool kHist, bool kFilter>
-__global__ void __launch_bounds__(ScanCfg<TOK>::kThreads, 4) scan_kernel(const uint32_t* __restrict__ planes,
+// TOK tokens per thread, T threads per CTA (T * TOK tokens per CTA); 512 threads per SM resident.
+template <int TOK, int T, bool kHist, bool kFilter>
+__global__ void __launch_bounds__(T, 512 / T) scan_kernel(const uint32_t* __restrict__ planes,
                                                                          const __half2* __restrict__ meta,
                                                                          const uint8_t* __restrict__ bits,
                                                                          const float* __restrict__ qbar,
@@ -99,8 +99,8 @@ __global__ void __launch_bounds__(ScanCfg<TOK>::kThreads, 4) scan_kernel(const u
                                                                          uint32_t* __restrict__ hist, int64_t n,
                                                                          int64_t nsb, int log2S, int64_t nblk,
                                                                          const ScanTopk tk) {
-  constexpr int T = ScanCfg<TOK>::kThreads;
   constexpr int W = ScanCfg<TOK>::kWords;
+  static_assert(T % 32 == 0 && T >= 32 && T <= 512, "whole warps");
   using PW = PlaneWords<W>;
   __shared__ int s_ch[kD];
   __shared__ int s_dep[kD];
@@ -116,15 +116,14 @@ __global__ void __launch_bounds__(ScanCfg<TOK>::kThreads, 4) scan_kernel(const u
   const int r = blockIdx.y;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
-  // Active channels of this row, in channel order (warps 0..3, whole warps, cover the 128 channels).
-  int dep = 0;
-  float qv = 0.0f;
-  unsigned ball = 0u;
-  if (tid < kD) {
-    dep = min(int(bits[int64_t(r) * kD + tid]), kPlanes);
-    qv = qbar[int64_t(r) * kD + tid];
-    ball = __ballot_sync(0xffffffffu, dep > 0);
-    if (lane == 0) s_wcnt[warp] = __popc(ball);
+  // Active channels of this row, in channel order: warp w handles channel groups w, w + T/32, ...
+  // of 32 channels (one group each when T = 128).
+  constexpr int kGroups = kD / 32;
+  constexpr int kWarpsT = T / 32;
+  for (int cg = warp; cg < kGroups; cg += kWarpsT) {
+    const int dep = min(int(bits[int64_t(r) * kD + cg * 32 + lane]), kPlanes);
+    const unsigned ball = __ballot_sync(0xffffffffu, dep > 0);
+    if (lane == 0) s_wcnt[cg] = __popc(ball);
   }
   if constexpr (kHist) {
     for (int i = tid; i < kHistBins; i += T) s_hist[i] = 0u;
@@ -133,14 +132,19 @@ __global__ void __launch_bounds__(ScanCfg<TOK>::kThreads, 4) scan_kernel(const u
   __syncthreads();
   int nact = 0;
 #pragma unroll
-  for (int w = 0; w < kD / 32; ++w) nact += s_wcnt[w];
-  if (tid < kD && dep > 0) {
-    int off = 0;
-    for (int w = 0; w < warp; ++w) off += s_wcnt[w];
-    const int pos = off + __popc(ball & ((1u << lane) - 1u));
-    s_ch[pos] = tid;
-    s_dep[pos] = dep;
-    s_q[pos] = qv;
+  for (int w = 0; w < kGroups; ++w) nact += s_wcnt[w];
+  for (int cg = warp; cg < kGroups; cg += kWarpsT) {
+    const int c = cg * 32 + lane;
+    const int dep = min(int(bits[int64_t(r) * kD + c]), kPlanes);
+    const unsigned ball = __ballot_sync(0xffffffffu, dep > 0);
+    if (dep > 0) {
+      int off = 0;
+      for (int w = 0; w < cg; ++w) off += s_wcnt[w];
+      const int pos = off + __popc(ball & ((1u << lane) - 1u));
+      s_ch[pos] = c;
+      s_dep[pos] = dep;
+      s_q[pos] = qbar[int64_t(r) * kD + c];
+    }
   }
   __syncthreads();
 
@@ -298,23 +302,23 @@ __global__ void __launch_bounds__(ScanCfg<TOK>::kThreads, 4) scan_kernel(const u
   }
 }
 
-template <int TOK>
+template <int TOK, int T>
 cudaError_t launch_scan_t(const IndexGeom& g, const uint32_t* planes, const __half2* meta, const uint8_t* bits,
                           const float* qbar, float* scores, uint32_t* hist, cudaStream_t st, const ScanTopk* tk) {
-  const int64_t tiles = (g.n + kScanTile - 1) / kScanTile;
+  constexpr int64_t kTileT = int64_t(T) * TOK;
+  const int64_t tiles = (g.n + kTileT - 1) / kTileT;
   const dim3 grid{unsigned(tiles), unsigned(g.rows), 1u};
-  constexpr int T = ScanCfg<TOK>::kThreads;
   const ScanTopk none{};
   if (hist && tk && tk->hint && !tk->state) return cudaErrorInvalidValue;
   if (hist && tk && tk->hint)
-    scan_kernel<TOK, true, true><<<grid, T, 0, st>>>(planes, meta, bits, qbar, scores, hist, g.n, g.nsb, g.log2S,
-                                                     g.nblk, *tk);
+    scan_kernel<TOK, T, true, true><<<grid, T, 0, st>>>(planes, meta, bits, qbar, scores, hist, g.n, g.nsb, g.log2S,
+                                                        g.nblk, *tk);
   else if (hist)
-    scan_kernel<TOK, true, false><<<grid, T, 0, st>>>(planes, meta, bits, qbar, scores, hist, g.n, g.nsb, g.log2S,
-                                                      g.nblk, none);
+    scan_kernel<TOK, T, true, false><<<grid, T, 0, st>>>(planes, meta, bits, qbar, scores, hist, g.n, g.nsb,
+                                                         g.log2S, g.nblk, none);
   else
-    scan_kernel<TOK, false, false><<<grid, T, 0, st>>>(planes, meta, bits, qbar, scores, nullptr, g.n, g.nsb,
-                                                       g.log2S, g.nblk, none);
+    scan_kernel<TOK, T, false, false><<<grid, T, 0, st>>>(planes, meta, bits, qbar, scores, nullptr, g.n, g.nsb,
+                                                          g.log2S, g.nblk, none);
   return cudaGetLastError();
 }
 
@@ -322,10 +326,21 @@ cudaError_t launch_scan_t(const IndexGeom& g, const uint32_t* planes, const __ha
 
 cudaError_t launch_scan(const IndexGeom& g, const uint32_t* planes, const __half2* meta, const uint8_t* bits,
                         const float* qbar, float* scores, uint32_t* hist, cudaStream_t st, const ScanTopk* tk) {
+  // Tokens per CTA: 8192, halved (down to 1024) while the rows give fewer than two CTAs per SM --
+  // every CTA walks its row's active channels one after the other, so short rows need more CTAs.
+  const int64_t want = 2 * int64_t(num_sms());
+  int64_t tile = kScanTile;
+  while (tile > 1024 && ((g.n + tile - 1) / tile) * g.rows < want) tile >>= 1;
   // two plane words per thread need 8-byte aligned planes (every run of S >= 128 tokens is)
-  if ((reinterpret_cast<uintptr_t>(planes) & 7) == 0)
-    return launch_scan_t<64>(g, planes, meta, bits, qbar, scores, hist, st, tk);
-  return launch_scan_t<32>(g, planes, meta, bits, qbar, scores, hist, st, tk);
+  if ((reinterpret_cast<uintptr_t>(planes) & 7) == 0 && tile >= 2048) {
+    if (tile == 8192) return launch_scan_t<64, 128>(g, planes, meta, bits, qbar, scores, hist, st, tk);
+    if (tile == 4096) return launch_scan_t<64, 64>(g, planes, meta, bits, qbar, scores, hist, st, tk);
+    return launch_scan_t<64, 32>(g, planes, meta, bits, qbar, scores, hist, st, tk);
+  }
+  if (tile == 8192) return launch_scan_t<32, 256>(g, planes, meta, bits, qbar, scores, hist, st, tk);
+  if (tile == 4096) return launch_scan_t<32, 128>(g, planes, meta, bits, qbar, scores, hist, st, tk);
+  if (tile == 2048) return launch_scan_t<32, 64>(g, planes, meta, bits, qbar, scores, hist, st, tk);
+  return launch_scan_t<32, 32>(g, planes, meta, bits, qbar, scores, hist, st, tk);
 }
 
 }  // namespace fathom

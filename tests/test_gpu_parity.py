@@ -468,3 +468,45 @@ def test_fused_filter_gives_the_same_steps(case, gpu_lib):
         a = [t.clone() for t in plain()]
         b = filt()
         assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1]), hv
+
+
+def _tile_case_n(t, rows):
+    """A row length for which the scan's launch takes t tokens per CTA: the tile halves from
+    8192 while the rows give fewer than two CTAs per SM, so 2 * SMs * t tokens over all rows
+    (plus a ragged tail) stop it exactly at t."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    return 2 * sms * t // rows + 77
+
+
+@pytest.mark.parametrize("aligned", [True, False], ids=["planes8B", "planes4B"])
+@pytest.mark.parametrize("tile", [8192, 4096, 2048, 1024])
+def test_scan_every_tile_shape(gpu_lib, tile, aligned):
+    """Every CTA shape of the scan (tokens per thread x threads per CTA, chosen from the row
+    length and the planes' alignment): scores against the oracle on a sampled row, the step's
+    winners against the exact top-k of those scores, the fused filter equal to the plain step."""
+    F = gpu_lib
+    w0 = synth.WORKLOADS["decode36"]
+    w = synth.scaled(w0, n=_tile_case_n(tile, w0.kv_heads), layers=1)
+    S, B, k, G = 4096, 92, 2048, w.group
+    K, V, q = gen(w, device="cuda")
+    ix = F.pack(K, S)
+    if aligned:
+        sx = ix
+    else:  # planes 4-byte but not 8-byte aligned: one word per plane per thread
+        buf = torch.empty(ix.planes.numel() + 1, dtype=torch.int32, device="cuda")
+        buf[1:].copy_(ix.planes.flatten())
+        sx = F.BitPlaneIndex(buf[1:].view(ix.planes.shape), ix.meta, ix.var, ix.n, ix.rows, S)
+        assert sx.planes.data_ptr() % 8 == 4
+    bits, qbar = F.allocate(q, ix.var, B, G)
+    s = F.scan(sx, bits, qbar)
+    r = 5
+    planes, meta, var = oracle.pack(f32(K[r:r + 1]), S)
+    ref, l1 = oracle.scan(planes, meta, bits[r:r + 1].cpu().numpy(), qbar[r:r + 1].cpu().numpy(), w.n, S)
+    check_scores(s[r:r + 1].cpu().numpy(), ref, l1)
+    plain = F.DecodeStep(sx, K, V, q, k, G, B)
+    idx, out, _ = [t.clone() for t in plain()]
+    assert np.array_equal(idx.cpu().numpy(), oracle.topk_f32(s.cpu().numpy(), k))
+    filt = F.DecodeStep(sx, K, V, q, k, G, B, hint=True)
+    for _ in range(3):  # first step: every key listed; then the carried hints
+        b = filt()
+        assert torch.equal(idx, b[0]) and torch.equal(out, b[1])
