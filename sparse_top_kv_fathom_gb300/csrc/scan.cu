@@ -89,8 +89,11 @@ __device__ __forceinline__ void channel_terms(float2* acc, uint32_t w0, uint32_t
   }
 }
 
-// TOK tokens per thread, T threads per CTA (T * TOK tokens per CTA); 512 threads per SM resident.
-template <int TOK, int T, bool kHist, bool kFilter>
+// TOK tokens per thread; T threads per CTA in P channel groups of T/P threads: group p sums
+// channels p, p + P, p + 2P, ... of the row's active channels over the CTA's (T/P) * TOK tokens,
+// and the groups' partial sums are added pairwise at the end (P > 1 gives short rows more
+// independent load streams).  512 threads per SM resident.
+template <int TOK, int T, int P, bool kHist, bool kFilter>
 __global__ void __launch_bounds__(T, 512 / T) scan_kernel(const uint32_t* __restrict__ planes,
                                                                          const __half2* __restrict__ meta,
                                                                          const uint8_t* __restrict__ bits,
@@ -100,7 +103,9 @@ __global__ void __launch_bounds__(T, 512 / T) scan_kernel(const uint32_t* __rest
                                                                          int64_t nsb, int log2S, int64_t nblk,
                                                                          const ScanTopk tk) {
   constexpr int W = ScanCfg<TOK>::kWords;
+  constexpr int TT = T / P;  // threads of one channel group = token slots of the CTA
   static_assert(T % 32 == 0 && T >= 32 && T <= 512, "whole warps");
+  static_assert((P & (P - 1)) == 0 && TT % 32 == 0, "channel groups of whole warps");
   using PW = PlaneWords<W>;
   __shared__ int s_ch[kD];
   __shared__ int s_dep[kD];
@@ -148,7 +153,9 @@ __global__ void __launch_bounds__(T, 512 / T) scan_kernel(const uint32_t* __rest
   }
   __syncthreads();
 
-  const int64_t t0 = (int64_t(blockIdx.x) * T + tid) * TOK;
+  const int sp = tid / TT, slot = tid % TT;  // channel group, token slot
+  const int nmine = nact > sp ? (nact - sp + P - 1) / P : 0;
+  const int64_t t0 = (int64_t(blockIdx.x) * TT + slot) * TOK;
   const bool valid = t0 < n;
   const int64_t S = int64_t(1) << log2S;
   const int64_t run = S >> 5;
@@ -156,10 +163,10 @@ __global__ void __launch_bounds__(T, 512 / T) scan_kernel(const uint32_t* __rest
   const uint32_t* pb = planes + (int64_t(r) * nsb + (tt >> log2S)) * (kD * kPlanes) * run + ((tt & (S - 1)) >> 5);
   const __half2* mb = meta + int64_t(r) * kD * nblk + (tt >> 7);
 
-  auto issue = [&](int a) {
-    if (a < nact && valid) {
+  auto issue = [&](int a) {  // this thread's a-th channel: sp + a * P
+    if (a < nmine && valid) {
       const int st = a % kStages;
-      const int c = s_ch[a], d = s_dep[a];
+      const int c = s_ch[sp + a * P], d = s_dep[sp + a * P];
       const uint32_t* p = pb + int64_t(c) * kPlanes * run;
       cp_async<4 * W>(&s_w[st][0][tid], p);
       if (d > 1) cp_async<4 * W>(&s_w[st][1][tid], p + run);
@@ -177,13 +184,13 @@ __global__ void __launch_bounds__(T, 512 / T) scan_kernel(const uint32_t* __rest
 
 #pragma unroll
   for (int a = 0; a < kStages - 1; ++a) issue(a);
-  for (int a = 0; a < nact; ++a) {
+  for (int a = 0; a < nmine; ++a) {
     issue(a + kStages - 1);
     cp_async_wait<kStages - 1>();  // this thread's copies for channel a have landed
     if (!valid) continue;
     const int st = a % kStages;
-    const int d = s_dep[a];
-    const float q = s_q[a];
+    const int d = s_dep[sp + a * P];
+    const float q = s_q[sp + a * P];
     const __half2 mh = s_m[st][tid];
     const float lo = __low2float(mh), dl = __high2float(mh);
     const float2 d16 = make_float2(16.0f * dl, 16.0f * dl);
@@ -193,7 +200,7 @@ __global__ void __launch_bounds__(T, 512 / T) scan_kernel(const uint32_t* __rest
     const float2 lop = make_float2(lo1, lo1);
     const float2 q2 = make_float2(q, q);
     const typename PW::T v0 = s_w[st][0][tid];
-    switch (d) {  // uniform across the CTA
+    switch (d) {  // uniform across the warp
       case 1:
 #pragma unroll
         for (int w = 0; w < W; ++w)
@@ -225,7 +232,35 @@ __global__ void __launch_bounds__(T, 512 / T) scan_kernel(const uint32_t* __rest
   }
   cp_async_wait<0>();
 
-  if (valid) {
+  if constexpr (P > 1) {
+    // groups [h, 2h) hand their sums to groups [0, h) through the copy ring, h = P/2, ..., 1
+    static_assert(sizeof(s_w) >= sizeof(float) * (P / 2) * TOK * TT, "ring holds half the groups' sums");
+    float* red = reinterpret_cast<float*>(&s_w[0][0][0]);
+    __syncthreads();  // every thread's last reads of the ring are done
+#pragma unroll
+    for (int h = P / 2; h >= 1; h >>= 1) {
+      if (sp >= h && sp < 2 * h) {
+        float* rw = red + int64_t(sp - h) * TOK * TT + slot;
+#pragma unroll
+        for (int i = 0; i < TOK / 2; ++i) {
+          rw[(2 * i) * TT] = acc[i].x;
+          rw[(2 * i + 1) * TT] = acc[i].y;
+        }
+      }
+      __syncthreads();
+      if (sp < h) {
+        const float* rr = red + int64_t(sp) * TOK * TT + slot;
+#pragma unroll
+        for (int i = 0; i < TOK / 2; ++i) {
+          acc[i].x += rr[(2 * i) * TT];
+          acc[i].y += rr[(2 * i + 1) * TT];
+        }
+      }
+      if (h > 1) __syncthreads();
+    }
+  }
+
+  if (valid && sp == 0) {
     float* out = scores + int64_t(r) * n + t0;
     if (t0 + TOK <= n && (reinterpret_cast<uintptr_t>(out) & 15) == 0) {
 #pragma unroll
@@ -302,23 +337,23 @@ __global__ void __launch_bounds__(T, 512 / T) scan_kernel(const uint32_t* __rest
   }
 }
 
-template <int TOK, int T>
+template <int TOK, int T, int P>
 cudaError_t launch_scan_t(const IndexGeom& g, const uint32_t* planes, const __half2* meta, const uint8_t* bits,
                           const float* qbar, float* scores, uint32_t* hist, cudaStream_t st, const ScanTopk* tk) {
-  constexpr int64_t kTileT = int64_t(T) * TOK;
+  constexpr int64_t kTileT = int64_t(T / P) * TOK;
   const int64_t tiles = (g.n + kTileT - 1) / kTileT;
   const dim3 grid{unsigned(tiles), unsigned(g.rows), 1u};
   const ScanTopk none{};
   if (hist && tk && tk->hint && !tk->state) return cudaErrorInvalidValue;
   if (hist && tk && tk->hint)
-    scan_kernel<TOK, T, true, true><<<grid, T, 0, st>>>(planes, meta, bits, qbar, scores, hist, g.n, g.nsb, g.log2S,
-                                                        g.nblk, *tk);
+    scan_kernel<TOK, T, P, true, true><<<grid, T, 0, st>>>(planes, meta, bits, qbar, scores, hist, g.n, g.nsb,
+                                                           g.log2S, g.nblk, *tk);
   else if (hist)
-    scan_kernel<TOK, T, true, false><<<grid, T, 0, st>>>(planes, meta, bits, qbar, scores, hist, g.n, g.nsb,
-                                                         g.log2S, g.nblk, none);
+    scan_kernel<TOK, T, P, true, false><<<grid, T, 0, st>>>(planes, meta, bits, qbar, scores, hist, g.n, g.nsb,
+                                                            g.log2S, g.nblk, none);
   else
-    scan_kernel<TOK, T, false, false><<<grid, T, 0, st>>>(planes, meta, bits, qbar, scores, nullptr, g.n, g.nsb,
-                                                          g.log2S, g.nblk, none);
+    scan_kernel<TOK, T, P, false, false><<<grid, T, 0, st>>>(planes, meta, bits, qbar, scores, nullptr, g.n,
+                                                             g.nsb, g.log2S, g.nblk, none);
   return cudaGetLastError();
 }
 
@@ -326,21 +361,21 @@ cudaError_t launch_scan_t(const IndexGeom& g, const uint32_t* planes, const __ha
 
 cudaError_t launch_scan(const IndexGeom& g, const uint32_t* planes, const __half2* meta, const uint8_t* bits,
                         const float* qbar, float* scores, uint32_t* hist, cudaStream_t st, const ScanTopk* tk) {
-  // Tokens per CTA: 8192, halved (down to 1024) while the rows give fewer than two CTAs per SM --
-  // every CTA walks its row's active channels one after the other, so short rows need more CTAs.
-  const int64_t want = 2 * int64_t(num_sms());
+  // Tokens per CTA: 8192, halved (down to 1024) while the rows give fewer than four CTAs per SM;
+  // a smaller tile splits the CTA's walk over the row's active channels into 2 or 4 groups.
+  const int64_t want = 4 * int64_t(num_sms());
   int64_t tile = kScanTile;
   while (tile > 1024 && ((g.n + tile - 1) / tile) * g.rows < want) tile >>= 1;
   // two plane words per thread need 8-byte aligned planes (every run of S >= 128 tokens is)
   if ((reinterpret_cast<uintptr_t>(planes) & 7) == 0 && tile >= 2048) {
-    if (tile == 8192) return launch_scan_t<64, 128>(g, planes, meta, bits, qbar, scores, hist, st, tk);
-    if (tile == 4096) return launch_scan_t<64, 64>(g, planes, meta, bits, qbar, scores, hist, st, tk);
-    return launch_scan_t<64, 32>(g, planes, meta, bits, qbar, scores, hist, st, tk);
+    if (tile == 8192) return launch_scan_t<64, 128, 1>(g, planes, meta, bits, qbar, scores, hist, st, tk);
+    if (tile == 4096) return launch_scan_t<64, 128, 2>(g, planes, meta, bits, qbar, scores, hist, st, tk);
+    return launch_scan_t<64, 128, 4>(g, planes, meta, bits, qbar, scores, hist, st, tk);
   }
-  if (tile == 8192) return launch_scan_t<32, 256>(g, planes, meta, bits, qbar, scores, hist, st, tk);
-  if (tile == 4096) return launch_scan_t<32, 128>(g, planes, meta, bits, qbar, scores, hist, st, tk);
-  if (tile == 2048) return launch_scan_t<32, 64>(g, planes, meta, bits, qbar, scores, hist, st, tk);
-  return launch_scan_t<32, 32>(g, planes, meta, bits, qbar, scores, hist, st, tk);
+  if (tile == 8192) return launch_scan_t<32, 256, 1>(g, planes, meta, bits, qbar, scores, hist, st, tk);
+  if (tile == 4096) return launch_scan_t<32, 128, 1>(g, planes, meta, bits, qbar, scores, hist, st, tk);
+  if (tile == 2048) return launch_scan_t<32, 128, 2>(g, planes, meta, bits, qbar, scores, hist, st, tk);
+  return launch_scan_t<32, 128, 4>(g, planes, meta, bits, qbar, scores, hist, st, tk);
 }
 
 }  // namespace fathom

@@ -472,17 +472,17 @@ def test_fused_filter_gives_the_same_steps(case, gpu_lib):
 
 def _tile_case_n(t, rows):
     """A row length for which the scan's launch takes t tokens per CTA: the tile halves from
-    8192 while the rows give fewer than two CTAs per SM, so 2 * SMs * t tokens over all rows
+    8192 while the rows give fewer than four CTAs per SM, so 4 * SMs * t tokens over all rows
     (plus a ragged tail) stop it exactly at t."""
     sms = torch.cuda.get_device_properties(0).multi_processor_count
-    return 2 * sms * t // rows + 77
+    return 4 * sms * t // rows + 77
 
 
 @pytest.mark.parametrize("aligned", [True, False], ids=["planes8B", "planes4B"])
 @pytest.mark.parametrize("tile", [8192, 4096, 2048, 1024])
 def test_scan_every_tile_shape(gpu_lib, tile, aligned):
-    """Every CTA shape of the scan (tokens per thread x threads per CTA, chosen from the row
-    length and the planes' alignment): scores against the oracle on a sampled row, the step's
+    """Every CTA shape of the scan (tokens per thread, threads per CTA and channel groups,
+    chosen from the row length and the planes' alignment): scores against the oracle on a sampled row, the step's
     winners against the exact top-k of those scores, the fused filter equal to the plain step."""
     F = gpu_lib
     w0 = synth.WORKLOADS["decode36"]
