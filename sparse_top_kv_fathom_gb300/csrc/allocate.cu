@@ -31,6 +31,8 @@ __global__ void __launch_bounds__(kCand) allocate_kernel(int group, int heads, c
                                                          const uint16_t* __restrict__ budgets, int budget,
                                                          uint8_t* __restrict__ bits, float* __restrict__ qbar,
                                                          int32_t* __restrict__ status) {
+  pdl_wait();  // the previous kernel on the stream has completed
+  pdl_trigger();
   __shared__ float s_gain[kD];
   __shared__ int s_count[kD];
   __shared__ int s_weq[kCand / 32];
@@ -95,6 +97,8 @@ __global__ void __launch_bounds__(kCand) allocate_kernel(int group, int heads, c
 __global__ void __launch_bounds__(kD) allocate_sparq_kernel(int group, const void* __restrict__ q, int q_dtype,
                                                             int r_channels, uint8_t* __restrict__ bits,
                                                             float* __restrict__ qbar, int32_t* __restrict__ status) {
+  pdl_wait();  // the previous kernel on the stream has completed
+  pdl_trigger();
   __shared__ float s_a[kD];
   const int r = blockIdx.x, c = threadIdx.x;
   const int64_t q0 = int64_t(r) * group * kD + c;
@@ -116,6 +120,8 @@ __global__ void __launch_bounds__(kD) allocate_sparq_kernel(int group, const voi
 
 __global__ void __launch_bounds__(kD) qbar_kernel(int group, const void* __restrict__ q, int q_dtype,
                                                   float* __restrict__ qbar) {
+  pdl_wait();  // the previous kernel on the stream has completed
+  pdl_trigger();
   const int r = blockIdx.x, c = threadIdx.x;
   const int64_t q0 = int64_t(r) * group * kD + c;
   float s = load_as_float(q, q0, q_dtype);
@@ -127,26 +133,25 @@ __global__ void __launch_bounds__(kD) qbar_kernel(int group, const void* __restr
 
 cudaError_t launch_allocate(int rows, int group, const void* q, int q_dtype, const float* var, const uint16_t* budgets,
                             int budget, uint8_t* bits, float* qbar, int32_t* status, cudaStream_t st) {
-  allocate_kernel<<<rows, kCand, 0, st>>>(group, 1, q, q_dtype, var, budgets, budget, bits, qbar, status);
-  return cudaGetLastError();
+  return pdl_launch(allocate_kernel, dim3(rows), dim3(kCand), 0, st, group, 1, q, q_dtype, var, budgets, budget, bits,
+                    qbar, status);
 }
 
 cudaError_t launch_allocate_heads(int rows, int group, const void* q, int q_dtype, const float* var,
                                   const uint16_t* budgets, int budget, uint8_t* bits, float* qh, int32_t* status,
                                   cudaStream_t st) {
-  allocate_kernel<<<rows * group, kCand, 0, st>>>(1, group, q, q_dtype, var, budgets, budget, bits, qh, status);
-  return cudaGetLastError();
+  return pdl_launch(allocate_kernel, dim3(rows * group), dim3(kCand), 0, st, 1, group, q, q_dtype, var, budgets,
+                    budget, bits, qh, status);
 }
 
 cudaError_t launch_allocate_sparq(int rows, int group, const void* q, int q_dtype, int r_channels, uint8_t* bits,
                                   float* qbar, int32_t* status, cudaStream_t st) {
-  allocate_sparq_kernel<<<rows, kD, 0, st>>>(group, q, q_dtype, r_channels, bits, qbar, status);
-  return cudaGetLastError();
+  return pdl_launch(allocate_sparq_kernel, dim3(rows), dim3(kD), 0, st, group, q, q_dtype, r_channels, bits, qbar,
+                    status);
 }
 
 cudaError_t launch_qbar(int rows, int group, const void* q, int q_dtype, float* qbar, cudaStream_t st) {
-  qbar_kernel<<<rows, kD, 0, st>>>(group, q, q_dtype, qbar);
-  return cudaGetLastError();
+  return pdl_launch(qbar_kernel, dim3(rows), dim3(kD), 0, st, group, q, q_dtype, qbar);
 }
 
 }  // namespace fathom

@@ -197,6 +197,8 @@ __global__ void __launch_bounds__(T) attn_cluster_kernel(int64_t n, int64_t k, i
                                                          const typename KS::Args ka, const KV* __restrict__ V,
                                                          const int32_t* __restrict__ idx, float* __restrict__ out,
                                                          uint16_t* __restrict__ out_bf16) {
+  pdl_wait();  // the previous kernel on the stream has completed
+  pdl_trigger();
   using L = AttnSmem<G, T>;
   using R = Row4<KV>;
   constexpr int kWarps = T / 32;
@@ -418,13 +420,15 @@ cudaError_t launch_attn_t(int rows, int64_t n, int64_t k, const void* q, int q_d
     cfg.blockDim = dim3(T, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = unsigned(cluster);
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // see pdl_wait
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, n, k, stride, kv_div, q, q_dtype, ka,
                                              reinterpret_cast<const KV*>(V), idx, out, out_bf16);
     if (e == cudaSuccess || cluster == 8) return e;

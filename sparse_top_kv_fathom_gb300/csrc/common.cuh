@@ -7,6 +7,7 @@
 #include <stdint.h>
 
 #include <string>
+#include <utility>
 
 #include "../../include/fathom.h"
 
@@ -39,6 +40,31 @@ int device_view(const void* p, const char* name, const void** dev, bool nullable
 inline cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
 
 int num_sms();
+
+// ------------------------------------------- programmatic dependent launch ---
+// The step's kernels are launched with programmatic stream serialisation: a kernel may be
+// scheduled while the kernel before it on the stream is still running.  Each such kernel calls
+// pdl_wait() before its first access to global memory (it returns once the previous kernel has
+// completed and its writes are visible; at once when there is no such kernel) and pdl_trigger()
+// right after it, so that every kernel still running when the next one starts has itself waited
+// for everything before it.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+cudaError_t pdl_launch(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st, Args&&... args) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
 
 // --------------------------------------------------------------- dtypes ---
 __device__ __forceinline__ float load_as_float(const void* p, int64_t i, int dtype) {

@@ -80,6 +80,8 @@ __global__ void __launch_bounds__(kThreads) scan136_kernel(int64_t n, const int3
                                                            const uint8_t* __restrict__ exps,
                                                            const float* __restrict__ qbar, float* __restrict__ scores,
                                                            uint32_t* __restrict__ hist) {
+  pdl_wait();  // the previous kernel on the stream has completed
+  pdl_trigger();
   __shared__ float s_q[kSel];
   __shared__ uint32_t s_hist[kHist ? kHistBins : 1];
   const int r = blockIdx.y;
@@ -115,10 +117,8 @@ cudaError_t launch_fixed136_scan(int rows, int64_t n, const int32_t* chans, cons
                                  const float* qbar, float* scores, uint32_t* hist, cudaStream_t st) {
   dim3 grid(unsigned((n + kThreads - 1) / kThreads), unsigned(rows));
   if (hist)
-    scan136_kernel<true><<<grid, kThreads, 0, st>>>(n, chans, codes, exps, qbar, scores, hist);
-  else
-    scan136_kernel<false><<<grid, kThreads, 0, st>>>(n, chans, codes, exps, qbar, scores, nullptr);
-  return cudaGetLastError();
+    return pdl_launch(scan136_kernel<true>, grid, dim3(kThreads), 0, st, n, chans, codes, exps, qbar, scores, hist);
+  return pdl_launch(scan136_kernel<false>, grid, dim3(kThreads), 0, st, n, chans, codes, exps, qbar, scores, nullptr);
 }
 
 }  // namespace fathom

@@ -102,6 +102,8 @@ __global__ void __launch_bounds__(T, 512 / T) scan_kernel(const uint32_t* __rest
                                                                          uint32_t* __restrict__ hist, int64_t n,
                                                                          int64_t nsb, int log2S, int64_t nblk,
                                                                          const ScanTopk tk) {
+  pdl_wait();  // the previous kernel on the stream has completed
+  pdl_trigger();
   constexpr int W = ScanCfg<TOK>::kWords;
   constexpr int TT = T / P;  // threads of one channel group = token slots of the CTA
   static_assert(T % 32 == 0 && T >= 32 && T <= 512, "whole warps");
@@ -346,15 +348,13 @@ cudaError_t launch_scan_t(const IndexGeom& g, const uint32_t* planes, const __ha
   const ScanTopk none{};
   if (hist && tk && tk->hint && !tk->state) return cudaErrorInvalidValue;
   if (hist && tk && tk->hint)
-    scan_kernel<TOK, T, P, true, true><<<grid, T, 0, st>>>(planes, meta, bits, qbar, scores, hist, g.n, g.nsb,
-                                                           g.log2S, g.nblk, *tk);
-  else if (hist)
-    scan_kernel<TOK, T, P, true, false><<<grid, T, 0, st>>>(planes, meta, bits, qbar, scores, hist, g.n, g.nsb,
-                                                            g.log2S, g.nblk, none);
-  else
-    scan_kernel<TOK, T, P, false, false><<<grid, T, 0, st>>>(planes, meta, bits, qbar, scores, nullptr, g.n,
-                                                             g.nsb, g.log2S, g.nblk, none);
-  return cudaGetLastError();
+    return pdl_launch(scan_kernel<TOK, T, P, true, true>, grid, dim3(T), 0, st, planes, meta, bits, qbar, scores, hist,
+                      g.n, g.nsb, g.log2S, g.nblk, *tk);
+  if (hist)
+    return pdl_launch(scan_kernel<TOK, T, P, true, false>, grid, dim3(T), 0, st, planes, meta, bits, qbar, scores,
+                      hist, g.n, g.nsb, g.log2S, g.nblk, none);
+  return pdl_launch(scan_kernel<TOK, T, P, false, false>, grid, dim3(T), 0, st, planes, meta, bits, qbar, scores,
+                    nullptr, g.n, g.nsb, g.log2S, g.nblk, none);
 }
 
 }  // namespace

@@ -61,6 +61,8 @@ __global__ void __launch_bounds__(kHThreads, 2)
                       const uint8_t* __restrict__ bits, const float* __restrict__ qh, float* __restrict__ scores,
                       uint32_t* __restrict__ hist, int group, int h0, int combine, int64_t n, int64_t nsb, int log2S,
                       int64_t nblk) {
+  pdl_wait();  // the previous kernel on the stream has completed
+  pdl_trigger();
   __shared__ int s_ch[kD];
   __shared__ int s_dep[kD];
   __shared__ int s_hb[NH][kD];
@@ -224,15 +226,13 @@ cudaError_t launch_chunk(const IndexGeom& g, int group, int h0, bool max_mode, b
   const dim3 grid{unsigned((g.n + kHTile - 1) / kHTile), unsigned(g.rows), 1u};
   const int combine = h0 > 0;
   if (!max_mode)
-    scan_heads_kernel<NH, false, false><<<grid, kHThreads, 0, st>>>(planes, meta, bits, qh, scores, nullptr, group,
-                                                                    h0, combine, g.n, g.nsb, g.log2S, g.nblk);
-  else if (last && hist)
-    scan_heads_kernel<NH, true, true><<<grid, kHThreads, 0, st>>>(planes, meta, bits, qh, scores, hist, group, h0,
-                                                                  combine, g.n, g.nsb, g.log2S, g.nblk);
-  else
-    scan_heads_kernel<NH, true, false><<<grid, kHThreads, 0, st>>>(planes, meta, bits, qh, scores, nullptr, group,
-                                                                   h0, combine, g.n, g.nsb, g.log2S, g.nblk);
-  return cudaGetLastError();
+    return pdl_launch(scan_heads_kernel<NH, false, false>, grid, dim3(kHThreads), 0, st, planes, meta, bits, qh,
+                      scores, nullptr, group, h0, combine, g.n, g.nsb, g.log2S, g.nblk);
+  if (last && hist)
+    return pdl_launch(scan_heads_kernel<NH, true, true>, grid, dim3(kHThreads), 0, st, planes, meta, bits, qh, scores,
+                      hist, group, h0, combine, g.n, g.nsb, g.log2S, g.nblk);
+  return pdl_launch(scan_heads_kernel<NH, true, false>, grid, dim3(kHThreads), 0, st, planes, meta, bits, qh, scores,
+                    nullptr, group, h0, combine, g.n, g.nsb, g.log2S, g.nblk);
 }
 
 }  // namespace

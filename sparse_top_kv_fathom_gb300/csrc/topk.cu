@@ -123,6 +123,8 @@ __device__ __forceinline__ void warp_append(bool pred, int32_t* counter, int* sl
 // ----------------------------------------------------------------- kernels ---
 __global__ void topk_all_kernel(int64_t n, int64_t k, const float* __restrict__ scores, int32_t* __restrict__ idx,
                                 float* __restrict__ vals) {
+  pdl_wait();  // the previous kernel on the stream has completed
+  pdl_trigger();
   const int r = blockIdx.y;
   for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < k; i += int64_t(gridDim.x) * blockDim.x) {
     idx[int64_t(r) * k + i] = i < n ? int32_t(i) : -1;
@@ -132,6 +134,8 @@ __global__ void topk_all_kernel(int64_t n, int64_t k, const float* __restrict__ 
 
 __global__ void __launch_bounds__(kPassThreads) topk_hist_kernel(int64_t n, const float* __restrict__ scores,
                                                                  uint32_t* __restrict__ hist) {
+  pdl_wait();  // the previous kernel on the stream has completed
+  pdl_trigger();
   __shared__ uint32_t h[kHistBins];
   const int r = blockIdx.y;
   for (int i = threadIdx.x; i < kHistBins; i += kPassThreads) h[i] = 0u;
@@ -163,6 +167,8 @@ __global__ void __launch_bounds__(kFinThreads) topk_bin_kernel(int64_t k, int64_
                                                                const uint32_t* __restrict__ hint,
                                                                const uint32_t* __restrict__ hist,
                                                                RowState* __restrict__ state) {
+  pdl_wait();  // the previous kernel on the stream has completed
+  pdl_trigger();
   __shared__ uint32_t h[kFinThreads];
   __shared__ int s_out[2];
   const int r = blockIdx.x;
@@ -267,6 +273,8 @@ __global__ void __launch_bounds__(kPassThreads, kCompactCtasPerSm) topk_compact_
                                                                     int32_t* __restrict__ sure,
                                                                     uint32_t* __restrict__ cand_key,
                                                                     int32_t* __restrict__ cand_idx) {
+  pdl_wait();  // the previous kernel on the stream has completed
+  pdl_trigger();
   using C = WarpChunk<kVec>;
   constexpr int kWarps = kPassThreads / 32;
   static_assert(kPassItems <= 16, "packed 16-bit counts");
@@ -542,6 +550,8 @@ __global__ void __launch_bounds__(kFinThreads) topk_final_kernel(int64_t n, int6
                                                                  const int32_t* __restrict__ cand_idx,
                                                                  int32_t* __restrict__ idx, float* __restrict__ vals,
                                                                  uint32_t* __restrict__ hint) {
+  pdl_wait();  // the previous kernel on the stream has completed
+  pdl_trigger();
   extern __shared__ int32_t s_dyn[];  // region A (sort buffer or bitmap), then kCandSmem keys and indices
   int32_t* s_sel = s_dyn;
   uint32_t* s_ck = reinterpret_cast<uint32_t*>(s_dyn + kRegionA);
@@ -759,8 +769,7 @@ cudaError_t launch_topk(int rows, int64_t n, int64_t k, const float* scores, int
                         bool hist_ready, cudaStream_t st, uint32_t* hint) {
   if (k >= n) {
     dim3 grid(unsigned((k + 255) / 256 < 1024 ? (k + 255) / 256 : 1024), unsigned(rows));
-    topk_all_kernel<<<grid, 256, 0, st>>>(n, k, scores, idx, vals);
-    return cudaGetLastError();
+    return pdl_launch(topk_all_kernel, grid, dim3(256), 0, st, n, k, scores, idx, vals);
   }
   TopkWs w = carve_topk(ws, rows, n, k);
   const int64_t tiles = (n + kPassThreads * kPassItems - 1) / (kPassThreads * kPassItems);
@@ -769,22 +778,19 @@ cudaError_t launch_topk(int rows, int64_t n, int64_t k, const float* scores, int
   if (!hist_ready) {
     e = cudaMemsetAsync(w.hist, 0, size_t(rows) * kHistBins * sizeof(uint32_t), st);
     if (e != cudaSuccess) return e;
-    topk_hist_kernel<<<pgrid, kPassThreads, 0, st>>>(n, scores, w.hist);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    e = pdl_launch(topk_hist_kernel, pgrid, dim3(kPassThreads), 0, st, n, scores, w.hist);
+    if (e != cudaSuccess) return e;
   }
-  topk_bin_kernel<<<rows, kFinThreads, 0, st>>>(k, w.cap, hint, w.hist, w.state);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  e = pdl_launch(topk_bin_kernel, dim3(rows), dim3(kFinThreads), 0, st, k, w.cap, hint, w.hist, w.state);
+  if (e != cudaSuccess) return e;
   {
     const int64_t ctiles = tiles * rows;
     const int64_t resident = int64_t(num_sms()) * kCompactCtasPerSm;
     const unsigned cgrid = unsigned(ctiles < resident ? ctiles : resident);
-    if (n % 4 == 0 && (reinterpret_cast<uintptr_t>(scores) & 15) == 0)
-      topk_compact_kernel<true><<<cgrid, kPassThreads, 0, st>>>(n, k, w.cap, rows, scores, w.state, w.sure,
-                                                                w.cand_key, w.cand_idx);
-    else
-      topk_compact_kernel<false><<<cgrid, kPassThreads, 0, st>>>(n, k, w.cap, rows, scores, w.state, w.sure,
-                                                                 w.cand_key, w.cand_idx);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    const bool vec = n % 4 == 0 && (reinterpret_cast<uintptr_t>(scores) & 15) == 0;
+    e = pdl_launch(vec ? topk_compact_kernel<true> : topk_compact_kernel<false>, dim3(cgrid), dim3(kPassThreads), 0,
+                   st, n, k, w.cap, rows, scores, w.state, w.sure, w.cand_key, w.cand_idx);
+    if (e != cudaSuccess) return e;
   }
   const size_t smem = (kRegionA + 2 * kCandSmem) * sizeof(int32_t);
   static bool attr_set = false;
@@ -793,9 +799,8 @@ cudaError_t launch_topk(int rows, int64_t n, int64_t k, const float* scores, int
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  topk_final_kernel<<<rows, kFinThreads, smem, st>>>(n, k, w.cap, scores, w.state, w.sure, w.cand_key, w.cand_idx,
-                                                     idx, vals, hint);
-  return cudaGetLastError();
+  return pdl_launch(topk_final_kernel, dim3(rows), dim3(kFinThreads), smem, st, n, k, w.cap, scores, w.state, w.sure,
+                    w.cand_key, w.cand_idx, idx, vals, hint);
 }
 
 ScanTopk topk_scan_side(void* ws, int rows, int64_t n, int64_t k, const uint32_t* hint) {
