@@ -400,20 +400,21 @@ __global__ void __launch_bounds__(T) attn_cluster_kernel(int64_t n, int64_t k, i
 template <int G, typename KV, typename KS>
 cudaError_t launch_attn_t(int rows, int64_t n, int64_t k, const void* q, int q_dtype, const typename KS::Args& ka,
                           const void* V, int64_t stride, int kv_div, const int32_t* idx, float* out,
-                          uint16_t* out_bf16, cudaStream_t st) {
+                          uint16_t* out_bf16, cudaStream_t st, bool wide) {
   auto kern = attn_cluster_kernel<G, KV, KS>;
   constexpr int T = attn_threads_ks<G, KS>();
   constexpr size_t smem = AttnSmem<G, T>::bytes;
   // 16-CTA clusters need an opt-in per kernel; fall back to the portable 8 if it is refused
-  static int cluster = 0;
-  if (cluster == 0) {
+  static int cluster_max = 0;
+  if (cluster_max == 0) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
     if (e != cudaSuccess) return e;
-    cluster = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess
-                  ? kClusterMax
-                  : 8;
+    cluster_max = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess
+                      ? kClusterMax
+                      : 8;
     cudaGetLastError();
   }
+  int cluster = wide ? cluster_max : 8;
   for (;;) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(unsigned(cluster), unsigned(rows), 1);
@@ -433,7 +434,7 @@ cudaError_t launch_attn_t(int rows, int64_t n, int64_t k, const void* q, int q_d
                                              reinterpret_cast<const KV*>(V), idx, out, out_bf16);
     if (e == cudaSuccess || cluster == 8) return e;
     cudaGetLastError();  // the larger cluster could not be scheduled: use the portable size from now on
-    cluster = 8;
+    cluster = cluster_max = 8;
   }
 }
 
@@ -441,18 +442,18 @@ cudaError_t launch_attn_t(int rows, int64_t n, int64_t k, const void* q, int q_d
 template <int G, template <typename> class KSel>
 cudaError_t launch_attn_g(int rows, int64_t n, int64_t k, const void* q, int q_dtype, const void* K,
                           const KeysQ4::Args* q4, const void* V, int kv_dtype, int64_t stride, const int32_t* idx,
-                          float* out, uint16_t* out_bf16, cudaStream_t st, int kv_div) {
+                          float* out, uint16_t* out_bf16, cudaStream_t st, int kv_div, bool wide) {
   if (kv_dtype == FATHOM_F32)
     return launch_attn_t<G, float, typename KSel<float>::type>(rows, n, k, q, q_dtype,
                                                                 KSel<float>::args(K, q4, n, stride), V, stride,
-                                                                kv_div, idx, out, out_bf16, st);
+                                                                kv_div, idx, out, out_bf16, st, wide);
   if (kv_dtype == FATHOM_F16)
     return launch_attn_t<G, __half, typename KSel<__half>::type>(rows, n, k, q, q_dtype,
                                                                   KSel<__half>::args(K, q4, n, stride), V, stride,
-                                                                  kv_div, idx, out, out_bf16, st);
+                                                                  kv_div, idx, out, out_bf16, st, wide);
   return launch_attn_t<G, __nv_bfloat16, typename KSel<__nv_bfloat16>::type>(
       rows, n, k, q, q_dtype, KSel<__nv_bfloat16>::args(K, q4, n, stride), V, stride, kv_div, idx, out, out_bf16,
-      st);
+      st, wide);
 }
 
 template <typename KV>
@@ -471,13 +472,15 @@ struct SelQ4 {
 template <template <typename> class KSel>
 cudaError_t launch_attn_any(int rows, int group, int64_t n, int64_t k, const void* q, int q_dtype, const void* K,
                             const KeysQ4::Args* q4, const void* V, int kv_dtype, int64_t kv_stride,
-                            const int32_t* idx, float* out, uint16_t* out_bf16, cudaStream_t st, bool per_head) {
+                            const int32_t* idx, float* out, uint16_t* out_bf16, cudaStream_t st, bool per_head,
+                            bool wide) {
   if (per_head)  // every query head is a row of its own over its KV row's K/V
     return launch_attn_g<1, KSel>(rows * group, n, k, q, q_dtype, K, q4, V, kv_dtype, kv_stride, idx, out, out_bf16,
-                                  st, group);
+                                  st, group, wide);
 #define FATHOM_ATTN_G(GG)                                                                                          \
   case GG:                                                                                                         \
-    return launch_attn_g<GG, KSel>(rows, n, k, q, q_dtype, K, q4, V, kv_dtype, kv_stride, idx, out, out_bf16, st, 1);
+    return launch_attn_g<GG, KSel>(rows, n, k, q, q_dtype, K, q4, V, kv_dtype, kv_stride, idx, out, out_bf16, st, 1, \
+                                   wide);
   switch (group) {
     FATHOM_ATTN_G(1)
     FATHOM_ATTN_G(2)
@@ -494,13 +497,25 @@ cudaError_t launch_attn_any(int rows, int group, int64_t n, int64_t k, const voi
 
 }  // namespace
 
+// Rows gathered over the host link take 16-CTA clusters (more rows in flight hide the link's
+// latency); rows in HBM take 8, whose clusters start sooner.
+static bool host_resident(const void* p) {
+  if (!p) return false;
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return a.type == cudaMemoryTypeHost;
+}
+
 size_t attn_ws_bytes(int, int, int64_t) { return 256; }
 
 cudaError_t launch_attn(int rows, int group, int64_t n, int64_t k, const void* q, int q_dtype, const void* K,
                         const void* V, int kv_dtype, int64_t kv_stride, const int32_t* idx, float* out,
                         uint16_t* out_bf16, void* /*ws*/, cudaStream_t st, bool per_head) {
   return launch_attn_any<Sel16>(rows, group, n, k, q, q_dtype, K, nullptr, V, kv_dtype, kv_stride, idx, out,
-                                out_bf16, st, per_head);
+                                out_bf16, st, per_head, host_resident(K) || host_resident(V));
 }
 
 cudaError_t launch_attn_q4(const IndexGeom& g, int group, int64_t k, const void* q, int q_dtype,
@@ -509,7 +524,7 @@ cudaError_t launch_attn_q4(const IndexGeom& g, int group, int64_t k, const void*
   // V rows, like the index, are `capacity` tokens long
   const KeysQ4::Args a{planes, meta, g.cap, g.nsb, g.nblk, g.log2S};
   return launch_attn_any<SelQ4>(g.rows, group, g.cap, k, q, q_dtype, nullptr, &a, V, v_dtype, v_stride, idx, out,
-                                out_bf16, st, per_head);
+                                out_bf16, st, per_head, host_resident(planes) || host_resident(V));
 }
 
 }  // namespace fathom

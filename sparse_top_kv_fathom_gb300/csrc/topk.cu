@@ -29,9 +29,9 @@ constexpr int kSortMax = 8192;    // largest k sorted in shared memory
 constexpr int kCandSmem = 8192;   // candidates staged in shared memory by the final select
 constexpr int kBitmapWords = 32768;  // n <= 2^20: the chosen indices leave the final select through a bitmap
 constexpr int kRegionA = kBitmapWords > kSortMax ? kBitmapWords : kSortMax;  // bitmap or sort buffer (words)
-constexpr int kPassThreads = 256;
-constexpr int kPassItems = 16;  // items per thread in the histogram / compaction passes
-constexpr int kCompactCtasPerSm = 3;  // resident CTAs per SM of the candidate pass
+constexpr int kCThreads = 256;  // threads of the histogram and candidate passes
+constexpr int kCTile = 8192;    // scores per CTA of those passes
+constexpr int kCItems = kCTile / kCThreads;
 
 using RowState = TopkRowState;
 static_assert(sizeof(RowState) == 32, "RowState layout");
@@ -121,6 +121,33 @@ __device__ __forceinline__ void warp_append(bool pred, int32_t* counter, int* sl
 }
 
 // ----------------------------------------------------------------- kernels ---
+// A thread's share of one tile of kCTile scores (histogram and candidate passes).
+template <bool kVec>
+struct TileItems {
+  // position of a thread's item i inside the tile: float4 j = i/4 of the thread sits at j * threads + tid
+  __device__ static int pos(int i, int tid) {
+    return kVec ? 4 * ((i >> 2) * kCThreads + tid) + (i & 3) : i * kCThreads + tid;
+  }
+  __device__ static void load(const float* __restrict__ s, int lim, int tid, float (&v)[kCItems]) {
+    if (kVec && lim == kCTile) {
+#pragma unroll
+      for (int j = 0; j < kCItems / 4; ++j) {
+        const float4 x = __ldg(reinterpret_cast<const float4*>(s) + j * kCThreads + tid);
+        v[4 * j] = x.x;
+        v[4 * j + 1] = x.y;
+        v[4 * j + 2] = x.z;
+        v[4 * j + 3] = x.w;
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < kCItems; ++i) {
+        const int p = pos(i, tid);
+        v[i] = p < lim ? __ldg(s + p) : 0.0f;
+      }
+    }
+  }
+};
+
 __global__ void topk_all_kernel(int64_t n, int64_t k, const float* __restrict__ scores, int32_t* __restrict__ idx,
                                 float* __restrict__ vals) {
   pdl_wait();  // the previous kernel on the stream has completed
@@ -132,22 +159,23 @@ __global__ void topk_all_kernel(int64_t n, int64_t k, const float* __restrict__ 
   }
 }
 
-__global__ void __launch_bounds__(kPassThreads) topk_hist_kernel(int64_t n, const float* __restrict__ scores,
-                                                                 uint32_t* __restrict__ hist) {
+__global__ void __launch_bounds__(kCThreads) topk_hist_kernel(int64_t n, const float* __restrict__ scores,
+                                                              uint32_t* __restrict__ hist) {
   pdl_wait();  // the previous kernel on the stream has completed
   pdl_trigger();
   __shared__ uint32_t h[kHistBins];
-  const int r = blockIdx.y;
-  for (int i = threadIdx.x; i < kHistBins; i += kPassThreads) h[i] = 0u;
+  const int r = blockIdx.y, tid = threadIdx.x;
+  for (int i = tid; i < kHistBins; i += kCThreads) h[i] = 0u;
+  const int64_t t0 = int64_t(blockIdx.x) * kCTile;
+  const int lim = n - t0 < kCTile ? int(n - t0) : kCTile;
+  float v[kCItems];
+  TileItems<false>::load(scores + int64_t(r) * n + t0, lim, tid, v);
   __syncthreads();
-  const int64_t t0 = int64_t(blockIdx.x) * kPassThreads * kPassItems;
-  const float* s = scores + int64_t(r) * n;
-  for (int i = 0; i < kPassItems; ++i) {
-    const int64_t t = t0 + int64_t(i) * kPassThreads + threadIdx.x;
-    if (t < n) atomicAdd(&h[score_key(s[t]) >> (32 - kHistBits)], 1u);
-  }
+#pragma unroll
+  for (int i = 0; i < kCItems; ++i)
+    if (TileItems<false>::pos(i, tid) < lim) atomicAdd(&h[score_key(v[i]) >> (32 - kHistBits)], 1u);
   __syncthreads();
-  for (int i = threadIdx.x; i < kHistBins; i += kPassThreads)
+  for (int i = tid; i < kHistBins; i += kCThreads)
     if (h[i]) atomicAdd(hist + int64_t(r) * kHistBins + i, h[i]);
 }
 
@@ -211,217 +239,88 @@ __device__ __forceinline__ uint32_t score_key_fast(float v) {
 }
 
 // Candidate pass: keys in bins above b1 go to the row's sure list, keys in b1
-// to its candidate list.  Every warp works on its own: it streams a contiguous
-// run of 512-score chunks (the next chunk in flight while the current one is
-// classified), counts its lanes' hits, and stages them in a private 64-entry
-// buffer in shared memory, which it writes out (one atomic per list reserves
-// the slots) when it would overflow, when the row changes, and at the end.  No
-// block barrier anywhere; a chunk with more hits than the buffer holds is
-// written straight to the global lists.
-constexpr int kChunk = 32 * kPassItems;  // scores per warp chunk
-constexpr int kWStage = 64;              // staged entries per warp and list
-
+// to its candidate list.  One CTA per tile of kCTile scores of one row: every
+// thread loads its kCItems scores at once (the whole tile in flight), then the
+// row's state (bin b1; its load overlaps the tile's), marks its hits in two bit
+// masks, and a CTA-wide scan of the packed (sure, candidate) counts gives each
+// thread its slots after one reservation per list (thread 0's atomics on the
+// row's counters).  Rows the scan's filter already listed (fast) are skipped.
 template <bool kVec>
-struct WarpChunk {
-  // position of lane's item i inside the chunk
-  __device__ static int pos(int i, int lane) { return kVec ? 4 * ((i >> 2) * 32 + lane) + (i & 3) : i * 32 + lane; }
-  __device__ static void load(const float* __restrict__ s, int64_t n, int64_t t0, int lane, float (&v)[kPassItems]) {
-    if (kVec && t0 + kChunk <= n) {
-#pragma unroll
-      for (int j = 0; j < kPassItems / 4; ++j) {
-        const float4 x = __ldg(reinterpret_cast<const float4*>(s + t0) + j * 32 + lane);
-        v[4 * j] = x.x;
-        v[4 * j + 1] = x.y;
-        v[4 * j + 2] = x.z;
-        v[4 * j + 3] = x.w;
-      }
-    } else {
-#pragma unroll
-      for (int i = 0; i < kPassItems; ++i) {
-        const int64_t t = t0 + pos(i, lane);
-        v[i] = t < n ? __ldg(s + t) : 0.0f;
-      }
-    }
-  }
-};
-
-// Write out a warp's staged hits of `row` (ns sure, nc candidates).
-__device__ __forceinline__ void warp_flush(int64_t row, int ns, int nc, int lane, RowState* state, int64_t k,
-                                           int64_t cap, const int32_t* si, const uint32_t* ck, const int32_t* ci,
-                                           int32_t* sure, uint32_t* cand_key, int32_t* cand_idx) {
-  int bs = 0, bc = 0;
-  if (lane == 0) {
-    bs = ns ? atomicAdd(&state[row].sure_cnt, ns) : 0;
-    bc = nc ? atomicAdd(&state[row].cand_cnt, nc) : 0;
-  }
-  bs = __shfl_sync(0xffffffffu, bs, 0);
-  bc = __shfl_sync(0xffffffffu, bc, 0);
-  for (int i = lane; i < ns; i += 32)
-    if (int64_t(bs) + i < k) sure[row * k + bs + i] = si[i];
-  for (int i = lane; i < nc; i += 32)
-    if (int64_t(bc) + i < cap) {
-      cand_key[row * cap + bc + i] = ck[i];
-      cand_idx[row * cap + bc + i] = ci[i];
-    }
-  __syncwarp();  // the buffer is free again
-}
-
-template <bool kVec>
-__global__ void __launch_bounds__(kPassThreads, kCompactCtasPerSm) topk_compact_kernel(int64_t n, int64_t k, int64_t cap, int rows,
-                                                                    const float* __restrict__ scores,
-                                                                    RowState* __restrict__ state,
-                                                                    int32_t* __restrict__ sure,
-                                                                    uint32_t* __restrict__ cand_key,
-                                                                    int32_t* __restrict__ cand_idx) {
+__global__ void __launch_bounds__(kCThreads) topk_compact_kernel(int64_t n, int64_t k, int64_t cap,
+                                                                 const float* __restrict__ scores,
+                                                                 RowState* __restrict__ state,
+                                                                 int32_t* __restrict__ sure,
+                                                                 uint32_t* __restrict__ cand_key,
+                                                                 int32_t* __restrict__ cand_idx) {
   pdl_wait();  // the previous kernel on the stream has completed
   pdl_trigger();
-  using C = WarpChunk<kVec>;
-  constexpr int kWarps = kPassThreads / 32;
-  static_assert(kPassItems <= 16, "packed 16-bit counts");
-  __shared__ int32_t st_si[kWarps][kWStage];
-  __shared__ uint32_t st_ck[kWarps][kWStage];
-  __shared__ int32_t st_ci[kWarps][kWStage];
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  int32_t* si = st_si[warp];
-  uint32_t* ck = st_ck[warp];
-  int32_t* ci = st_ci[warp];
-  const int64_t chunks_row = (n + kChunk - 1) / kChunk;
-  const int64_t total = chunks_row * rows;
-  const int64_t nw = int64_t(gridDim.x) * kWarps;
-  const int64_t per = (total + nw - 1) / nw;
-  const int64_t c0 = (int64_t(blockIdx.x) * kWarps + warp) * per;
-  const int64_t c1 = c0 + per < total ? c0 + per : total;
-  if (c0 >= c1) return;  // whole warps only: no block barrier follows
-  int ns_st = 0, nc_st = 0;  // staged counts (warp-uniform)
-  // (row, first token) of the current chunk and of the next one, stepped without divisions
-  int64_t r = c0 / chunks_row, t0 = (c0 % chunks_row) * kChunk;
-  int64_t rn = t0 + kChunk < n ? r : r + 1, tn = t0 + kChunk < n ? t0 + kChunk : 0;
-  int64_t row_st = r;
-  float cur[kPassItems];
-  if (!__ldg(&state[r].fast)) C::load(scores + r * n, n, t0, lane, cur);
-  for (int64_t c = c0; c < c1; ++c) {
-    float nxt[kPassItems];
-    if (c + 1 < c1 && !__ldg(&state[rn].fast)) C::load(scores + rn * n, n, tn, lane, nxt);
-    // keys in (khi, ~0] are sure, keys in [klo, khi] candidates
-    if (__ldg(&state[r].fast)) {  // the scan's filter already listed this row's candidates
-      if (c + 1 < c1) {
+  using I = TileItems<kVec>;
+  static_assert(kCItems <= 32 && kCTile < 65536, "32-bit item masks, packed 16-bit counts");
+  __shared__ uint32_t s_warp[kCThreads / 32];
+  __shared__ int s_base[2];
+  const int r = blockIdx.y, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  RowState* srow = state + r;
+  const int64_t t0 = int64_t(blockIdx.x) * kCTile;
+  const int lim = n - t0 < kCTile ? int(n - t0) : kCTile;  // items of this tile inside the row
+  float v[kCItems];
+  I::load(scores + int64_t(r) * n + t0, lim, tid, v);
+  const int32_t fast = __ldg(&srow->fast);
+  const uint32_t b1 = __ldg(&srow->b1);
+  if (fast) return;  // the scan's filter already listed this row's candidates
+  // keys in (khi, ~0] are sure, keys in [klo, khi] candidates
+  constexpr uint32_t kSpan = (1u << (32 - kHistBits)) - 1u;
+  const uint32_t klo = b1 << (32 - kHistBits), khi = klo | kSpan;
+  uint32_t ms = 0u, mc = 0u;  // bit i: this thread's item i is a sure winner / a candidate
 #pragma unroll
-        for (int i = 0; i < kPassItems; ++i) cur[i] = nxt[i];
-      }
-      r = rn;
-      t0 = tn;
-      if (tn + kChunk < n) {
-        tn += kChunk;
-      } else {
-        ++rn;
-        tn = 0;
-      }
-      continue;
-    }
-    const uint32_t b1 = __ldg(&state[r].b1);
-    constexpr uint32_t kSpan = (1u << (32 - kHistBits)) - 1u;
-    const uint32_t klo = b1 << (32 - kHistBits), khi = klo | kSpan;
-    const int lim = n - t0 < kChunk ? int(n - t0) : kChunk;  // items of this chunk inside the row
-    uint32_t ms = 0u, mc = 0u;  // bit i: this lane's item i is a sure winner / a candidate
+  for (int i = 0; i < kCItems; ++i) {
+    const uint32_t key = score_key_fast(v[i]);
+    const uint32_t in = uint32_t(I::pos(i, tid) < lim);
+    ms |= (uint32_t(key > khi) & in) << i;
+    mc |= (uint32_t(key - klo <= kSpan) & in) << i;
+  }
+  // CTA-wide exclusive scan of the packed counts (sure in the low, candidates in the high half)
+  const uint32_t mine = uint32_t(__popc(ms)) | (uint32_t(__popc(mc)) << 16);
+  uint32_t x = mine;
 #pragma unroll
-    for (int i = 0; i < kPassItems; ++i) {
-      const uint32_t key = score_key_fast(cur[i]);
-      ms |= uint32_t(key > khi) << i;
-      mc |= uint32_t(key - klo <= kSpan) << i;
-    }
-    if (lim < kChunk) {  // the row's last chunk: drop items past n
-      uint32_t vm = 0u;
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) s_warp[warp] = x;
+  __syncthreads();
+  uint32_t before = 0u, tot = 0u;
 #pragma unroll
-      for (int i = 0; i < kPassItems; ++i) vm |= uint32_t(C::pos(i, lane) < lim) << i;
-      ms &= vm;
-      mc &= vm;
-    }
-    const uint32_t mine = uint32_t(__popc(ms)) | (uint32_t(__popc(mc)) << 16);
-    uint32_t x = mine;  // inclusive warp scan of the packed (sure, candidate) counts
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
-      if (lane >= o) x += y;
-    }
-    const uint32_t tot = __shfl_sync(0xffffffffu, x, 31);
+  for (int w = 0; w < kCThreads / 32; ++w) {
+    const uint32_t c = s_warp[w];
+    before += w < warp ? c : 0u;
+    tot += c;
+  }
+  if (tid == 0) {
     const int ts = int(tot & 0xFFFFu), tc = int(tot >> 16);
-    if (ts == 0 && tc == 0) {
-      if (c + 1 < c1) {
+    s_base[0] = ts ? atomicAdd(&srow->sure_cnt, ts) : 0;
+    s_base[1] = tc ? atomicAdd(&srow->cand_cnt, tc) : 0;
+  }
+  __syncthreads();
+  if (!mine) return;
+  const uint32_t excl = before + x - mine;
+  int64_t ps = int64_t(s_base[0]) + (excl & 0xFFFFu);
+  int64_t pc = int64_t(s_base[1]) + (excl >> 16);
+  const uint32_t hit = ms | mc;
 #pragma unroll
-        for (int i = 0; i < kPassItems; ++i) cur[i] = nxt[i];
-      }
-      r = rn;
-      t0 = tn;
-      if (tn + kChunk < n) {
-        tn += kChunk;
-      } else {
-        ++rn;
-        tn = 0;
-      }
-      continue;
-    }
-    const bool direct = ts > kWStage || tc > kWStage;
-    if (ns_st + nc_st > 0 && (row_st != r || direct || ns_st + ts > kWStage || nc_st + tc > kWStage)) {
-      warp_flush(row_st, ns_st, nc_st, lane, state, k, cap, si, ck, ci, sure, cand_key, cand_idx);
-      ns_st = nc_st = 0;
-    }
-    int64_t ps, pc;  // this lane's first slot in each list (stage or global)
-    const uint32_t excl = x - mine;
-    if (direct) {
-      int bs = 0, bc = 0;
-      if (lane == 0) {
-        bs = ts ? atomicAdd(&state[r].sure_cnt, ts) : 0;
-        bc = tc ? atomicAdd(&state[r].cand_cnt, tc) : 0;
-      }
-      ps = int64_t(__shfl_sync(0xffffffffu, bs, 0)) + (excl & 0xFFFFu);
-      pc = int64_t(__shfl_sync(0xffffffffu, bc, 0)) + (excl >> 16);
+  for (int i = 0; i < kCItems; ++i) {
+    if (!((hit >> i) & 1u)) continue;
+    const int32_t t = int32_t(t0 + I::pos(i, tid));
+    if ((ms >> i) & 1u) {
+      if (ps < k) sure[int64_t(r) * k + ps] = t;
+      ++ps;
     } else {
-      ps = ns_st + (excl & 0xFFFFu);
-      pc = nc_st + (excl >> 16);
-    }
-    if (mine) {  // this lane holds hits: place them, visiting only the marked items
-      const uint32_t hit = ms | mc;
-#pragma unroll
-      for (int i = 0; i < kPassItems; ++i) {
-        if (!((hit >> i) & 1u)) continue;
-        const int32_t t = int32_t(t0 + C::pos(i, lane));
-        if ((ms >> i) & 1u) {
-          if (!direct) si[ps] = t;
-          else if (ps < k) sure[r * k + ps] = t;
-          ++ps;
-        } else {
-          const uint32_t key = score_key_fast(cur[i]);
-          if (!direct) {
-            ck[pc] = key;
-            ci[pc] = t;
-          } else if (pc < cap) {
-            cand_key[r * cap + pc] = key;
-            cand_idx[r * cap + pc] = t;
-          }
-          ++pc;
-        }
+      if (pc < cap) {
+        cand_key[int64_t(r) * cap + pc] = score_key_fast(v[i]);
+        cand_idx[int64_t(r) * cap + pc] = t;
       }
-    }
-    __syncwarp();  // staged entries visible to the whole warp
-    if (!direct) {
-      ns_st += ts;
-      nc_st += tc;
-      row_st = r;
-    }
-    if (c + 1 < c1) {
-#pragma unroll
-      for (int i = 0; i < kPassItems; ++i) cur[i] = nxt[i];
-    }
-    r = rn;
-    t0 = tn;
-    if (tn + kChunk < n) {
-      tn += kChunk;
-    } else {
-      ++rn;
-      tn = 0;
+      ++pc;
     }
   }
-  if (ns_st + nc_st > 0) warp_flush(row_st, ns_st, nc_st, lane, state, k, cap, si, ck, ci, sure, cand_key, cand_idx);
 }
 
 // Bitonic sort (ascending) of s[0..m) in shared memory, m a power of two.
@@ -450,8 +349,9 @@ __device__ void bitonic_sort(int32_t* s, int m) {
 }
 
 // Exact select directly over the row's n scores (one CTA): threshold key T, the
-// index cut among keys equal to T, then ordered output.
-__device__ void select_row_direct(int64_t n, int64_t k, const float* s, int32_t* out_idx, float* out_vals,
+// index cut among keys equal to T, then ordered output.  Out of line (a fallback):
+// the final select's common path stays short in the instruction cache.
+__device__ __noinline__ void select_row_direct(int64_t n, int64_t k, const float* s, int32_t* out_idx, float* out_vals,
                                   uint32_t* h, int* s_out, uint32_t* hint_out) {
   const int tid = threadIdx.x;
   // --- threshold key by three digits: 12 bits (in 4 folds of 1024), 10, 10
@@ -542,6 +442,37 @@ __device__ void select_row_direct(int64_t n, int64_t k, const float* s, int32_t*
   (void)gt;
 }
 
+// The k chosen indices (the sure list, then the candidates above T or equal to T
+// up to index `cut`) gathered into s_sel and sorted (rows too long for the bitmap).
+// Out of line, like select_row_direct.
+__device__ __noinline__ void emit_sorted(int64_t k, int r, const float* s, const int32_t* __restrict__ sure, int nsure,
+                                         const uint32_t* ck, const int32_t* ci, int m, uint32_t T, int32_t cut,
+                                         int32_t* s_sel, int* s_fill, int32_t* oi, float* ov) {
+  const int tid = threadIdx.x;
+  int pow2 = 1;
+  while (pow2 < k) pow2 <<= 1;
+  for (int i = tid; i < pow2; i += kFinThreads) s_sel[i] = 0x7fffffff;
+  if (tid == 0) *s_fill = 0;
+  __syncthreads();
+  for (int i = tid; i < nsure; i += kFinThreads) s_sel[i] = sure[int64_t(r) * k + i];
+  if (tid == 0) *s_fill = nsure;
+  __syncthreads();
+  for (int i0 = 0; i0 < m; i0 += kFinThreads) {  // whole warps: one shared atomic per warp
+    const int i = i0 + tid;
+    const bool take = i < m && (ck[i] > T || (ck[i] == T && ci[i] <= cut));
+    int p;
+    warp_append(take, s_fill, &p);
+    if (take) s_sel[p] = ci[i];
+  }
+  __syncthreads();
+  bitonic_sort(s_sel, pow2);
+  for (int i = tid; i < k; i += kFinThreads) {
+    const int32_t t = s_sel[i];
+    oi[i] = t;
+    if (ov) ov[i] = s[t];
+  }
+}
+
 __global__ void __launch_bounds__(kFinThreads) topk_final_kernel(int64_t n, int64_t k, int64_t cap,
                                                                  const float* __restrict__ scores,
                                                                  const RowState* __restrict__ state,
@@ -561,6 +492,12 @@ __global__ void __launch_bounds__(kFinThreads) topk_final_kernel(int64_t n, int6
   __shared__ int s_fill;
   const int r = blockIdx.x;
   const int tid = threadIdx.x;
+  // the row's first candidates and sure entries, loaded before its state (their counts) arrives:
+  // one round trip to memory instead of two (entries past the counts are never used)
+  const uint32_t pk = tid < cap ? cand_key[int64_t(r) * cap + tid] : 0u;
+  const int32_t pi = tid < cap ? cand_idx[int64_t(r) * cap + tid] : 0;
+  const int32_t ps0 = tid < k ? sure[int64_t(r) * k + tid] : -1;
+  const int32_t ps1 = tid + kFinThreads < k ? sure[int64_t(r) * k + kFinThreads + tid] : -1;
   const RowState st = state[r];
   const float* s = scores + int64_t(r) * n;
   int32_t* oi = idx + int64_t(r) * k;
@@ -576,7 +513,11 @@ __global__ void __launch_bounds__(kFinThreads) topk_final_kernel(int64_t n, int6
   const int32_t* ci = cand_idx + int64_t(r) * cap;
   if (m <= kCandSmem) {  // stage the candidates once, many loads in flight per thread
     constexpr int kBatch = 8;
-    for (int base = 0; base < m; base += kFinThreads * kBatch) {
+    if (tid < m) {
+      s_ck[tid] = pk;
+      s_ci[tid] = pi;
+    }
+    for (int base = kFinThreads; base < m; base += kFinThreads * kBatch) {
       uint32_t kk[kBatch];
       int32_t ii[kBatch];
 #pragma unroll
@@ -686,7 +627,7 @@ __global__ void __launch_bounds__(kFinThreads) topk_final_kernel(int64_t n, int6
     touch[tid] = 0u;
     __syncthreads();
     for (int i = tid; i < nsure; i += kFinThreads) {
-      const int32_t t = sure[int64_t(r) * k + i];
+      const int32_t t = i < kFinThreads ? ps0 : i < 2 * kFinThreads ? ps1 : sure[int64_t(r) * k + i];
       if (uint32_t(t) < uint32_t(n)) {
         atomicOr(&bm[t >> 5], 1u << (t & 31));
         atomicOr(&touch[t >> 10], 1u << ((t >> 5) & 31));
@@ -732,28 +673,7 @@ __global__ void __launch_bounds__(kFinThreads) topk_final_kernel(int64_t n, int6
     return;
   }
   // --- gather the k chosen indices and sort them
-  int pow2 = 1;
-  while (pow2 < k) pow2 <<= 1;
-  for (int i = tid; i < pow2; i += kFinThreads) s_sel[i] = 0x7fffffff;
-  if (tid == 0) s_fill = 0;
-  __syncthreads();
-  for (int i = tid; i < nsure; i += kFinThreads) s_sel[i] = sure[int64_t(r) * k + i];
-  if (tid == 0) s_fill = nsure;
-  __syncthreads();
-  for (int i0 = 0; i0 < m; i0 += kFinThreads) {  // whole warps: one shared atomic per warp
-    const int i = i0 + tid;
-    const bool take = i < m && (ck[i] > T || (ck[i] == T && ci[i] <= cut));
-    int p;
-    warp_append(take, &s_fill, &p);
-    if (take) s_sel[p] = ci[i];
-  }
-  __syncthreads();
-  bitonic_sort(s_sel, pow2);
-  for (int i = tid; i < k; i += kFinThreads) {
-    const int32_t t = s_sel[i];
-    oi[i] = t;
-    if (ov) ov[i] = s[t];
-  }
+  emit_sorted(k, r, s, sure, nsure, ck, ci, m, T, cut, s_sel, &s_fill, oi, ov);
 }
 
 }  // namespace
@@ -772,26 +692,21 @@ cudaError_t launch_topk(int rows, int64_t n, int64_t k, const float* scores, int
     return pdl_launch(topk_all_kernel, grid, dim3(256), 0, st, n, k, scores, idx, vals);
   }
   TopkWs w = carve_topk(ws, rows, n, k);
-  const int64_t tiles = (n + kPassThreads * kPassItems - 1) / (kPassThreads * kPassItems);
+  const int64_t tiles = (n + kCTile - 1) / kCTile;
   const dim3 pgrid{unsigned(tiles), unsigned(rows), 1u};
   cudaError_t e;
   if (!hist_ready) {
     e = cudaMemsetAsync(w.hist, 0, size_t(rows) * kHistBins * sizeof(uint32_t), st);
     if (e != cudaSuccess) return e;
-    e = pdl_launch(topk_hist_kernel, pgrid, dim3(kPassThreads), 0, st, n, scores, w.hist);
+    e = pdl_launch(topk_hist_kernel, pgrid, dim3(kCThreads), 0, st, n, scores, w.hist);
     if (e != cudaSuccess) return e;
   }
   e = pdl_launch(topk_bin_kernel, dim3(rows), dim3(kFinThreads), 0, st, k, w.cap, hint, w.hist, w.state);
   if (e != cudaSuccess) return e;
-  {
-    const int64_t ctiles = tiles * rows;
-    const int64_t resident = int64_t(num_sms()) * kCompactCtasPerSm;
-    const unsigned cgrid = unsigned(ctiles < resident ? ctiles : resident);
-    const bool vec = n % 4 == 0 && (reinterpret_cast<uintptr_t>(scores) & 15) == 0;
-    e = pdl_launch(vec ? topk_compact_kernel<true> : topk_compact_kernel<false>, dim3(cgrid), dim3(kPassThreads), 0,
-                   st, n, k, w.cap, rows, scores, w.state, w.sure, w.cand_key, w.cand_idx);
-    if (e != cudaSuccess) return e;
-  }
+  const bool vec = n % 4 == 0 && (reinterpret_cast<uintptr_t>(scores) & 15) == 0;
+  e = pdl_launch(vec ? topk_compact_kernel<true> : topk_compact_kernel<false>, pgrid, dim3(kCThreads), 0, st, n, k,
+                 w.cap, scores, w.state, w.sure, w.cand_key, w.cand_idx);
+  if (e != cudaSuccess) return e;
   const size_t smem = (kRegionA + 2 * kCandSmem) * sizeof(int32_t);
   static bool attr_set = false;
   if (!attr_set) {

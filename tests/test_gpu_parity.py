@@ -40,6 +40,13 @@ def check_scores(gpu, ref, l1):
     assert not bad.any(), "max rel err %g" % (err / np.maximum(l1, 1e-300)).max()
 
 
+def same_attention(a, b):
+    """Attention outputs of the same winners with K/V in different memories.  Rows gathered over
+    the host link are split over twice as many CTAs (16-CTA clusters instead of 8), so the
+    fp32 partial sums are merged in another order: equal within fp32 rounding, not bit for bit."""
+    assert torch.allclose(a, b, rtol=1e-5, atol=1e-6), (a - b).abs().max().item()
+
+
 def check_attn(out, outb, ref):
     assert np.abs(out - ref).max() <= ATTN_ATOL, np.abs(out - ref).max()
     rne = torch.from_numpy(out).to(torch.bfloat16).float().numpy()
@@ -145,7 +152,7 @@ def test_decode_step_host_resident_kv_and_index(case, gpu_lib):
     Kh, Vh = case["Kd"].cpu().pin_memory(), case["Vd"].cpu().pin_memory()
     b = F.decode_step(case["index"].to_host(), case["qd"], Kh, Vh, k, w.group, B)
     assert torch.equal(a[0], b[0])
-    assert torch.equal(a[1], b[1])
+    same_attention(a[1], b[1])
 
 
 def test_interleaved_kv_in_huge_page_host_memory(case, gpu_lib):
@@ -166,7 +173,7 @@ def test_interleaved_kv_in_huge_page_host_memory(case, gpu_lib):
     b = F.decode_step(hix, case["qd"], KV[:, :, 0], KV[:, :, 1], k, w.group, 92)
     torch.cuda.synchronize()
     assert torch.equal(a[0], b[0])
-    assert torch.equal(a[1], b[1])
+    same_attention(a[1], b[1])
     for t in (KV, planes, meta):
         F.host_release(t)
 
@@ -351,7 +358,7 @@ def test_sparse_attention_on_the_index_parity(case, gpu_lib):
     check_attn(out.cpu().numpy(), outb, ref)
     # index and V in pinned host memory: the same result
     o2, _ = F.sparse_attn_q4(case["index"].to_host(), case["qd"], case["Vd"].cpu().pin_memory(), idt, w.group)
-    assert torch.equal(out, o2)
+    same_attention(out, o2)
 
 
 @pytest.mark.parametrize("gqa", ["sum", "per_head"])
