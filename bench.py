@@ -665,7 +665,8 @@ def main():
         "machine_balance": machine_balance(int_ops, hbm_peak, link_gbs, w, args.budget),
         "e2e": p.get("e2e"),
         "clocks": p.get("clocks"),
-        # per layer: allocate, scan, top-k bin / candidate / final, attention (plus one memset node)
+        # per layer: allocate (which also clears the histogram), scan, top-k bin / candidate /
+        # final passes, attention
         "gpu_launches": args.steps * w.layers * 6,
     }
     if "device" in result and primary == "host":

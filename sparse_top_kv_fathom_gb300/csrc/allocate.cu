@@ -16,7 +16,9 @@
 // patterns of non-negative fp32 gains (which order like integers), the largest
 // tau with at least B gains >= tau, each count taken by one __syncthreads_count.
 // Gains above tau are taken; gains equal to tau are handed out in (j, c) order
-// (j ascending, then c ascending) until exactly B are taken.
+// (j ascending, then c ascending) until exactly B are taken.  The kernel also
+// zeroes a span of the caller's workspace (the top-k histogram the scan fills
+// next), sparing the step a memset.
 #include "common.cuh"
 
 namespace fathom {
@@ -30,9 +32,12 @@ __global__ void __launch_bounds__(kCand) allocate_kernel(int group, int heads, c
                                                          const float* __restrict__ var,
                                                          const uint16_t* __restrict__ budgets, int budget,
                                                          uint8_t* __restrict__ bits, float* __restrict__ qbar,
-                                                         int32_t* __restrict__ status) {
+                                                         int32_t* __restrict__ status, uint4* __restrict__ zero,
+                                                         int64_t zero16) {
   pdl_wait();  // the previous kernel on the stream has completed
   pdl_trigger();
+  for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < zero16; i += int64_t(gridDim.x) * blockDim.x)
+    zero[i] = make_uint4(0u, 0u, 0u, 0u);
   __shared__ float s_gain[kD];
   __shared__ int s_count[kD];
   __shared__ int s_weq[kCand / 32];
@@ -132,16 +137,18 @@ __global__ void __launch_bounds__(kD) qbar_kernel(int group, const void* __restr
 }  // namespace
 
 cudaError_t launch_allocate(int rows, int group, const void* q, int q_dtype, const float* var, const uint16_t* budgets,
-                            int budget, uint8_t* bits, float* qbar, int32_t* status, cudaStream_t st) {
+                            int budget, uint8_t* bits, float* qbar, int32_t* status, cudaStream_t st, void* zero,
+                            size_t zero_bytes) {
+  if ((reinterpret_cast<uintptr_t>(zero) | zero_bytes) & 15) return cudaErrorInvalidValue;
   return pdl_launch(allocate_kernel, dim3(rows), dim3(kCand), 0, st, group, 1, q, q_dtype, var, budgets, budget, bits,
-                    qbar, status);
+                    qbar, status, static_cast<uint4*>(zero), int64_t(zero_bytes / 16));
 }
 
 cudaError_t launch_allocate_heads(int rows, int group, const void* q, int q_dtype, const float* var,
                                   const uint16_t* budgets, int budget, uint8_t* bits, float* qh, int32_t* status,
                                   cudaStream_t st) {
   return pdl_launch(allocate_kernel, dim3(rows * group), dim3(kCand), 0, st, 1, group, q, q_dtype, var, budgets,
-                    budget, bits, qh, status);
+                    budget, bits, qh, status, static_cast<uint4*>(nullptr), int64_t(0));
 }
 
 cudaError_t launch_allocate_sparq(int rows, int group, const void* q, int q_dtype, int r_channels, uint8_t* bits,

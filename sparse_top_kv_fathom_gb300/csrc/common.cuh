@@ -150,8 +150,10 @@ ScanTopk topk_scan_side(void* ws, int rows, int64_t n, int64_t k, const uint32_t
 size_t topk_state_clear_bytes(int rows);
 
 // launchers used by the step functions (arguments already validated)
+// zero / zero_bytes (16-byte aligned, or NULL / 0): a workspace span the kernel clears as well
 cudaError_t launch_allocate(int rows, int group, const void* q, int q_dtype, const float* var, const uint16_t* budgets,
-                            int budget, uint8_t* bits, float* qbar, int32_t* status, cudaStream_t st);
+                            int budget, uint8_t* bits, float* qbar, int32_t* status, cudaStream_t st,
+                            void* zero = nullptr, size_t zero_bytes = 0);
 cudaError_t launch_allocate_heads(int rows, int group, const void* q, int q_dtype, const float* var,
                                   const uint16_t* budgets, int budget, uint8_t* bits, float* qh, int32_t* status,
                                   cudaStream_t st);
@@ -163,8 +165,9 @@ cudaError_t launch_allocate_sparq(int rows, int group, const void* q, int q_dtyp
 cudaError_t launch_scan(const IndexGeom& g, const uint32_t* planes, const __half2* meta, const uint8_t* bits,
                         const float* qbar, float* scores, uint32_t* hist, cudaStream_t st,
                         const ScanTopk* topk = nullptr);
-// hist_ready: the histogram is built; hint: the fused filter's per-row hints (read, and
-// rewritten for the next step), or NULL
+// hist_ready: the histogram is built (the caller cleared histogram and row states,
+// topk_state_clear_bytes from the histogram on, before filling it); hint: the fused
+// filter's per-row hints (read, and rewritten for the next step), or NULL
 cudaError_t launch_topk(int rows, int64_t n, int64_t k, const float* scores, int32_t* idx, float* vals, void* ws,
                         bool hist_ready, cudaStream_t st, uint32_t* hint = nullptr);
 // per_head: idx holds one winner set per query head ([rows*group][k]), each head attends over its own

@@ -105,7 +105,7 @@ int fathom_decode_step(const fathom_step_desc* s, void* workspace, size_t ws_byt
     const int srows = gqa == FATHOM_GQA_PER_HEAD ? g.rows * s->group : g.rows;
     const bool use_hist = gqa == FATHOM_GQA_MAX && s->k < g.n;
     uint32_t* hist = use_hist ? topk_hist_ptr(w.topk, srows, g.n, s->k) : nullptr;
-    if (hist) FATHOM_TRY_CUDA(cudaMemsetAsync(hist, 0, size_t(srows) * kHistBins * sizeof(uint32_t), st));
+    if (hist) FATHOM_TRY_CUDA(cudaMemsetAsync(hist, 0, topk_state_clear_bytes(srows), st));
     FATHOM_TRY_CUDA(launch_allocate_heads(g.rows, s->group, dq, s->q_dtype, (const float*)dVar,
                                           (const uint16_t*)dBud, s->budget, w.bits, w.qbar, (int32_t*)dSt, st));
     FATHOM_TRY_CUDA(launch_scan_heads(g, s->group, gqa, (const uint32_t*)dP, (const __half2*)dM, w.bits, w.qbar,
@@ -126,17 +126,18 @@ int fathom_decode_step(const fathom_step_desc* s, void* workspace, size_t ws_byt
   const void* dH = nullptr;
   FATHOM_TRY(device_view(s->hint, "hint", &dH, true));
   uint32_t* hint = use_hist ? (uint32_t*)dH : nullptr;  // the fused filter (k < n only)
-  // the histogram, and with the filter the row states whose candidate counters the scan bumps
-  if (hist)
-    FATHOM_TRY_CUDA(cudaMemsetAsync(hist, 0, hint ? topk_state_clear_bytes(g.rows)
-                                                    : size_t(g.rows) * kHistBins * sizeof(uint32_t), st));
+  // the histogram, and with the filter the row states whose candidate counters the scan bumps,
+  // start at zero (cleared by the allocation kernel, or a memset before the SparQ-style one)
+  const size_t clear = hist ? topk_state_clear_bytes(g.rows) : 0;
   const ScanTopk tk = topk_scan_side(w.topk, g.rows, g.n, s->k, hint);
-  if (s->sparq_r > 0)
+  if (s->sparq_r > 0) {
+    if (clear) FATHOM_TRY_CUDA(cudaMemsetAsync(hist, 0, clear, st));
     FATHOM_TRY_CUDA(launch_allocate_sparq(g.rows, s->group, dq, s->q_dtype, s->sparq_r, w.bits, w.qbar,
                                           (int32_t*)dSt, st));
-  else
+  } else {
     FATHOM_TRY_CUDA(launch_allocate(g.rows, s->group, dq, s->q_dtype, (const float*)dVar, (const uint16_t*)dBud,
-                                    s->budget, w.bits, w.qbar, (int32_t*)dSt, st));
+                                    s->budget, w.bits, w.qbar, (int32_t*)dSt, st, hist, clear));
+  }
   FATHOM_TRY_CUDA(launch_scan(g, (const uint32_t*)dP, (const __half2*)dM, w.bits, w.qbar, w.scores, hist, st,
                               hint ? &tk : nullptr));
   FATHOM_TRY_CUDA(launch_topk(g.rows, g.n, s->k, w.scores, (int32_t*)dI, nullptr, w.topk, use_hist, st, hint));
@@ -188,7 +189,7 @@ int fathom_fixed136_decode_step(const fathom_fixed136_step_desc* s, void* worksp
   cudaStream_t st = as_stream(stream);
   const bool use_hist = s->k < s->n;
   uint32_t* hist = use_hist ? topk_hist_ptr(w.topk, s->rows, s->n, s->k) : nullptr;
-  if (hist) FATHOM_TRY_CUDA(cudaMemsetAsync(hist, 0, size_t(s->rows) * kHistBins * sizeof(uint32_t), st));
+  if (hist) FATHOM_TRY_CUDA(cudaMemsetAsync(hist, 0, topk_state_clear_bytes(s->rows), st));
   FATHOM_TRY_CUDA(launch_qbar(s->rows, s->group, dq, s->q_dtype, w.qbar, st));
   FATHOM_TRY_CUDA(launch_fixed136_scan(s->rows, s->n, (const int32_t*)dC, (const uint8_t*)dX, (const uint8_t*)dE,
                                        w.qbar, w.scores, hist, st));

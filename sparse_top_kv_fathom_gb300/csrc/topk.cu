@@ -498,12 +498,17 @@ __global__ void __launch_bounds__(kFinThreads) topk_final_kernel(int64_t n, int6
   const int32_t pi = tid < cap ? cand_idx[int64_t(r) * cap + tid] : 0;
   const int32_t ps0 = tid < k ? sure[int64_t(r) * k + tid] : -1;
   const int32_t ps1 = tid + kFinThreads < k ? sure[int64_t(r) * k + kFinThreads + tid] : -1;
+  const int64_t words = (n + 31) >> 5;
+  if (words <= kBitmapWords) {  // clear the output bitmap while those loads travel
+    const int64_t words4 = (words + 3) >> 2;
+    for (int64_t i = tid; i < words4; i += kFinThreads)
+      reinterpret_cast<uint4*>(s_dyn)[i] = make_uint4(0u, 0u, 0u, 0u);
+  }
   const RowState st = state[r];
   const float* s = scores + int64_t(r) * n;
   int32_t* oi = idx + int64_t(r) * k;
   float* ov = vals ? vals + int64_t(r) * k : nullptr;
   const int m = st.cand_cnt;
-  const int64_t words = (n + 31) >> 5;
   uint32_t* hint_out = hint ? hint + r : nullptr;
   if (m > cap || (k > kSortMax && words > kBitmapWords)) {
     select_row_direct(n, k, s, oi, ov, h, s_out, hint_out);
@@ -546,6 +551,7 @@ __global__ void __launch_bounds__(kFinThreads) topk_final_kernel(int64_t n, int6
   int need = int(k) - above;  // >= 1
   // --- digits 2 and 3 (bits 19..10 and 9..0) among the candidates
   uint32_t prefix = b1 << 20, pmask = 0xFFF00000u;
+  int eq_total = 0;  // candidates equal to the threshold key: the last digit's bin
   for (int sh = 10; sh >= 0; sh -= 10) {
     h[tid] = 0u;
     __syncthreads();
@@ -558,6 +564,7 @@ __global__ void __launch_bounds__(kFinThreads) topk_final_kernel(int64_t n, int6
     need -= s_out[1];
     prefix |= uint32_t(s_out[0]) << sh;
     pmask |= 0x3FFu << sh;
+    eq_total = int(h[s_out[0]]);
     __syncthreads();
   }
   const uint32_t T = prefix;
@@ -567,11 +574,7 @@ __global__ void __launch_bounds__(kFinThreads) topk_final_kernel(int64_t n, int6
   {
     uint32_t ip = 0u, im = 0u;
     int ineed = need;
-    int eq_total = 0;
-    for (int i = tid; i < m; i += kFinThreads) eq_total += ck[i] == T;
-    int tot;
-    block_exclusive_scan(eq_total, &tot);
-    if (tot > need) {
+    if (eq_total > need) {
       const int ishift[3] = {21, 10, 0};
       const int iwidth[3] = {10, 11, 10};
       for (int p = 0; p < 3; ++p) {
@@ -620,10 +623,8 @@ __global__ void __launch_bounds__(kFinThreads) topk_final_kernel(int64_t n, int6
   if (words <= kBitmapWords) {
     // --- mark the k chosen indices in a bitmap (and the words touched in a second
     // one), then emit them in index order
-    uint32_t* bm = reinterpret_cast<uint32_t*>(s_dyn);
+    uint32_t* bm = reinterpret_cast<uint32_t*>(s_dyn);  // cleared at the start
     uint32_t* touch = h;  // 1024 words: one bit per bitmap word
-    const int64_t words4 = (words + 3) >> 2;
-    for (int64_t i = tid; i < words4; i += kFinThreads) reinterpret_cast<uint4*>(bm)[i] = make_uint4(0u, 0u, 0u, 0u);
     touch[tid] = 0u;
     __syncthreads();
     for (int i = tid; i < nsure; i += kFinThreads) {
@@ -696,7 +697,7 @@ cudaError_t launch_topk(int rows, int64_t n, int64_t k, const float* scores, int
   const dim3 pgrid{unsigned(tiles), unsigned(rows), 1u};
   cudaError_t e;
   if (!hist_ready) {
-    e = cudaMemsetAsync(w.hist, 0, size_t(rows) * kHistBins * sizeof(uint32_t), st);
+    e = cudaMemsetAsync(w.hist, 0, topk_state_clear_bytes(rows), st);
     if (e != cudaSuccess) return e;
     e = pdl_launch(topk_hist_kernel, pgrid, dim3(kCThreads), 0, st, n, scores, w.hist);
     if (e != cudaSuccess) return e;
