@@ -196,15 +196,24 @@ __global__ void __launch_bounds__(T) attn_cluster_kernel(int64_t n, int64_t k, i
                                                          const void* __restrict__ q, int q_dtype,
                                                          const typename KS::Args ka, const KV* __restrict__ V,
                                                          const int32_t* __restrict__ idx, float* __restrict__ out,
-                                                         uint16_t* __restrict__ out_bf16) {
-  pdl_wait();  // the previous kernel on the stream has completed
-  pdl_trigger();
+                                                         uint16_t* __restrict__ out_bf16, bool q_ready) {
   using L = AttnSmem<G, T>;
   using R = Row4<KV>;
   constexpr int kWarps = T / 32;
   constexpr int U = KS::kQ4 ? 4 : attn_batch<G>();  // a 4-bit key holds 21 registers per lane until converted
   extern __shared__ float smem[];
   float* s_q = smem + L::q;
+  const float scale = 0.08838834764831845f;  // 1/sqrt(128)
+  auto load_q = [&] {
+    for (int i = threadIdx.x; i < G * kD; i += T)
+      s_q[i] = load_as_float(q, int64_t(blockIdx.y) * G * kD + i, q_dtype) * scale;
+  };
+  // q_ready: the queries were complete before the stream's previous kernel started (an input of
+  // the decode step), so they are read before the wait
+  if (q_ready) load_q();
+  pdl_wait();  // the previous kernel on the stream has completed
+  pdl_trigger();
+  if (!q_ready) load_q();
   cg::cluster_group cluster = cg::this_cluster();
   const int crank = int(cluster.block_rank());
   const int csize = int(cluster.num_blocks());
@@ -220,8 +229,6 @@ __global__ void __launch_bounds__(T) attn_cluster_kernel(int64_t n, int64_t k, i
   int64_t base = i0 + int64_t(warp) * U;
   // lane u < U holds the index of winner base + u (loaded one batch ahead)
   int32_t tl = (lane < U && base + lane < i1) ? __ldg(ir + base + lane) : -1;
-  const float scale = 0.08838834764831845f;  // 1/sqrt(128)
-  for (int i = tid; i < G * kD; i += T) s_q[i] = load_as_float(q, int64_t(r) * G * kD + i, q_dtype) * scale;
   __syncthreads();
   float4 qv[G];
 #pragma unroll
@@ -400,7 +407,7 @@ __global__ void __launch_bounds__(T) attn_cluster_kernel(int64_t n, int64_t k, i
 template <int G, typename KV, typename KS>
 cudaError_t launch_attn_t(int rows, int64_t n, int64_t k, const void* q, int q_dtype, const typename KS::Args& ka,
                           const void* V, int64_t stride, int kv_div, const int32_t* idx, float* out,
-                          uint16_t* out_bf16, cudaStream_t st, bool wide) {
+                          uint16_t* out_bf16, cudaStream_t st, bool wide, bool q_ready) {
   auto kern = attn_cluster_kernel<G, KV, KS>;
   constexpr int T = attn_threads_ks<G, KS>();
   constexpr size_t smem = AttnSmem<G, T>::bytes;
@@ -431,7 +438,7 @@ cudaError_t launch_attn_t(int rows, int64_t n, int64_t k, const void* q, int q_d
     cfg.attrs = attr;
     cfg.numAttrs = 2;
     const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, n, k, stride, kv_div, q, q_dtype, ka,
-                                             reinterpret_cast<const KV*>(V), idx, out, out_bf16);
+                                             reinterpret_cast<const KV*>(V), idx, out, out_bf16, q_ready);
     if (e == cudaSuccess || cluster == 8) return e;
     cudaGetLastError();  // the larger cluster could not be scheduled: use the portable size from now on
     cluster = cluster_max = 8;
@@ -442,18 +449,20 @@ cudaError_t launch_attn_t(int rows, int64_t n, int64_t k, const void* q, int q_d
 template <int G, template <typename> class KSel>
 cudaError_t launch_attn_g(int rows, int64_t n, int64_t k, const void* q, int q_dtype, const void* K,
                           const KeysQ4::Args* q4, const void* V, int kv_dtype, int64_t stride, const int32_t* idx,
-                          float* out, uint16_t* out_bf16, cudaStream_t st, int kv_div, bool wide) {
+                          float* out, uint16_t* out_bf16, cudaStream_t st, int kv_div, bool wide, bool q_ready) {
   if (kv_dtype == FATHOM_F32)
     return launch_attn_t<G, float, typename KSel<float>::type>(rows, n, k, q, q_dtype,
                                                                 KSel<float>::args(K, q4, n, stride), V, stride,
-                                                                kv_div, idx, out, out_bf16, st, wide);
+                                                                kv_div, idx, out, out_bf16, st, wide,
+                                                                q_ready);
   if (kv_dtype == FATHOM_F16)
     return launch_attn_t<G, __half, typename KSel<__half>::type>(rows, n, k, q, q_dtype,
                                                                   KSel<__half>::args(K, q4, n, stride), V, stride,
-                                                                  kv_div, idx, out, out_bf16, st, wide);
+                                                                  kv_div, idx, out, out_bf16, st, wide,
+                                                                q_ready);
   return launch_attn_t<G, __nv_bfloat16, typename KSel<__nv_bfloat16>::type>(
       rows, n, k, q, q_dtype, KSel<__nv_bfloat16>::args(K, q4, n, stride), V, stride, kv_div, idx, out, out_bf16,
-      st, wide);
+      st, wide, q_ready);
 }
 
 template <typename KV>
@@ -473,14 +482,14 @@ template <template <typename> class KSel>
 cudaError_t launch_attn_any(int rows, int group, int64_t n, int64_t k, const void* q, int q_dtype, const void* K,
                             const KeysQ4::Args* q4, const void* V, int kv_dtype, int64_t kv_stride,
                             const int32_t* idx, float* out, uint16_t* out_bf16, cudaStream_t st, bool per_head,
-                            bool wide) {
+                            bool wide, bool q_ready) {
   if (per_head)  // every query head is a row of its own over its KV row's K/V
     return launch_attn_g<1, KSel>(rows * group, n, k, q, q_dtype, K, q4, V, kv_dtype, kv_stride, idx, out, out_bf16,
-                                  st, group, wide);
+                                  st, group, wide, q_ready);
 #define FATHOM_ATTN_G(GG)                                                                                          \
   case GG:                                                                                                         \
     return launch_attn_g<GG, KSel>(rows, n, k, q, q_dtype, K, q4, V, kv_dtype, kv_stride, idx, out, out_bf16, st, 1, \
-                                   wide);
+                                   wide, q_ready);
   switch (group) {
     FATHOM_ATTN_G(1)
     FATHOM_ATTN_G(2)
@@ -513,18 +522,19 @@ size_t attn_ws_bytes(int, int, int64_t) { return 256; }
 
 cudaError_t launch_attn(int rows, int group, int64_t n, int64_t k, const void* q, int q_dtype, const void* K,
                         const void* V, int kv_dtype, int64_t kv_stride, const int32_t* idx, float* out,
-                        uint16_t* out_bf16, void* /*ws*/, cudaStream_t st, bool per_head) {
+                        uint16_t* out_bf16, void* /*ws*/, cudaStream_t st, bool per_head, bool q_ready) {
   return launch_attn_any<Sel16>(rows, group, n, k, q, q_dtype, K, nullptr, V, kv_dtype, kv_stride, idx, out,
-                                out_bf16, st, per_head, host_resident(K) || host_resident(V));
+                                out_bf16, st, per_head, host_resident(K) || host_resident(V), q_ready);
 }
 
 cudaError_t launch_attn_q4(const IndexGeom& g, int group, int64_t k, const void* q, int q_dtype,
                            const uint32_t* planes, const __half2* meta, const void* V, int v_dtype, int64_t v_stride,
-                           const int32_t* idx, float* out, uint16_t* out_bf16, cudaStream_t st, bool per_head) {
+                           const int32_t* idx, float* out, uint16_t* out_bf16, cudaStream_t st, bool per_head,
+                           bool q_ready) {
   // V rows, like the index, are `capacity` tokens long
   const KeysQ4::Args a{planes, meta, g.cap, g.nsb, g.nblk, g.log2S};
   return launch_attn_any<SelQ4>(g.rows, group, g.cap, k, q, q_dtype, nullptr, &a, V, v_dtype, v_stride, idx, out,
-                                out_bf16, st, per_head, host_resident(planes) || host_resident(V));
+                                out_bf16, st, per_head, host_resident(planes) || host_resident(V), q_ready);
 }
 
 }  // namespace fathom

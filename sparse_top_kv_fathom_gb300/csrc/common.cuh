@@ -170,14 +170,17 @@ cudaError_t launch_scan(const IndexGeom& g, const uint32_t* planes, const __half
 // filter's per-row hints (read, and rewritten for the next step), or NULL
 cudaError_t launch_topk(int rows, int64_t n, int64_t k, const float* scores, int32_t* idx, float* vals, void* ws,
                         bool hist_ready, cudaStream_t st, uint32_t* hint = nullptr);
-// per_head: idx holds one winner set per query head ([rows*group][k]), each head attends over its own
+// per_head: idx holds one winner set per query head ([rows*group][k]), each head attends over its own;
+// q_ready: q was complete before the stream's previous kernel started (a decode step's input), so
+// the kernel may read it before waiting on that kernel
 cudaError_t launch_attn(int rows, int group, int64_t n, int64_t k, const void* q, int q_dtype, const void* K,
-                        const void* V, int kv_dtype, int64_t kv_stride, const int32_t* idx, float* out, uint16_t* out_bf16, void* ws,
-                        cudaStream_t st, bool per_head = false);
+                        const void* V, int kv_dtype, int64_t kv_stride, const int32_t* idx, float* out,
+                        uint16_t* out_bf16, void* ws, cudaStream_t st, bool per_head = false, bool q_ready = false);
 // attention whose keys are read back from the bit-plane index (the unified 4-bit store)
 cudaError_t launch_attn_q4(const IndexGeom& g, int group, int64_t k, const void* q, int q_dtype,
                            const uint32_t* planes, const __half2* meta, const void* V, int v_dtype, int64_t v_stride,
-                           const int32_t* idx, float* out, uint16_t* out_bf16, cudaStream_t st, bool per_head = false);
+                           const int32_t* idx, float* out, uint16_t* out_bf16, cudaStream_t st, bool per_head = false,
+                           bool q_ready = false);
 cudaError_t launch_fixed136_scan(int rows, int64_t n, const int32_t* chans, const uint8_t* codes, const uint8_t* exps,
                                  const float* qbar, float* scores, uint32_t* hist, cudaStream_t st);
 

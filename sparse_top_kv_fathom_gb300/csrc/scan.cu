@@ -102,8 +102,6 @@ __global__ void __launch_bounds__(T, 512 / T) scan_kernel(const uint32_t* __rest
                                                                          uint32_t* __restrict__ hist, int64_t n,
                                                                          int64_t nsb, int log2S, int64_t nblk,
                                                                          const ScanTopk tk) {
-  pdl_wait();  // the previous kernel on the stream has completed
-  pdl_trigger();
   constexpr int W = ScanCfg<TOK>::kWords;
   constexpr int TT = T / P;  // threads of one channel group = token slots of the CTA
   static_assert(T % 32 == 0 && T >= 32 && T <= 512, "whole warps");
@@ -122,6 +120,12 @@ __global__ void __launch_bounds__(T, 512 / T) scan_kernel(const uint32_t* __rest
 
   const int r = blockIdx.y;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if constexpr (kHist) {  // shared memory only: before the wait
+    for (int i = tid; i < kHistBins; i += T) s_hist[i] = 0u;
+  }
+  if (tid == 0) s_fcnt = 0;
+  pdl_wait();  // the previous kernel on the stream has completed
+  pdl_trigger();
 
   // Active channels of this row, in channel order: warp w handles channel groups w, w + T/32, ...
   // of 32 channels (one group each when T = 128).
@@ -132,10 +136,6 @@ __global__ void __launch_bounds__(T, 512 / T) scan_kernel(const uint32_t* __rest
     const unsigned ball = __ballot_sync(0xffffffffu, dep > 0);
     if (lane == 0) s_wcnt[cg] = __popc(ball);
   }
-  if constexpr (kHist) {
-    for (int i = tid; i < kHistBins; i += T) s_hist[i] = 0u;
-  }
-  if (tid == 0) s_fcnt = 0;
   __syncthreads();
   int nact = 0;
 #pragma unroll

@@ -114,11 +114,11 @@ int fathom_decode_step(const fathom_step_desc* s, void* workspace, size_t ws_byt
     if (q4)
       FATHOM_TRY_CUDA(launch_attn_q4(g, s->group, s->k, dq, s->q_dtype, (const uint32_t*)dP, (const __half2*)dM, dV,
                                      s->kv_dtype, s->kv_stride, (const int32_t*)dI, (float*)dO, (uint16_t*)dB, st,
-                                     gqa == FATHOM_GQA_PER_HEAD));
+                                     gqa == FATHOM_GQA_PER_HEAD, true));
     else
       FATHOM_TRY_CUDA(launch_attn(g.rows, s->group, g.cap, s->k, dq, s->q_dtype, dK, dV, s->kv_dtype, s->kv_stride,
                                   (const int32_t*)dI, (float*)dO, (uint16_t*)dB, w.attn, st,
-                                  gqa == FATHOM_GQA_PER_HEAD));
+                                  gqa == FATHOM_GQA_PER_HEAD, true));
     return FATHOM_OK;
   }
   const bool use_hist = s->k < g.n;
@@ -143,10 +143,11 @@ int fathom_decode_step(const fathom_step_desc* s, void* workspace, size_t ws_byt
   FATHOM_TRY_CUDA(launch_topk(g.rows, g.n, s->k, w.scores, (int32_t*)dI, nullptr, w.topk, use_hist, st, hint));
   if (q4)
     FATHOM_TRY_CUDA(launch_attn_q4(g, s->group, s->k, dq, s->q_dtype, (const uint32_t*)dP, (const __half2*)dM, dV,
-                                   s->kv_dtype, s->kv_stride, (const int32_t*)dI, (float*)dO, (uint16_t*)dB, st));
+                                   s->kv_dtype, s->kv_stride, (const int32_t*)dI, (float*)dO, (uint16_t*)dB, st, false,
+                                   true));
   else
     FATHOM_TRY_CUDA(launch_attn(g.rows, s->group, g.cap, s->k, dq, s->q_dtype, dK, dV, s->kv_dtype, s->kv_stride,
-                                (const int32_t*)dI, (float*)dO, (uint16_t*)dB, w.attn, st));
+                                (const int32_t*)dI, (float*)dO, (uint16_t*)dB, w.attn, st, false, true));
   return FATHOM_OK;
 }
 
@@ -194,8 +195,8 @@ int fathom_fixed136_decode_step(const fathom_fixed136_step_desc* s, void* worksp
   FATHOM_TRY_CUDA(launch_fixed136_scan(s->rows, s->n, (const int32_t*)dC, (const uint8_t*)dX, (const uint8_t*)dE,
                                        w.qbar, w.scores, hist, st));
   FATHOM_TRY_CUDA(launch_topk(s->rows, s->n, s->k, w.scores, (int32_t*)dI, nullptr, w.topk, use_hist, st));
-  FATHOM_TRY_CUDA(launch_attn(s->rows, s->group, s->n, s->k, dq, s->q_dtype, dK, dV, s->kv_dtype, s->kv_stride, (const int32_t*)dI,
-                              (float*)dO, (uint16_t*)dB, w.attn, st));
+  FATHOM_TRY_CUDA(launch_attn(s->rows, s->group, s->n, s->k, dq, s->q_dtype, dK, dV, s->kv_dtype, s->kv_stride,
+                              (const int32_t*)dI, (float*)dO, (uint16_t*)dB, w.attn, st, false, true));
   return FATHOM_OK;
 }
 

@@ -481,8 +481,6 @@ __global__ void __launch_bounds__(kFinThreads) topk_final_kernel(int64_t n, int6
                                                                  const int32_t* __restrict__ cand_idx,
                                                                  int32_t* __restrict__ idx, float* __restrict__ vals,
                                                                  uint32_t* __restrict__ hint) {
-  pdl_wait();  // the previous kernel on the stream has completed
-  pdl_trigger();
   extern __shared__ int32_t s_dyn[];  // region A (sort buffer or bitmap), then kCandSmem keys and indices
   int32_t* s_sel = s_dyn;
   uint32_t* s_ck = reinterpret_cast<uint32_t*>(s_dyn + kRegionA);
@@ -492,18 +490,20 @@ __global__ void __launch_bounds__(kFinThreads) topk_final_kernel(int64_t n, int6
   __shared__ int s_fill;
   const int r = blockIdx.x;
   const int tid = threadIdx.x;
+  const int64_t words = (n + 31) >> 5;
+  if (words <= kBitmapWords) {  // clear the output bitmap (shared memory only: before the wait)
+    const int64_t words4 = (words + 3) >> 2;
+    for (int64_t i = tid; i < words4; i += kFinThreads)
+      reinterpret_cast<uint4*>(s_dyn)[i] = make_uint4(0u, 0u, 0u, 0u);
+  }
+  pdl_wait();  // the previous kernel on the stream has completed
+  pdl_trigger();
   // the row's first candidates and sure entries, loaded before its state (their counts) arrives:
   // one round trip to memory instead of two (entries past the counts are never used)
   const uint32_t pk = tid < cap ? cand_key[int64_t(r) * cap + tid] : 0u;
   const int32_t pi = tid < cap ? cand_idx[int64_t(r) * cap + tid] : 0;
   const int32_t ps0 = tid < k ? sure[int64_t(r) * k + tid] : -1;
   const int32_t ps1 = tid + kFinThreads < k ? sure[int64_t(r) * k + kFinThreads + tid] : -1;
-  const int64_t words = (n + 31) >> 5;
-  if (words <= kBitmapWords) {  // clear the output bitmap while those loads travel
-    const int64_t words4 = (words + 3) >> 2;
-    for (int64_t i = tid; i < words4; i += kFinThreads)
-      reinterpret_cast<uint4*>(s_dyn)[i] = make_uint4(0u, 0u, 0u, 0u);
-  }
   const RowState st = state[r];
   const float* s = scores + int64_t(r) * n;
   int32_t* oi = idx + int64_t(r) * k;
