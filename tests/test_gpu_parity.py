@@ -517,3 +517,21 @@ def test_scan_every_tile_shape(gpu_lib, tile, aligned):
     for _ in range(3):  # first step: every key listed; then the carried hints
         b = filt()
         assert torch.equal(idx, b[0]) and torch.equal(out, b[1])
+
+
+@pytest.mark.parametrize("hint", [False, True], ids=["plain", "filter"])
+def test_step_ignores_what_the_workspace_held(case, gpu_lib, hint):
+    """The step clears what it accumulates into (the top-k histogram and row states) itself:
+    a workspace full of stale bytes gives the same winners and outputs as a fresh one."""
+    F, w = gpu_lib, case["w"]
+    B, k = 92, min(w.k, w.n)
+    nbytes = F.DecodeStep.workspace_bytes(case["index"], k, w.group)
+    outs = []
+    for fill in (0, 0xFF, 0x5A):
+        ws = torch.full((nbytes,), fill, dtype=torch.uint8, device="cuda")
+        st = F.DecodeStep(case["index"], case["Kd"], case["Vd"], case["qd"], k, w.group, B, workspace=ws,
+                          hint=True if hint else None)
+        outs.append([t.clone() for t in st()])
+        outs.append([t.clone() for t in st()])  # and again over what the first call left
+    for o in outs[1:]:
+        assert torch.equal(outs[0][0], o[0]) and torch.equal(outs[0][1], o[1])
