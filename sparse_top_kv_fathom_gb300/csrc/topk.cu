@@ -30,7 +30,7 @@ constexpr int kCandSmem = 8192;   // candidates staged in shared memory by the f
 constexpr int kBitmapWords = 32768;  // n <= 2^20: the chosen indices leave the final select through a bitmap
 constexpr int kRegionA = kBitmapWords > kSortMax ? kBitmapWords : kSortMax;  // bitmap or sort buffer (words)
 constexpr int kCThreads = 256;  // threads of the histogram and candidate passes
-constexpr int kCTile = 8192;    // scores per CTA of those passes
+constexpr int kCTile = 8192;    // scores per CTA of those passes (the candidate pass halves it for short rows)
 constexpr int kCItems = kCTile / kCThreads;
 
 using RowState = TopkRowState;
@@ -121,17 +121,18 @@ __device__ __forceinline__ void warp_append(bool pred, int32_t* counter, int* sl
 }
 
 // ----------------------------------------------------------------- kernels ---
-// A thread's share of one tile of kCTile scores (histogram and candidate passes).
-template <bool kVec>
+// A thread's share of one tile of kItems * kCThreads scores (histogram and candidate passes).
+template <bool kVec, int kItems = kCItems>
 struct TileItems {
+  static constexpr int kTile = kItems * kCThreads;
   // position of a thread's item i inside the tile: float4 j = i/4 of the thread sits at j * threads + tid
   __device__ static int pos(int i, int tid) {
     return kVec ? 4 * ((i >> 2) * kCThreads + tid) + (i & 3) : i * kCThreads + tid;
   }
-  __device__ static void load(const float* __restrict__ s, int lim, int tid, float (&v)[kCItems]) {
-    if (kVec && lim == kCTile) {
+  __device__ static void load(const float* __restrict__ s, int lim, int tid, float (&v)[kItems]) {
+    if (kVec && lim == kTile) {
 #pragma unroll
-      for (int j = 0; j < kCItems / 4; ++j) {
+      for (int j = 0; j < kItems / 4; ++j) {
         const float4 x = __ldg(reinterpret_cast<const float4*>(s) + j * kCThreads + tid);
         v[4 * j] = x.x;
         v[4 * j + 1] = x.y;
@@ -140,7 +141,7 @@ struct TileItems {
       }
     } else {
 #pragma unroll
-      for (int i = 0; i < kCItems; ++i) {
+      for (int i = 0; i < kItems; ++i) {
         const int p = pos(i, tid);
         v[i] = p < lim ? __ldg(s + p) : 0.0f;
       }
@@ -239,13 +240,13 @@ __device__ __forceinline__ uint32_t score_key_fast(float v) {
 }
 
 // Candidate pass: keys in bins above b1 go to the row's sure list, keys in b1
-// to its candidate list.  One CTA per tile of kCTile scores of one row: every
-// thread loads its kCItems scores at once (the whole tile in flight), then the
+// to its candidate list.  One CTA per tile of kItems * kCThreads scores of one row:
+// every thread loads its kItems scores at once (the whole tile in flight), then the
 // row's state (bin b1; its load overlaps the tile's), marks its hits in two bit
 // masks, and a CTA-wide scan of the packed (sure, candidate) counts gives each
 // thread its slots after one reservation per list (thread 0's atomics on the
 // row's counters).  Rows the scan's filter already listed (fast) are skipped.
-template <bool kVec>
+template <bool kVec, int kItems>
 __global__ void __launch_bounds__(kCThreads) topk_compact_kernel(int64_t n, int64_t k, int64_t cap,
                                                                  const float* __restrict__ scores,
                                                                  RowState* __restrict__ state,
@@ -254,15 +255,15 @@ __global__ void __launch_bounds__(kCThreads) topk_compact_kernel(int64_t n, int6
                                                                  int32_t* __restrict__ cand_idx) {
   pdl_wait();  // the previous kernel on the stream has completed
   pdl_trigger();
-  using I = TileItems<kVec>;
-  static_assert(kCItems <= 32 && kCTile < 65536, "32-bit item masks, packed 16-bit counts");
+  using I = TileItems<kVec, kItems>;
+  static_assert(kItems <= 32 && I::kTile < 65536, "32-bit item masks, packed 16-bit counts");
   __shared__ uint32_t s_warp[kCThreads / 32];
   __shared__ int s_base[2];
   const int r = blockIdx.y, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   RowState* srow = state + r;
-  const int64_t t0 = int64_t(blockIdx.x) * kCTile;
-  const int lim = n - t0 < kCTile ? int(n - t0) : kCTile;  // items of this tile inside the row
-  float v[kCItems];
+  const int64_t t0 = int64_t(blockIdx.x) * I::kTile;
+  const int lim = n - t0 < I::kTile ? int(n - t0) : I::kTile;  // items of this tile inside the row
+  float v[kItems];
   I::load(scores + int64_t(r) * n + t0, lim, tid, v);
   const int32_t fast = __ldg(&srow->fast);
   const uint32_t b1 = __ldg(&srow->b1);
@@ -272,7 +273,7 @@ __global__ void __launch_bounds__(kCThreads) topk_compact_kernel(int64_t n, int6
   const uint32_t klo = b1 << (32 - kHistBits), khi = klo | kSpan;
   uint32_t ms = 0u, mc = 0u;  // bit i: this thread's item i is a sure winner / a candidate
 #pragma unroll
-  for (int i = 0; i < kCItems; ++i) {
+  for (int i = 0; i < kItems; ++i) {
     const uint32_t key = score_key_fast(v[i]);
     const uint32_t in = uint32_t(I::pos(i, tid) < lim);
     ms |= (uint32_t(key > khi) & in) << i;
@@ -307,7 +308,7 @@ __global__ void __launch_bounds__(kCThreads) topk_compact_kernel(int64_t n, int6
   int64_t pc = int64_t(s_base[1]) + (excl >> 16);
   const uint32_t hit = ms | mc;
 #pragma unroll
-  for (int i = 0; i < kCItems; ++i) {
+  for (int i = 0; i < kItems; ++i) {
     if (!((hit >> i) & 1u)) continue;
     const int32_t t = int32_t(t0 + I::pos(i, tid));
     if ((ms >> i) & 1u) {
@@ -704,9 +705,18 @@ cudaError_t launch_topk(int rows, int64_t n, int64_t k, const float* scores, int
   }
   e = pdl_launch(topk_bin_kernel, dim3(rows), dim3(kFinThreads), 0, st, k, w.cap, hint, w.hist, w.state);
   if (e != cudaSuccess) return e;
+  // candidate pass: half tiles when the rows give fewer tiles than SMs (more, shorter CTAs)
   const bool vec = n % 4 == 0 && (reinterpret_cast<uintptr_t>(scores) & 15) == 0;
-  e = pdl_launch(vec ? topk_compact_kernel<true> : topk_compact_kernel<false>, pgrid, dim3(kCThreads), 0, st, n, k,
-                 w.cap, scores, w.state, w.sure, w.cand_key, w.cand_idx);
+  if (tiles * rows < num_sms()) {
+    constexpr int kHalf = kCItems / 2;
+    const int64_t htiles = (n + kHalf * kCThreads - 1) / (kHalf * kCThreads);
+    e = pdl_launch(vec ? topk_compact_kernel<true, kHalf> : topk_compact_kernel<false, kHalf>,
+                   dim3(unsigned(htiles), unsigned(rows), 1u), dim3(kCThreads), 0, st, n, k, w.cap, scores, w.state,
+                   w.sure, w.cand_key, w.cand_idx);
+  } else {
+    e = pdl_launch(vec ? topk_compact_kernel<true, kCItems> : topk_compact_kernel<false, kCItems>, pgrid,
+                   dim3(kCThreads), 0, st, n, k, w.cap, scores, w.state, w.sure, w.cand_key, w.cand_idx);
+  }
   if (e != cudaSuccess) return e;
   const size_t smem = (kRegionA + 2 * kCandSmem) * sizeof(int32_t);
   static bool attr_set = false;
