@@ -58,7 +58,6 @@ def parse():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--layers", type=int, default=None, help="override layer count (smaller runs)")
     p.add_argument("--n", type=int, default=None, help="override tokens per row (smaller runs)")
-    p.add_argument("--profile", action="store_true", help="few launches, for ncu")
     p.add_argument("--filter", action="store_true",
                    help="time the step with the fused scan -> top-k filter (hints carried between steps)")
     return p.parse_args()

@@ -53,14 +53,26 @@ int device_view(const void* p, const char* name, const void** dev, bool nullable
   }
 }
 
+int current_device() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return dev;
+}
+
 int num_sms() {
-  static int sms = 0;
+  // cached per device (the launch shapes follow the SM count of the device in use)
+  static std::atomic<int> cache[kMaxDevices];
+  const int dev = current_device();
+  int sms = dev < kMaxDevices ? cache[dev].load(std::memory_order_relaxed) : 0;
   if (sms == 0) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1) {
       cudaGetLastError();
-      sms = 148;
+      return 1;  // any shape is correct; the launch that follows reports the device's error
     }
+    if (dev < kMaxDevices) cache[dev].store(sms, std::memory_order_relaxed);
   }
   return sms;
 }

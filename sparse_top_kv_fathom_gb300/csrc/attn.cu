@@ -411,8 +411,10 @@ cudaError_t launch_attn_t(int rows, int64_t n, int64_t k, const void* q, int q_d
   auto kern = attn_cluster_kernel<G, KV, KS>;
   constexpr int T = attn_threads_ks<G, KS>();
   constexpr size_t smem = AttnSmem<G, T>::bytes;
-  // 16-CTA clusters need an opt-in per kernel; fall back to the portable 8 if it is refused
-  static int cluster_max = 0;
+  // 16-CTA clusters need an opt-in per kernel and device; fall back to the portable 8 if it is refused
+  static std::atomic<int> cluster_max_dev[kMaxDevices];  // 0: the device's attributes are not set yet
+  const int dev = current_device();
+  int cluster_max = dev < kMaxDevices ? cluster_max_dev[dev].load(std::memory_order_relaxed) : 0;
   if (cluster_max == 0) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
     if (e != cudaSuccess) return e;
@@ -420,6 +422,7 @@ cudaError_t launch_attn_t(int rows, int64_t n, int64_t k, const void* q, int q_d
                       ? kClusterMax
                       : 8;
     cudaGetLastError();
+    if (dev < kMaxDevices) cluster_max_dev[dev].store(cluster_max, std::memory_order_relaxed);
   }
   int cluster = wide ? cluster_max : 8;
   for (;;) {
@@ -441,7 +444,8 @@ cudaError_t launch_attn_t(int rows, int64_t n, int64_t k, const void* q, int q_d
                                              reinterpret_cast<const KV*>(V), idx, out, out_bf16, q_ready);
     if (e == cudaSuccess || cluster == 8) return e;
     cudaGetLastError();  // the larger cluster could not be scheduled: use the portable size from now on
-    cluster = cluster_max = 8;
+    cluster = 8;
+    if (dev < kMaxDevices) cluster_max_dev[dev].store(8, std::memory_order_relaxed);
   }
 }
 

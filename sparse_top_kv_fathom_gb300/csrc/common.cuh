@@ -6,6 +6,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
 #include <string>
 #include <utility>
 
@@ -40,6 +41,8 @@ int device_view(const void* p, const char* name, const void** dev, bool nullable
 inline cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
 
 int num_sms();
+int current_device();
+constexpr int kMaxDevices = 64;  // devices whose per-device launch settings are cached
 
 // ------------------------------------------- programmatic dependent launch ---
 // The step's kernels are launched with programmatic stream serialisation: a kernel may be

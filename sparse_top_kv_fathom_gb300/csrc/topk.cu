@@ -719,11 +719,12 @@ cudaError_t launch_topk(int rows, int64_t n, int64_t k, const float* scores, int
   }
   if (e != cudaSuccess) return e;
   const size_t smem = (kRegionA + 2 * kCandSmem) * sizeof(int32_t);
-  static bool attr_set = false;
-  if (!attr_set) {
+  static std::atomic<bool> attr_set[kMaxDevices];  // the final kernel's shared-memory opt-in, per device
+  const int dev = current_device();
+  if (dev >= kMaxDevices || !attr_set[dev].load(std::memory_order_relaxed)) {
     e = cudaFuncSetAttribute(topk_final_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
     if (e != cudaSuccess) return e;
-    attr_set = true;
+    if (dev < kMaxDevices) attr_set[dev].store(true, std::memory_order_relaxed);
   }
   return pdl_launch(topk_final_kernel, dim3(rows), dim3(kFinThreads), smem, st, n, k, w.cap, scores, w.state, w.sure,
                     w.cand_key, w.cand_idx, idx, vals, hint);
