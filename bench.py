@@ -481,6 +481,12 @@ def cpu_baseline(model, store, log, seconds=(10.0, 30.0)):
                       "heads of layer 0 at n=%d, B=%d, k=%d; %.1f s" % (reps, rows, w.n, model.budget, w.k, t)}
 
 
+def metric_name(w, budget):
+    """The benchmark's metric, the same string on both arms."""
+    return ("scan keys/s and decode-step ms at n=%d, B=%d (%d-layer step); GB/s vs HBM / host-link peak"
+            % (w.n, budget, w.layers))
+
+
 def run_reference(args, log):
     """CPU oracle as the reference arm: each step = the oracle's decode step over a bounded row sample."""
     import oracle
@@ -503,12 +509,13 @@ def run_reference(args, log):
             times.append(time.time() - t0)
     per = statistics.mean(times)
     value = rows * w.n / per
-    return {"impl": "reference", "metric": "decode-step scan throughput (keys/s) at n=%d, B=%d" % (w.n, args.budget),
+    return {"impl": "reference", "metric": metric_name(w, args.budget),
             "value": value, "unit": "keys/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": per * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "f64", "data": "synthetic",
             "config": {"workload": w.name, "layers": w.layers, "kv_heads": w.kv_heads, "group": w.group, "n": w.n,
-                       "budget": args.budget, "k": w.k, "sample_rows": rows},
+                       "budget": args.budget, "k": w.k, "superblock": args.superblock,
+                       "residency": "host memory (the CPU oracle)", "sample_rows": rows},
             "cpu_baseline": {"value": value, "unit": "keys/s", "cores": oracle.num_threads(), "kind": "oracle",
                              "sample": "each step: the oracle decode step on the %d KV heads of layer 0 at full n"
                                        % rows},
@@ -639,8 +646,7 @@ def main():
     p = result[primary]
     scan_peak = link_gbs if primary == "host" else hbm_peak
     line = {
-        "metric": "scan keys/s and decode-step ms at n=%d, B=%d (36-layer step); GB/s vs HBM / host-link peak"
-                  % (w.n, args.budget),
+        "metric": metric_name(w, args.budget),
         "value": p["keys_per_s"], "unit": "keys/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": p["ms_per_step"], "ms_per_step_median": statistics.median(p["per_step_ms"]),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
