@@ -4,7 +4,9 @@
 // relevance; "The first fix": attend over just the k winners).  Every query
 // head of a KV head uses its own q with that KV head's winner set.
 //
-// GPU form: one thread-block cluster of 16 (or the portable 8) CTAs per KV head.  Each CTA
+// GPU form: one thread-block cluster per KV head, of 8 CTAs when the K/V rows sit
+// in HBM (every KV head's cluster starts at once) and of 16 when they are read over
+// the host link (more rows in flight for the address translations).  Each CTA
 // takes a slice of the winners; each warp gathers whole K and V rows (a lane
 // holds 4 channels: 8 contiguous bytes of a 16-bit row) for a batch of 8
 // winners at once, the indices of the next batch loaded while this one is

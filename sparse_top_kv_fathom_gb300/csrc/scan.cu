@@ -27,7 +27,10 @@
 //   * x = fma(16*delta, 1 + u/16, lo + delta*((m-1)/2 - 16)) = lo + delta*(u +
 //     (m-1)/2) with a single rounding, then acc += qbar * x; both FMAs run on
 //     two tokens at a time (packed f32x2), so each term carries only a few ulps
-//     of |qbar_c * x_c| of error.
+//     of |qbar_c * x_c| of error;
+//   * short rows get smaller tiles (4096 or 2048 tokens per CTA) whose warps
+//     split the walk over the row's active channels into 2 or 4 groups, so the
+//     launch still has several CTAs per SM.
 // Inside the decode step the kernel also builds the 12-bit first-digit
 // histogram of its scores for the top-k, and, with the step's fused filter,
 // lists every key at or above the row's hint (the previous step's k-th key,

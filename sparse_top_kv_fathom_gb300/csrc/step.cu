@@ -1,11 +1,12 @@
 // fathom_decode_step and fathom_fixed136_decode_step: one decode step over a
 // set of independent rows (Rootconf proposal, summary: the index scan ranks
 // all n keys to pick the top k, then attention runs over the selected rows).
-// The steps are enqueued back to back on the caller's stream; scores, depths,
-// the top-k state and the attention partials live in the caller's workspace.
-// The scan also builds the first radix digit's histogram for the top-k, so
-// the scores are read only twice more (candidate pass, then the small final
-// select) before attention.
+// The steps are enqueued back to back on the caller's stream (programmatic
+// dependent launches: each kernel may be scheduled while its predecessor drains);
+// scores, depths and the top-k state live in the caller's workspace, whose
+// accumulators the allocation kernel clears.  The scan also builds the first
+// radix digit's histogram for the top-k, so the scores are read once more (the
+// candidate pass) before the final select works on the candidates alone.
 #include "common.cuh"
 
 namespace fathom {
