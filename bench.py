@@ -349,12 +349,26 @@ SCAN_SOURCES = [os.path.join(ROOT, "sparse_top_kv_fathom_gb300", "csrc", f) for 
 TRAFFIC_RECORD = os.path.join(ROOT, "profiles", "scan_kernel_traffic.json")
 
 
+def code_tokens(text):
+    """Source text without // comments and with whitespace collapsed: the code the compiler sees
+    (a comment edit leaves the recorded counters valid)."""
+    lines = []
+    for line in text.splitlines():
+        i = line.find("//")
+        if i >= 0:
+            line = line[:i]
+        line = " ".join(line.split())
+        if line:
+            lines.append(line)
+    return "\n".join(lines)
+
+
 def scan_source_hash():
-    """sha256 over the scan kernel's sources (scan.cu, then bitplane.cuh)."""
+    """sha256 over the scan kernel's code (scan.cu, then bitplane.cuh; comments and layout ignored)."""
     import hashlib
     h = hashlib.sha256()
     for f in SCAN_SOURCES:
-        h.update(open(f, "rb").read())
+        h.update(code_tokens(open(f).read()).encode())
     return h.hexdigest()
 
 
