@@ -364,9 +364,10 @@ cudaError_t launch_scan_t(const IndexGeom& g, const uint32_t* planes, const __ha
 
 cudaError_t launch_scan(const IndexGeom& g, const uint32_t* planes, const __half2* meta, const uint8_t* bits,
                         const float* qbar, float* scores, uint32_t* hist, cudaStream_t st, const ScanTopk* tk) {
-  // Tokens per CTA: 8192, halved (down to 1024) while the rows give fewer than four CTAs per SM;
-  // a smaller tile splits the CTA's walk over the row's active channels into 2 or 4 groups.
-  const int64_t want = 4 * int64_t(num_sms());
+  // Tokens per CTA: 8192, halved (down to 1024) while the rows give fewer than two CTAs per SM;
+  // a smaller tile splits the CTA's walk over the row's active channels into 2 or 4 groups
+  // (each CTA also flushes a histogram in the decode step, so fewer, fuller CTAs pay off).
+  const int64_t want = 2 * int64_t(num_sms());
   int64_t tile = kScanTile;
   while (tile > 1024 && ((g.n + tile - 1) / tile) * g.rows < want) tile >>= 1;
   // two plane words per thread need 8-byte aligned planes (every run of S >= 128 tokens is)

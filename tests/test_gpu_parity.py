@@ -479,10 +479,10 @@ def test_fused_filter_gives_the_same_steps(case, gpu_lib):
 
 def _tile_case_n(t, rows):
     """A row length for which the scan's launch takes t tokens per CTA: the tile halves from
-    8192 while the rows give fewer than four CTAs per SM, so 4 * SMs * t tokens over all rows
+    8192 while the rows give fewer than two CTAs per SM, so 2 * SMs * t tokens over all rows
     (plus a ragged tail) stop it exactly at t."""
     sms = torch.cuda.get_device_properties(0).multi_processor_count
-    return 4 * sms * t // rows + 77
+    return 2 * sms * t // rows + 77
 
 
 @pytest.mark.parametrize("aligned", [True, False], ids=["planes8B", "planes4B"])
