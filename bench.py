@@ -139,18 +139,22 @@ class Model:
         self.h = {}
         self.d = {}
         kvrows = KL * H
-        for store, empty in ((self.h, F.host_empty),
-                             (self.d, lambda shape, dtype: torch.empty(shape, dtype=dtype, device=dev))):
+        # host residency: the streamed index in pinned memory (cudaHostAlloc), the randomly gathered
+        # K/V rows in fathom_host_alloc memory (mapped by the GPU's own page tables: no stalls when
+        # the host's page tables change)
+        pinned = lambda shape, dtype: torch.empty(shape, dtype=dtype, pin_memory=True)
+        on_dev = lambda shape, dtype: torch.empty(shape, dtype=dtype, device=dev)
+        for store, stream_mem, gather_mem in ((self.h, pinned, F.host_empty), (self.d, on_dev, on_dev)):
             if (store is self.h and not host) or (store is self.d and not devr):
                 continue
-            store["planes"] = empty(ps, torch.int32)
-            store["meta"] = empty(ms, torch.float16)
+            store["planes"] = stream_mem(ps, torch.int32)
+            store["meta"] = stream_mem(ms, torch.float16)
             # K and V of a token side by side: one 512-byte row per winner
-            store["KV"] = empty((kvrows, n, 2, D), w.kv_dtype)
+            store["KV"] = gather_mem((kvrows, n, 2, D), w.kv_dtype)
             store["K"], store["V"] = store["KV"][:, :, 0, :], store["KV"][:, :, 1, :]
             if comparator:
-                store["codes"] = empty((rows, n, 16), torch.uint8)
-                store["exps"] = empty((rows, n), torch.uint8)
+                store["codes"] = stream_mem((rows, n, 16), torch.uint8)
+                store["exps"] = stream_mem((rows, n), torch.uint8)
         log("allocated buffers in %.1f s" % (time.time() - t0))
         self.var = torch.empty((rows, D), dtype=torch.float32, device=dev)
         self.chans = torch.empty((rows, 32), dtype=torch.int32, device=dev)

@@ -384,17 +384,23 @@ int fathom_fixed136_decode_step(const fathom_fixed136_step_desc* step, void* wor
  * With the cache in host memory, the index scan and the winner gathers cross
  * the host link ([A] "Where the memory lives changes the answer"; [R] "What
  * made it difficult": gathers of 4 KB runs reach the link rate).  The scan
- * streams at the link rate from any pinned memory, but the winner gathers are
- * random rows, and their rate is bounded by address translation: memory
- * backed by transparent huge pages translates several times fewer pages per
- * gathered row than 64 KB-page pinned memory.
+ * streams at the link rate from ordinary pinned memory (cudaHostAlloc).  The
+ * winner gathers are random rows: their rate is bounded by address
+ * translation, and memory the host kernel may remap (registered pageable
+ * memory) stalls them whenever the host's page tables change.
  *
- * fathom_host_alloc: `bytes` (> 0) of page-aligned host memory, anonymous,
- * advised for transparent huge pages, touched, and registered with CUDA
- * (mapped, portable) so that kernels read it over the host link.  *ptr is
- * both the host and the device address.  The library keeps no record of it;
- * release it with fathom_host_free(ptr, bytes) (same size).  ENOMEM if the
- * mapping or the registration fails.  Host-only work plus one CUDA call. */
+ * fathom_host_alloc: `bytes` (> 0) of pinned host memory for randomly gathered
+ * rows (K/V).  It is created through CUDA's virtual-memory API with a host
+ * location (the device's nearest NUMA node), so the GPU reaches it through its
+ * own page tables at the allocation granularity (2 MB on GB300), independent of
+ * the host process's page tables; both the host and the device may access it,
+ * and *ptr is both addresses.  The contents are zero.  Where that API is
+ * unavailable, an anonymous mapping advised for transparent huge pages,
+ * touched and registered with CUDA is returned instead.  Streamed data (the
+ * index) is better placed in cudaHostAlloc memory: the virtual-memory
+ * allocation streams at under half the link rate.  Release with
+ * fathom_host_free(ptr, bytes) (same size); the library records each block.
+ * ENOMEM if the allocation fails.  Host-only work plus a few CUDA calls. */
 int fathom_host_alloc(size_t bytes, void** ptr);
 int fathom_host_free(void* ptr, size_t bytes);
 

@@ -407,8 +407,10 @@ class _HostBlock:
 
 
 def host_empty(shape, dtype):
-    """A CPU tensor in pinned, transparent-huge-page host memory (fathom_host_alloc),
-    readable by the kernels over the host link.  Contents are zero."""
+    """A CPU tensor in fathom_host_alloc memory: pinned host memory that the GPU maps with its
+    own page tables (2 MB pages), for rows the kernels gather at random over the host link
+    (K/V).  Contents are zero.  Streamed data (the index) is better in ordinary pinned memory
+    (`torch.empty(..., pin_memory=True)`, as `BitPlaneIndex.to_host` does)."""
     numel = 1
     for x in shape:
         numel *= int(x)

@@ -1,11 +1,146 @@
-// Pinned host memory backed by transparent huge pages, for host-resident
-// index and K/V stores (fathom_host_alloc / fathom_host_free).
+// Pinned host memory for host-resident K/V rows (fathom_host_alloc / fathom_host_free).
+//
+// The decode step gathers the winners' K/V rows at random.  In host memory that
+// registered with cudaHostRegister the gathers stall, for tens to hundreds of
+// milliseconds at a time, whenever the host kernel changes the process's page
+// tables (periodically, about every 0.5 s, on these machines).  Memory created
+// through CUDA's virtual-memory API with a host location is mapped by the GPU's
+// own page tables at 2 MB granularity and does not stall.  The driver entry points
+// are resolved at run time (no link-time dependency on the driver library); if
+// they are missing, or the allocation is refused, an anonymous mapping advised
+// for transparent huge pages and registered with CUDA is used instead.
+#include <cuda.h>
 #include <string.h>
 #include <sys/mman.h>
+
+#include <mutex>
+#include <unordered_map>
 
 #include "common.cuh"
 
 using namespace fathom;
+
+namespace {
+
+struct Vmm {
+  decltype(&cuMemCreate) create = nullptr;
+  decltype(&cuMemAddressReserve) reserve = nullptr;
+  decltype(&cuMemMap) map = nullptr;
+  decltype(&cuMemSetAccess) access = nullptr;
+  decltype(&cuMemGetAllocationGranularity) granularity = nullptr;
+  decltype(&cuMemUnmap) unmap = nullptr;
+  decltype(&cuMemAddressFree) address_free = nullptr;
+  decltype(&cuMemRelease) release = nullptr;
+  bool ok = false;
+};
+
+template <typename Fn>
+bool driver_symbol(const char* name, Fn* fn) {
+  cudaDriverEntryPointQueryResult q;
+  void* p = nullptr;
+  if (cudaGetDriverEntryPointByVersion(name, &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess || !p) {
+    cudaGetLastError();
+    return false;
+  }
+  *fn = reinterpret_cast<Fn>(p);
+  return true;
+}
+
+Vmm& vmm() {
+  static Vmm v = [] {
+    Vmm a;
+    a.ok = driver_symbol("cuMemCreate", &a.create) && driver_symbol("cuMemAddressReserve", &a.reserve) &&
+           driver_symbol("cuMemMap", &a.map) && driver_symbol("cuMemSetAccess", &a.access) &&
+           driver_symbol("cuMemGetAllocationGranularity", &a.granularity) &&
+           driver_symbol("cuMemUnmap", &a.unmap) && driver_symbol("cuMemAddressFree", &a.address_free) &&
+           driver_symbol("cuMemRelease", &a.release);
+    return a;
+  }();
+  return v;
+}
+
+struct Block {
+  bool vmm;                        // virtual-memory allocation, else a registered mapping
+  CUmemGenericAllocationHandle h;  // (vmm)
+  size_t size;                     // bytes reserved / mapped
+};
+std::mutex g_mu;
+std::unordered_map<uintptr_t, Block> g_blocks;
+
+void remember(void* p, const Block& b) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  g_blocks[reinterpret_cast<uintptr_t>(p)] = b;
+}
+
+// CUDA virtual memory with a host location, readable and writable by the device and the host.
+// Returns nullptr (nothing held) if any step is refused.
+void* vmm_alloc(size_t bytes, Block* b) {
+  Vmm& v = vmm();
+  if (!v.ok) return nullptr;
+  const int dev = current_device();
+  int numa = -1;
+  if (cudaDeviceGetAttribute(&numa, cudaDevAttrHostNumaId, dev) != cudaSuccess) {
+    cudaGetLastError();
+    numa = -1;
+  }
+  CUmemAllocationProp prop{};
+  prop.type = CU_MEM_ALLOCATION_TYPE_PINNED;
+  prop.location.type = numa >= 0 ? CU_MEM_LOCATION_TYPE_HOST_NUMA : CU_MEM_LOCATION_TYPE_HOST;
+  prop.location.id = numa >= 0 ? numa : 0;
+  size_t gran = 0;
+  if (v.granularity(&gran, &prop, CU_MEM_ALLOC_GRANULARITY_RECOMMENDED) != CUDA_SUCCESS || gran == 0) return nullptr;
+  const size_t size = (bytes + gran - 1) / gran * gran;
+  CUmemGenericAllocationHandle h;
+  if (v.create(&h, size, &prop, 0) != CUDA_SUCCESS) return nullptr;
+  CUdeviceptr va = 0;
+  if (v.reserve(&va, size, gran, 0, 0) != CUDA_SUCCESS) {
+    v.release(h);
+    return nullptr;
+  }
+  if (v.map(va, size, 0, h, 0) != CUDA_SUCCESS) {
+    v.address_free(va, size);
+    v.release(h);
+    return nullptr;
+  }
+  CUmemAccessDesc acc[2] = {};
+  acc[0].location.type = CU_MEM_LOCATION_TYPE_DEVICE;
+  acc[0].location.id = dev;
+  acc[0].flags = CU_MEM_ACCESS_FLAGS_PROT_READWRITE;
+  acc[1].location = prop.location;
+  acc[1].flags = CU_MEM_ACCESS_FLAGS_PROT_READWRITE;
+  if (v.access(va, size, acc, 2) != CUDA_SUCCESS) {
+    v.unmap(va, size);
+    v.address_free(va, size);
+    v.release(h);
+    return nullptr;
+  }
+  *b = Block{true, h, size};
+  return reinterpret_cast<void*>(va);
+}
+
+void* registered_alloc(size_t bytes, Block* b, int* err) {
+  void* p = mmap(nullptr, bytes, PROT_READ | PROT_WRITE, MAP_PRIVATE | MAP_ANONYMOUS, -1, 0);
+  if (p == MAP_FAILED) {
+    *err = set_error(FATHOM_ENOMEM, "mmap of %zu bytes failed", bytes);
+    return nullptr;
+  }
+#ifdef MADV_HUGEPAGE
+  madvise(p, bytes, MADV_HUGEPAGE);  // advisory: without THP the memory is still usable
+#endif
+  memset(p, 0, bytes);  // populate before registration
+  const cudaError_t e = cudaHostRegister(p, bytes, cudaHostRegisterMapped | cudaHostRegisterPortable);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    munmap(p, bytes);
+    *err = set_error(FATHOM_ENOMEM, "cudaHostRegister of %zu bytes failed: %s", bytes, cudaGetErrorString(e));
+    return nullptr;
+  }
+  *b = Block{false, CUmemGenericAllocationHandle{}, bytes};
+  return p;
+}
+
+}  // namespace
 
 extern "C" {
 
@@ -13,18 +148,20 @@ int fathom_host_alloc(size_t bytes, void** ptr) {
   clear_error();
   if (!ptr || bytes == 0) return set_error(FATHOM_EINVAL, "bytes must be > 0 and ptr non-NULL");
   *ptr = nullptr;
-  void* p = mmap(nullptr, bytes, PROT_READ | PROT_WRITE, MAP_PRIVATE | MAP_ANONYMOUS, -1, 0);
-  if (p == MAP_FAILED) return set_error(FATHOM_ENOMEM, "mmap of %zu bytes failed", bytes);
-#ifdef MADV_HUGEPAGE
-  madvise(p, bytes, MADV_HUGEPAGE);  // advisory: without THP the memory is still usable
-#endif
-  memset(p, 0, bytes);  // populate before registration
-  cudaError_t e = cudaHostRegister(p, bytes, cudaHostRegisterMapped | cudaHostRegisterPortable);
-  if (e != cudaSuccess) {
+  if (cudaFree(nullptr) != cudaSuccess) {  // the runtime's context, current for the driver calls
     cudaGetLastError();
-    munmap(p, bytes);
-    return set_error(FATHOM_ENOMEM, "cudaHostRegister of %zu bytes failed: %s", bytes, cudaGetErrorString(e));
+    return set_error(FATHOM_ECUDA, "no CUDA device");
   }
+  Block b{};
+  void* p = vmm_alloc(bytes, &b);
+  if (p) {
+    memset(p, 0, b.size);
+  } else {
+    int err = FATHOM_OK;
+    p = registered_alloc(bytes, &b, &err);
+    if (!p) return err;
+  }
+  remember(p, b);
   *ptr = p;
   return FATHOM_OK;
 }
@@ -32,8 +169,23 @@ int fathom_host_alloc(size_t bytes, void** ptr) {
 int fathom_host_free(void* ptr, size_t bytes) {
   clear_error();
   if (!ptr || bytes == 0) return set_error(FATHOM_EINVAL, "ptr and bytes required");
-  cudaError_t e = cudaHostUnregister(ptr);
-  const int rc = munmap(ptr, bytes);
+  Block b;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    auto it = g_blocks.find(reinterpret_cast<uintptr_t>(ptr));
+    if (it == g_blocks.end()) return set_error(FATHOM_EINVAL, "not a block of fathom_host_alloc");
+    b = it->second;
+    g_blocks.erase(it);
+  }
+  if (b.vmm) {
+    Vmm& v = vmm();
+    const CUdeviceptr va = reinterpret_cast<CUdeviceptr>(ptr);
+    const bool ok = v.unmap(va, b.size) == CUDA_SUCCESS && v.address_free(va, b.size) == CUDA_SUCCESS &&
+                    v.release(b.h) == CUDA_SUCCESS;
+    return ok ? FATHOM_OK : set_error(FATHOM_ECUDA, "releasing a virtual-memory block failed");
+  }
+  const cudaError_t e = cudaHostUnregister(ptr);
+  const int rc = munmap(ptr, b.size);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return set_error(FATHOM_ECUDA, "cudaHostUnregister: %s", cudaGetErrorString(e));

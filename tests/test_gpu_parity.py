@@ -155,7 +155,7 @@ def test_decode_step_host_resident_kv_and_index(case, gpu_lib):
     same_attention(a[1], b[1])
 
 
-def test_interleaved_kv_in_huge_page_host_memory(case, gpu_lib):
+def test_interleaved_kv_in_host_alloc_memory(case, gpu_lib):
     """K and V interleaved per token (row stride 256) in fathom_host_alloc memory, index too:
     same winners and outputs as the dense device-resident step."""
     F, w = gpu_lib, case["w"]
