@@ -718,7 +718,7 @@ def main():
             line["hbm_resident"]["sparq"] = result["device"].get("sparq")
             line["hbm_resident"]["unified_store"] = result["device"].get("unified_store")
             line["hbm_resident"]["fused_filter"] = result["device"].get("fused_filter")
-    if rank == 0 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:  # the CPU baseline is an N = 1 figure
         line["cpu_baseline"] = cpu_baseline(model, model.h if model.h else model.d, log)
     if rank == 0:
         print(json.dumps(line), flush=True)
