@@ -499,6 +499,29 @@ def cpu_baseline(model, store, log, seconds=(10.0, 30.0)):
                       "heads of layer 0 at n=%d, B=%d, k=%d; %.1f s" % (reps, rows, w.n, model.budget, w.k, t)}
 
 
+def host_kv_layers(w, args, comparator, log):
+    """Distinct K/V layers to store (at most --kv-layers): with the cache in host memory every
+    process on the machine holds its own copy, so the count shrinks to what fits in this
+    process's share of the available host memory (the index, always complete, comes first)."""
+    if args.residency not in ("host", "both"):
+        return args.kv_layers
+    try:
+        avail = next(int(l.split()[1]) * 1024 for l in open("/proc/meminfo") if l.startswith("MemAvailable:"))
+    except (OSError, StopIteration, ValueError):
+        return args.kv_layers
+    local = int(os.environ.get("LOCAL_WORLD_SIZE", os.environ.get("WORLD_SIZE", "1")))
+    share = 0.85 * avail / max(local, 1)
+    D = 128
+    fixed = w.rows * w.n * (64 + 4)  # the index: 4-bit planes and block meta of every layer
+    fixed += (w.rows * w.n * 17 if comparator else 0) + (4 << 30)  # the 136-bit store, the link probe
+    per_layer = w.kv_heads * w.n * 2 * D * torch.empty((), dtype=w.kv_dtype).element_size()
+    fit = int((share - fixed) // per_layer)
+    kl = max(1, min(args.kv_layers, w.layers, fit))
+    if kl < min(args.kv_layers, w.layers):
+        log("host memory: %.0f GB available for %d process(es): storing %d distinct K/V layers" % (avail / 1e9, local, kl))
+    return kl
+
+
 def metric_name(w, budget):
     """The benchmark's metric, the same string on both arms."""
     return ("scan keys/s and decode-step ms at n=%d, B=%d (%d-layer step); GB/s vs HBM / host-link peak"
@@ -575,7 +598,8 @@ def main():
     import sparse_top_kv_fathom_gb300 as FF
     int_ops = FF.probe_int_ops()
     log("integer ALU rate: %.2f T ops/s" % (int_ops / 1e12))
-    model = Model(w, args.budget, args.superblock, args.residency, comparator, log, args.kv_layers)
+    kv_layers = host_kv_layers(w, args, comparator, log)
+    model = Model(w, args.budget, args.superblock, args.residency, comparator, log, kv_layers)
     stream = torch.cuda.Stream()
     keys_per_step = w.rows * w.n
     result = {}
