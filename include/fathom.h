@@ -293,7 +293,13 @@ int fathom_sparse_attn_q4(const fathom_index_desc* desc, int group, int64_t k, c
 /* One decode step over `index.rows` rows: allocate -> scan -> top-k ->
  * sparse attention ([R] summary: the index scan ranks all n keys to choose
  * the top k; the selected rows are attended).  Same definitions as the
- * individual calls; scores and bits are kept in the workspace. */
+ * individual calls; scores and bits are kept in the workspace, whose contents
+ * on entry do not matter (the step clears what it accumulates into).  The
+ * kernels are enqueued on `stream` with programmatic dependent launch: each may
+ * be scheduled while the one before it drains, and waits for it before touching
+ * memory.  q must be complete when the call's work starts on the stream (as
+ * for any stream-ordered input); the attention may read it before the top-k
+ * has finished. */
 typedef struct fathom_step_desc {
   fathom_index_desc index;
   int32_t group;            /* query heads per KV head, 1..8 */
