@@ -2,8 +2,9 @@
 """Benchmark of the Fathom decode step on one GB300.
 
 Workload (default "million"): 36 layers x 8 KV heads x 128 dims, 32 query heads
-(GQA 4), n = 2^20 tokens, bit-plane index and bf16 K/V in pinned host memory
-read over the host link, B = 92 bits per token, k = 2048 winners per KV head.
+(GQA 4), n = 2^20 tokens, the bit-plane index in pinned host memory and the bf16
+K/V rows in fathom_host_alloc memory, both read over the host link, B = 92 bits
+per token, k = 2048 winners per KV head.
 A step is one decode step of the whole model: for each of the 36 layers in
 order, allocate -> scan -> top-k -> sparse attention (the layers run in
 sequence as in a real decode step), captured once as a CUDA graph.
@@ -21,7 +22,8 @@ Reported (one JSON line):
   cpu_baseline the CPU oracle on a bounded sample of rows, on the host cores
 
 --impl reference times the CPU oracle (the only "reference" in this repository:
-the pages ship no runnable code) on a bounded row sample of the same workload.
+the Fathom article and proposal ship no runnable code) on a bounded row sample
+of the same workload.
 """
 import argparse
 import json
@@ -425,7 +427,7 @@ def captured_issue_rate(residency, w, budget, ms_per_launch):
 
 
 def machine_balance(int_ops, hbm_gbs, link_gbs, w, budget):
-    """Integer ALU operations per byte of bandwidth (the pages' argument that a scan is
+    """Integer ALU operations per byte of bandwidth (the Fathom article's argument that a scan is
     arithmetic-bound wherever ops per byte fall short of what it needs), beside what the scan
     needs: its ALU-pipe operations (committed ncu record, 32 lanes per warp instruction) per
     algorithmic byte of index read."""

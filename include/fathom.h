@@ -342,7 +342,7 @@ int fathom_decode_step_workspace_bytes(const fathom_step_desc* step, size_t* byt
 int fathom_decode_step(const fathom_step_desc* step, void* workspace, size_t ws_bytes, void* stream);
 
 /* ---------------- fixed 136-bit comparator index ----------------------------
- * The fixed-depth scans the pages compare against keep 32 channels read at 4
+ * The fixed-depth scans the Fathom article compares against keep 32 channels read at 4
  * bits plus a scale, about 136 bits per token ([A] "The catch": Double
  * Sparsity keeps 32 channels chosen offline).  Here: the 32 channels of
  * largest var (ties to the lower channel), ascending; per token a power-of-two

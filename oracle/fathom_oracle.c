@@ -14,11 +14,11 @@
  *   [R] Rootconf 2026 proposal, "Decoding at a million tokens when the KV cache
  *       lives in host memory: what actually bounds the step"
  *
- * What each function follows is written above it.  Where the pages leave a
+ * What each function follows is written above it.  Where the sources leave a
  * step open, the reading taken is stated in the comment ("reading: ...").
  *
  * Parity status: every function here is pinned by tests against closed forms,
- * brute force, library routines or the pages' printed figure (see tests/).
+ * brute force, library routines or the article's printed figure (see tests/).
  */
 #include <math.h>
 #include <stdint.h>

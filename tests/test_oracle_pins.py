@@ -1,4 +1,4 @@
-"""Pins of the CPU oracle against what the pages and mathematics fix.
+"""Pins of the CPU oracle against what the Fathom article and mathematics fix.
 
 Each test checks the oracle against something other than itself: the page's
 printed bit-plane figure, numpy's IEEE conversions and variance, brute force
