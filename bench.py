@@ -520,7 +520,8 @@ def host_kv_layers(w, args, comparator, log):
     fit = int((share - fixed) // per_layer)
     kl = max(1, min(args.kv_layers, w.layers, fit))
     if kl < min(args.kv_layers, w.layers):
-        log("host memory: %.0f GB available for %d process(es): storing %d distinct K/V layers" % (avail / 1e9, local, kl))
+        log("host memory: %.0f GB available for %d process(es): storing %d distinct K/V layers"
+            % (avail / 1e9, local, kl))
     return kl
 
 
