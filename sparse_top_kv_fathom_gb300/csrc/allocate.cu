@@ -12,9 +12,11 @@
 // own q_h instead of the summed group query), the alternative reading of GQA.
 //
 // GPU form: one CTA per row, one thread per candidate (channel c, plane j).
-// As on the page, the threshold tau is found by binary search: over the bit
-// patterns of non-negative fp32 gains (which order like integers), the largest
-// tau with at least B gains >= tau, each count taken by one __syncthreads_count.
+// The threshold tau -- the B-th largest gain -- is found (as on the page, by
+// narrowing down a threshold) as a radix select over the bit patterns of the
+// non-negative fp32 gains, which order like integers: four passes of 8 bits,
+// each a 256-bin histogram of the candidates that match the digits found so far,
+// then one warp finding the digit where the count from the top reaches B.
 // Gains above tau are taken; gains equal to tau are handed out in (j, c) order
 // (j ascending, then c ascending) until exactly B are taken.  The kernel also
 // zeroes a span of the caller's workspace (the top-k histogram the scan fills
@@ -42,6 +44,8 @@ __global__ void __launch_bounds__(kCand) allocate_kernel(int group, int heads, c
   __shared__ int s_count[kD];
   __shared__ int s_weq[kCand / 32];
   __shared__ int s_bad;
+  __shared__ uint32_t s_h[256];
+  __shared__ int s_dig[2];  // the digit found, and the matching candidates above it
   const int r = blockIdx.x;
   const int i = threadIdx.x;  // candidate index = j * 128 + c
   const int c = i & (kD - 1), j = i >> 7;
@@ -77,13 +81,46 @@ __global__ void __launch_bounds__(kCand) allocate_kernel(int group, int heads, c
   }
   bool take = false;
   if (B > 0) {
-    uint32_t lo = 0u, hi = 0x7f800000u;  // count(gain >= lo) = 512 >= B
-    while (lo < hi) {                    // uniform: every thread holds the same lo, hi
-      const uint32_t mid = lo + (hi - lo + 1u) / 2u;
-      if (__syncthreads_count(gb >= mid) >= B) lo = mid;
-      else hi = mid - 1u;
+    // radix select of the B-th largest gain, 8 bits a pass from the top
+    uint32_t prefix = 0u, pmask = 0u;
+    int need = B;  // gains still to reach among those matching prefix under pmask
+#pragma unroll 1
+    for (int sh = 24; sh >= 0; sh -= 8) {
+      if (i < 256) s_h[i] = 0u;
+      __syncthreads();
+      if ((gb & pmask) == prefix) atomicAdd(&s_h[(gb >> sh) & 255u], 1u);
+      __syncthreads();
+      if (i < 32) {  // lane l holds bins 255 - 8l .. 248 - 8l (descending)
+        int bins[8], sum = 0;
+#pragma unroll
+        for (int b = 0; b < 8; ++b) {
+          bins[b] = int(s_h[255 - 8 * i - b]);
+          sum += bins[b];
+        }
+        int cum = sum;  // inclusive scan over the lanes
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int y = __shfl_up_sync(0xffffffffu, cum, o);
+          if (i >= o) cum += y;
+        }
+        int before = cum - sum;
+        if (before < need && cum >= need) {
+          int b = 0;
+          for (; b < 7; ++b) {
+            if (before + bins[b] >= need) break;
+            before += bins[b];
+          }
+          s_dig[0] = 255 - 8 * i - b;
+          s_dig[1] = before;
+        }
+      }
+      __syncthreads();
+      need -= s_dig[1];
+      prefix |= uint32_t(s_dig[0]) << sh;
+      pmask |= 255u << sh;
     }
-    const int above = __syncthreads_count(gb > lo);
+    const uint32_t lo = prefix;  // tau: B - need gains lie above it
+    const int above = B - need;
     // rank of this candidate among those equal to tau, in (j, c) order = thread order
     const unsigned eqb = __ballot_sync(0xffffffffu, gb == lo);
     if ((i & 31) == 0) s_weq[i >> 5] = __popc(eqb);
