@@ -58,7 +58,8 @@ extern "C" {
 #define FATHOM_BF16 2
 
 /* Bits that device-side checks OR into an optional int32 status word. */
-#define FATHOM_STATUS_NONFINITE 1     /* non-finite query or variance: that row gets no bits */
+#define FATHOM_STATUS_NONFINITE 1     /* non-finite query, variance or importance qbar^2*var (overflow),
+                                         or a negative variance: that row gets no bits */
 #define FATHOM_STATUS_BUDGET_CLAMPED 2 /* a per-row budget above 4*d was clamped to 4*d */
 
 /* Shape of a packed bit-plane index.
@@ -148,8 +149,9 @@ int fathom_pack_append(const fathom_index_desc* desc, int64_t n_old, const void*
  * Definition: w_c = (qbar_c*qbar_c)*var_c (fp32); the gain of plane j of
  * channel c is w_c multiplied j times by 0.25; the `budget` (c, j) pairs with
  * the largest gains are taken, ties going to the smaller j and then to the
- * smaller c; b_c counts the pairs taken for c.  EINVAL if budget is outside
- * [0, 512] when budgets is NULL. */
+ * smaller c; b_c counts the pairs taken for c.  A zero gain ranks as zero
+ * whatever its sign (var_c = -0 is the variance zero).  EINVAL if budget is
+ * outside [0, 512] when budgets is NULL. */
 int fathom_allocate(int rows, int group, const void* q, int q_dtype, const float* var, const uint16_t* budgets,
                     int budget, uint8_t* bits, float* qbar, int32_t* status, void* stream);
 

@@ -184,7 +184,14 @@ int oracle_code_at(const uint32_t* planes, int64_t n, int64_t S, int64_t row, in
 /*   ascending then channel c ascending.                                      */
 /* ------------------------------------------------------------------------ */
 
-static uint32_t fbits(float f) { uint32_t u; memcpy(&u, &f, 4); return u; }
+/* bit pattern of a gain (finite, >= 0); -0 is the value zero, so it takes +0's
+ * pattern (reading: a zero gain ranks as zero, whatever its sign bit) */
+static uint32_t fbits(float f) {
+  uint32_t u;
+  if (f == 0.0f) return 0u;
+  memcpy(&u, &f, 4);
+  return u;
+}
 
 /* number of (c, j) whose gain is >= the threshold whose fp32 bit pattern is tau */
 static int count_ge(int d, const float* w, uint32_t tau) {
@@ -248,9 +255,10 @@ int oracle_allocate(int rows, int group, const float* q, const float* var, const
     for (int c = 0; c < D_CH; ++c) {
       float s = q[((size_t)r * group + 0) * D_CH + c];
       for (int h = 1; h < group; ++h) s = s + q[((size_t)r * group + h) * D_CH + c];
-      if (!isfinite(s) || !isfinite(var[(size_t)r * D_CH + c])) return 1;
+      const float v = var[(size_t)r * D_CH + c];
+      if (!isfinite(s) || !isfinite(v) || v < 0.0f) return 1; /* a variance is never negative */
       qbar[(size_t)r * D_CH + c] = s;
-      w[c] = (s * s) * var[(size_t)r * D_CH + c];
+      w[c] = (s * s) * v;
     }
     if (oracle_waterfill(D_CH, w, budget[r], bits + (size_t)r * D_CH)) return 1;
   }
@@ -270,8 +278,9 @@ int oracle_allocate_heads(int rows, int group, const float* q, const float* var,
       float w[D_CH];
       const float* qh = q + ((size_t)r * group + h) * D_CH;
       for (int c = 0; c < D_CH; ++c) {
-        if (!isfinite(qh[c]) || !isfinite(var[(size_t)r * D_CH + c])) return 1;
-        w[c] = (qh[c] * qh[c]) * var[(size_t)r * D_CH + c];
+        const float v = var[(size_t)r * D_CH + c];
+        if (!isfinite(qh[c]) || !isfinite(v) || v < 0.0f) return 1;
+        w[c] = (qh[c] * qh[c]) * v;
       }
       if (oracle_waterfill(D_CH, w, budget[r], bits + ((size_t)r * group + h) * D_CH)) return 1;
     }

@@ -58,9 +58,11 @@ __global__ void __launch_bounds__(kCand) allocate_kernel(int group, int heads, c
     float s = load_as_float(q, q0, q_dtype);
     for (int h = 1; h < group; ++h) s = __fadd_rn(s, load_as_float(q, q0 + int64_t(h) * kD, q_dtype));
     const float v = var[int64_t(r / heads) * kD + c];
-    if (!isfinite(s) || !isfinite(v)) s_bad = 1;
     qbar[int64_t(r) * kD + c] = s;
-    w = __fmul_rn(__fmul_rn(s, s), v);
+    // + 0 turns a -0 product (var = -0) into +0: equal gains need equal bit patterns
+    w = __fadd_rn(__fmul_rn(__fmul_rn(s, s), v), 0.0f);
+    // a variance is never negative; an importance that overflows has no order
+    if (!isfinite(s) || !isfinite(v) || v < 0.0f || !isfinite(w)) s_bad = 1;
     s_gain[c] = w;
   }
   __syncthreads();

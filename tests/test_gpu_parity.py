@@ -101,6 +101,79 @@ def test_allocate_bit_exact(case, gpu_lib, budget):
     assert np.array_equal(qbar.cpu().numpy().view(np.uint32), oq.view(np.uint32))
 
 
+_ALLOC_BUDGETS = [0, 1, 2, 3, 64, 127, 128, 129, 255, 256, 257, 384, 511, 512]
+
+
+def _allocation_inputs(rng, kind, rows, group):
+    """Queries and variances whose gains collide (powers of four), vanish, underflow, come close
+    to the fp32 maximum, or carry a -0 variance."""
+    q = rng.standard_normal((rows * group, 128)).astype(np.float32)
+    var = np.exp(rng.normal(0, 2, (rows, 128))).astype(np.float32)
+    if kind == "pow4":  # qbar = group exactly; every gain is a power of four times group^2
+        q[:] = 1.0
+        var = (4.0 ** rng.integers(-8, 8, (rows, 128))).astype(np.float32)
+    elif kind == "allequal":
+        q[:] = 1.0
+        var[:] = 1.0
+    elif kind == "zeros":
+        var[rng.random((rows, 128)) < 0.5] = 0.0
+        q[:, rng.random(128) < 0.25] = 0.0
+    elif kind == "tiny":  # subnormal gains, several of them zero after the 4^-j scaling
+        q[:] = 1.0
+        var = (rng.random((rows, 128)) * np.where(rng.random((rows, 128)) < 0.5, 1e-38, 1e-44)).astype(np.float32)
+    elif kind == "huge":
+        q = (q * 1e3).astype(np.float32)
+        var = (rng.random((rows, 128)) * 1e29).astype(np.float32)  # importances up to ~1e37
+    elif kind == "negzero":
+        var[:, ::3] = -0.0
+        q[:, 1::6] = 0.0
+    return q, var
+
+
+@pytest.mark.parametrize("kind", ["pow4", "allequal", "zeros", "tiny", "huge", "negzero"])
+def test_allocate_threshold_edge_cases(gpu_lib, kind):
+    """The allocation's threshold (the B-th largest gain) and its tie rule on gains that tie,
+    vanish or underflow, one budget per row across the whole range."""
+    F, group = gpu_lib, 4
+    rng = np.random.default_rng(len(kind))
+    rows = len(_ALLOC_BUDGETS)
+    q, var = _allocation_inputs(rng, kind, rows, group)
+    b = np.array(_ALLOC_BUDGETS, np.int32)
+    bt = torch.from_numpy(b.astype(np.int16)).cuda()
+    qd, vd = torch.from_numpy(q).cuda(), torch.from_numpy(var).cuda()
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    bits, qbar = F.allocate(qd, vd, bt, group, status=status)
+    ob, oq = oracle.allocate(q, var, b, group)
+    assert int(status.item()) == 0
+    assert np.array_equal(bits.cpu().numpy(), ob)
+    assert np.array_equal(qbar.cpu().numpy().view(np.uint32), oq.view(np.uint32))
+    hb, _ = F.allocate_heads(qd, vd, bt, group)
+    assert np.array_equal(hb.cpu().numpy(), oracle.allocate_heads(q, var, b, group))
+
+
+def test_allocate_flags_invalid_rows(gpu_lib):
+    """A non-finite query or variance, a negative variance or an importance that overflows fp32
+    gives that row no bits and sets the status bit; the other rows are allocated as usual."""
+    F, group = gpu_lib, 4
+    rng = np.random.default_rng(5)
+    q, var = _allocation_inputs(rng, "normal", 5, group)
+    var[1, 7] = np.nan
+    var[2, 9] = -1e-3
+    q[3 * group + 2, 100] = np.inf
+    q[4 * group:5 * group, 50] = 1e20  # qbar^2 overflows
+    var[4, 50] = 1.0
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    bits, _ = F.allocate(torch.from_numpy(q).cuda(), torch.from_numpy(var).cuda(), 92, group, status=status)
+    bits = bits.cpu().numpy()
+    assert int(status.item()) & 1
+    assert not bits[1:].any()
+    ob, _ = oracle.allocate(q[:group], var[:1], 92, group)
+    assert np.array_equal(bits[:1], ob)
+    for r in (1, 2, 3, 4):
+        with pytest.raises(ValueError):
+            oracle.allocate(q[r * group:(r + 1) * group], var[r:r + 1], 92, group)
+
+
 @pytest.mark.parametrize("budget", [0, 1, 68, 92, 136, 512])
 def test_scan_within_tolerance(case, gpu_lib, budget):
     F, w = gpu_lib, case["w"]

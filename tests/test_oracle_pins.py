@@ -363,6 +363,40 @@ def test_allocate_uses_group_sum_and_variance():
         oracle.allocate(q, var, 513, g)
 
 
+def test_zero_gain_ranks_as_zero_whatever_its_sign():
+    """A variance of -0 is the variance zero: its gains tie with +0 gains (plane, then channel,
+    ascending), they do not outrank positive gains as a -0 bit pattern read as an integer would."""
+    w = np.array([16.0, -0.0, 1.0, 0.0], np.float32)
+    for B in range(17):
+        assert np.array_equal(oracle.waterfill(w, B), oracle.waterfill(np.abs(w), B)), B
+    assert tuple(oracle.waterfill(w, 1)) == (1, 0, 0, 0)
+    assert tuple(oracle.waterfill(w, 7)) == (4, 0, 3, 0)
+    assert tuple(oracle.waterfill(w, 8)) == (4, 0, 4, 0)  # 1/64 is still above every zero gain
+    assert tuple(oracle.waterfill(w, 9)) == (4, 1, 4, 0)  # zero gains: channel 1 (the -0) first ...
+    assert tuple(oracle.waterfill(w, 10)) == (4, 1, 4, 1)  # ... then channel 3, plane 0 before plane 1
+    rng = np.random.default_rng(11)
+    q = rng.standard_normal((2 * 4, D)).astype(np.float32)
+    var = np.exp(rng.normal(0, 1, (2, D))).astype(np.float32)
+    var[:, ::3] = -0.0
+    b_neg, _ = oracle.allocate(q, var, 300, 4)
+    b_pos, _ = oracle.allocate(q, np.abs(var), 300, 4)
+    assert np.array_equal(b_neg, b_pos)
+    assert np.array_equal(oracle.allocate_heads(q, var, 300, 4), oracle.allocate_heads(q, np.abs(var), 300, 4))
+
+
+def test_allocate_rejects_negative_variance():
+    q = np.ones((4, D), np.float32)
+    var = np.ones((1, D), np.float32)
+    var[0, 5] = -1e-3
+    with pytest.raises(ValueError):
+        oracle.allocate(q, var, 92, 4)
+    with pytest.raises(ValueError):
+        oracle.allocate_heads(q, var, 92, 4)
+    q[:, 5] = 0.0  # a zero query does not make the variance valid
+    with pytest.raises(ValueError):
+        oracle.allocate(q, var, 92, 4)
+
+
 # ------------------------------------------------------------------ top-k ---
 def brute_topk(s, k):
     order = sorted(range(len(s)), key=lambda i: (-float(s[i]), i))
