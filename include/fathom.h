@@ -355,7 +355,8 @@ int fathom_decode_step(const fathom_step_desc* step, void* workspace, size_t ws_
  *          nibble and channel 2i+1 in its high nibble (two's complement).
  *   exps   device uint8 [rows][n] out: e + 127.
  *   workspace  device scratch of fathom_fixed136_pack_workspace_bytes.
- * Synchronises `stream` (EDATA as for fathom_pack). */
+ * Synchronises `stream`.  EDATA as for fathom_pack, and also when var holds a
+ * non-finite or negative value (a variance of -0 counts as 0). */
 int fathom_fixed136_pack_workspace_bytes(int rows, int64_t n, size_t* bytes);
 int fathom_fixed136_pack(int rows, int64_t n, const void* K, int k_dtype, const float* var, int32_t* chans,
                          uint8_t* codes, uint8_t* exps, void* workspace, size_t ws_bytes, void* stream);

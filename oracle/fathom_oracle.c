@@ -520,7 +520,10 @@ int oracle_fixed136_pack(int64_t n, int rows, const float* K, const float* var, 
   for (int r = 0; r < rows; ++r) {
     const float* v = var + (size_t)r * D_CH;
     int used[D_CH];
-    for (int c = 0; c < D_CH; ++c) used[c] = 0;
+    for (int c = 0; c < D_CH; ++c) {
+      if (!isfinite(v[c]) || v[c] < 0.0f) return 1; /* a variance is finite and never negative */
+      used[c] = 0;
+    }
     for (int i = 0; i < 32; ++i) {
       int best = -1;
       for (int c = 0; c < D_CH; ++c)

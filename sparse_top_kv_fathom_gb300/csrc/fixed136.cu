@@ -13,12 +13,19 @@ namespace {
 constexpr int kSel = 32;
 constexpr int kThreads = 256;
 constexpr int kErrRange = 1;
+constexpr int kErrVar = 2;
 
-__global__ void __launch_bounds__(kD) chans_kernel(const float* __restrict__ var, int32_t* __restrict__ chans) {
+__global__ void __launch_bounds__(kD) chans_kernel(const float* __restrict__ var, int32_t* __restrict__ chans,
+                                                   int* __restrict__ err) {
   __shared__ float s_v[kD];
   __shared__ int s_cnt[kD / 32];
   const int r = blockIdx.x, c = threadIdx.x, lane = c & 31, warp = c >> 5;
-  s_v[c] = var[int64_t(r) * kD + c];
+  // ranking key: the variance (-0 as +0); an invalid one (non-finite, negative) ranks below every
+  // valid one and is reported.  A total order selects exactly kSel channels per row.
+  const float x = var[int64_t(r) * kD + c];
+  const bool ok = isfinite(x) && x >= 0.0f;
+  if (!ok) atomicOr(err, kErrVar);
+  s_v[c] = ok ? __fadd_rn(x, 0.0f) : -1.0f;
   __syncthreads();
   const float v = s_v[c];
   int rank = 0;
@@ -152,7 +159,7 @@ int fathom_fixed136_pack(int rows, int64_t n, const void* K, int k_dtype, const 
   cudaStream_t st = as_stream(stream);
   int* err = static_cast<int*>(const_cast<void*>(dW));
   FATHOM_TRY_CUDA(cudaMemsetAsync(err, 0, sizeof(int), st));
-  chans_kernel<<<rows, kD, 0, st>>>((const float*)dV, (int32_t*)dC);
+  chans_kernel<<<rows, kD, 0, st>>>((const float*)dV, (int32_t*)dC, err);
   FATHOM_TRY_CUDA(cudaGetLastError());
   pack136_kernel<<<dim3(unsigned((n + kThreads - 1) / kThreads), unsigned(rows)), kThreads, 0, st>>>(
       n, dK, k_dtype, (const int32_t*)dC, (uint8_t*)dX, (uint8_t*)dE, err);
@@ -160,6 +167,7 @@ int fathom_fixed136_pack(int rows, int64_t n, const void* K, int k_dtype, const 
   int herr = 0;
   FATHOM_TRY_CUDA(cudaMemcpyAsync(&herr, err, sizeof(int), cudaMemcpyDeviceToHost, st));
   FATHOM_TRY_CUDA(cudaStreamSynchronize(st));
+  if (herr & kErrVar) return set_error(FATHOM_EDATA, "var holds a non-finite or negative value");
   if (herr & kErrRange) return set_error(FATHOM_EDATA, "K holds a non-finite value or one outside the fp16 range");
   return FATHOM_OK;
 }

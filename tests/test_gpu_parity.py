@@ -251,6 +251,28 @@ def test_interleaved_kv_in_host_alloc_memory(case, gpu_lib):
         F.host_release(t)
 
 
+def test_fixed136_channel_choice_with_zero_and_invalid_variances(gpu_lib):
+    """Zero variances of either sign tie (to the lower channel) as in the oracle; NaN, infinite or
+    negative variances, however many, are reported and still select exactly 32 channels."""
+    F = gpu_lib
+    rng = np.random.default_rng(21)
+    K = rng.standard_normal((2, 300, 128)).astype(np.float32)
+    var = np.exp(rng.normal(0, 1, (2, 128))).astype(np.float32)
+    var[0, :100] = np.where(np.arange(100) % 2 == 0, -0.0, 0.0)
+    var[1, 60:] = 0.0
+    fx = F.fixed136_pack(torch.from_numpy(K).cuda(), torch.from_numpy(var).cuda())
+    chans, codes, exps = oracle.fixed136_pack(K, var)
+    assert np.array_equal(fx.chans.cpu().numpy(), chans)
+    assert np.array_equal(fx.codes.cpu().numpy(), codes)
+    assert np.array_equal(fx.exps.cpu().numpy(), exps)
+    bad = var.copy()
+    bad[0, :40] = np.nan  # more invalid channels than the 32 chosen
+    bad[1, 3] = -2.0
+    bad[1, 90:] = np.inf
+    with pytest.raises(F.FathomError, match="var holds"):
+        F.fixed136_pack(torch.from_numpy(K).cuda(), torch.from_numpy(bad).cuda())
+
+
 def test_fixed136_parity(case, gpu_lib):
     F, w = gpu_lib, case["w"]
     fx = F.fixed136_pack(case["Kd"], case["index"].var)

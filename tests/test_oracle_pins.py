@@ -496,6 +496,22 @@ def test_fixed136_pack_and_scan():
         np.testing.assert_allclose(s[r], want, rtol=1e-13, atol=1e-13)
 
 
+def test_fixed136_channel_choice_with_zero_and_invalid_variances():
+    """Variances of -0 are zeros (ties to the lower channel); a non-finite or negative one is
+    invalid."""
+    K = rand_keys(1, 64, seed=13)
+    var = np.exp(np.random.default_rng(13).normal(0, 1, (1, D))).astype(np.float32)
+    var[0, :100] = np.where(np.arange(100) % 2 == 0, -0.0, 0.0)  # 28 positive variances left
+    chans, _, _ = oracle.fixed136_pack(K, var)
+    assert list(chans[0]) == [0, 1, 2, 3] + list(range(100, 128))
+    assert np.array_equal(chans, oracle.fixed136_pack(K, np.abs(var))[0])
+    for bad in (np.nan, np.inf, -1e-6):
+        v = var.copy()
+        v[0, 120] = bad
+        with pytest.raises(ValueError):
+            oracle.fixed136_pack(K, v)
+
+
 # ------------------------------------------------------------ decode step ---
 def test_decode_step_composes_the_steps():
     rng = np.random.default_rng(13)
