@@ -217,7 +217,10 @@ int fathom_topk_workspace_bytes(int rows, int64_t n, int64_t k, size_t* bytes);
  *           the lower index, -0.0 equal to +0.0, written in ascending index
  *           order; if k > n the first n entries are 0..n-1 and the rest -1.
  *   vals    device float [rows][k] out (scores at idx, -inf for padding), or NULL.
- * EINVAL for k < 1, n < 1 or n >= 2^31. */
+ * EINVAL for k < 1, n < 1 or n >= 2^31.  A NaN score has no value to rank by
+ * (the scan makes none from finite inputs); it is ordered by its bit pattern,
+ * above +inf with the sign bit clear and below -inf with it set, so the output
+ * stays well formed. */
 int fathom_topk(int rows, int64_t n, int64_t k, const float* scores, int32_t* idx, float* vals, void* workspace,
                 size_t ws_bytes, void* stream);
 

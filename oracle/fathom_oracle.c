@@ -391,7 +391,11 @@ int oracle_topk_f32(int64_t n, int rows, int64_t k, const float* scores, int32_t
   scored* buf = (scored*)malloc(sizeof(scored) * (size_t)n);
   if (!buf) return 1;
   for (int r = 0; r < rows; ++r) {
-    for (int64_t t = 0; t < n; ++t) { buf[t].s = (double)scores[(size_t)r * n + t]; buf[t].i = t; }
+    for (int64_t t = 0; t < n; ++t) {
+      buf[t].s = (double)scores[(size_t)r * n + t];
+      buf[t].i = t;
+      if (isnan(buf[t].s)) { free(buf); return 1; } /* a NaN has no place in the order */
+    }
     topk_row(n, k, buf, idx + (size_t)r * k);
   }
   free(buf);
@@ -403,7 +407,11 @@ int oracle_topk_f64(int64_t n, int rows, int64_t k, const double* scores, int32_
   scored* buf = (scored*)malloc(sizeof(scored) * (size_t)n);
   if (!buf) return 1;
   for (int r = 0; r < rows; ++r) {
-    for (int64_t t = 0; t < n; ++t) { buf[t].s = scores[(size_t)r * n + t]; buf[t].i = t; }
+    for (int64_t t = 0; t < n; ++t) {
+      buf[t].s = scores[(size_t)r * n + t];
+      buf[t].i = t;
+      if (isnan(buf[t].s)) { free(buf); return 1; }
+    }
     topk_row(n, k, buf, idx + (size_t)r * k);
   }
   free(buf);

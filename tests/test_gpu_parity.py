@@ -327,6 +327,26 @@ def test_topk_bit_exact(gpu_lib, n):
                 assert np.array_equal(v[r][sel].view(np.uint32), s[r][want[r][sel]].view(np.uint32))
 
 
+def test_topk_orders_nan_by_bit_pattern(gpu_lib):
+    """NaN scores are outside the oracle's domain; the GPU ranks a NaN with its sign bit clear
+    above +inf and one with it set below -inf, and the other scores as the oracle does."""
+    F = gpu_lib
+    rng = np.random.default_rng(9)
+    n, k = 5000, 64
+    s = rng.standard_normal((2, n)).astype(np.float32)
+    pos = np.sort(rng.choice(n, 20, replace=False))
+    neg = rng.choice(n, 4000, replace=False)
+    s[0, pos] = np.array(0x7FC00000, np.uint32).view(np.float32)
+    s[1, neg] = np.array(0xFFC00000, np.uint32).view(np.float32)
+    s[0, :3] = np.inf
+    idx = F.topk(torch.from_numpy(s).cuda(), k).cpu().numpy()
+    rest = np.setdiff1d(np.arange(n), pos)  # row 0: every NaN, then the k - 20 largest others
+    want0 = np.sort(np.concatenate([pos, rest[oracle.topk_f32(s[0:1, rest], k - 20)[0]]]))
+    assert np.array_equal(idx[0], want0)
+    fin = np.setdiff1d(np.arange(n), neg)  # row 1: the NaNs rank last
+    assert np.array_equal(idx[1], np.sort(fin[oracle.topk_f32(s[1:2, fin], k)[0]]))
+
+
 # ------------------------------------------------------------ attention ---
 @pytest.mark.parametrize("dtype", [torch.float32, torch.float16, torch.bfloat16])
 @pytest.mark.parametrize("group", [1, 3, 4, 8])

@@ -435,6 +435,14 @@ def dense_attention(q, K, V):
     return p @ V.astype(np.float64)
 
 
+def test_topk_rejects_nan():
+    s = np.array([[1.0, np.nan, 2.0]], np.float32)
+    with pytest.raises(ValueError):
+        oracle.topk_f32(s, 2)
+    with pytest.raises(ValueError):
+        oracle.topk_f64(s.astype(np.float64), 2)
+
+
 def test_sparse_attention_with_all_keys_is_dense_attention():
     rng = np.random.default_rng(8)
     rows, g, n = 2, 4, 200
