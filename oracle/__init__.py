@@ -8,12 +8,16 @@ this module only marshals numpy arrays into it.
 
 Function map (each C function cites the page passage it follows):
   pack            per-block min/max 4-bit codes -> MSB-first bit planes + var
+  code_at         one key's 4-bit code read back from the planes
   allocate        reverse water-filling (threshold binary search)
+  allocate_heads  the same per query head (the alternative GQA reading)
   allocate_sparq  the SparQ-style comparator: full depth on the r largest |qbar|
-  waterfill       the same for one row of weights, any channel count
+  waterfill       reverse water-filling of one row of weights, any channel count
   scan            fp64 score of every key from the chosen plane prefixes
+  scan_heads      the same per query head, or the max over a group's heads
   topk_f32/_f64   k largest, ties to the lower index, ascending output
   sparse_attn     fp64 softmax attention over the selected rows
+  sparse_attn_q4  the same with the keys dequantised from the 4-bit index
   fixed136_pack / fixed136_scan   the 136-bit fixed-channel comparator
   decode_step     allocate -> scan -> top-k -> attention for many rows
 """
