@@ -293,6 +293,45 @@ def test_fixed136_parity(case, gpu_lib):
                                                             w.group))
 
 
+@pytest.mark.parametrize("n", [1, 2, 31, 33, 127, 129, 1023, 1025])
+def test_short_and_ragged_rows(gpu_lib, n):
+    """Rows shorter than a plane word, a 128-token block or a superblock, and one key past them:
+    packing, allocation, scan, top-k (k up to beyond n) and the step against the oracle."""
+    F = gpu_lib
+    rng = np.random.default_rng(1000 + n)
+    rows, group = 2, 2
+    K = rng.standard_normal((rows, n, 128)).astype(np.float32)
+    V = rng.standard_normal((rows, n, 128)).astype(np.float32)
+    q = rng.standard_normal((rows * group, 128)).astype(np.float32)
+    Kd, Vd, qd = (torch.from_numpy(x).cuda() for x in (K, V, q))
+    for S in (128, 1024):
+        ix = F.pack(Kd, S)
+        planes, meta, var = oracle.pack(K, S)
+        assert np.array_equal(ix.planes.cpu().numpy().view(np.uint32), planes)
+        assert np.array_equal(ix.meta.cpu().numpy().view(np.uint16), meta)
+        assert np.array_equal(ix.var.cpu().numpy().view(np.uint32), var.view(np.uint32))
+        for B in (1, 92, 512):
+            bits, qbar = F.allocate(qd, ix.var, B, group)
+            ob, oq = oracle.allocate(q, var, B, group)
+            assert np.array_equal(bits.cpu().numpy(), ob)
+            s = F.scan(ix, bits, qbar)
+            ref, l1 = oracle.scan(planes, meta, ob, oq, n, S)
+            check_scores(s.cpu().numpy(), ref, l1)
+            sc = s.cpu().numpy()
+            for k in sorted({1, max(1, n // 2), n, n + 7}):
+                assert np.array_equal(F.topk(s, k).cpu().numpy(), oracle.topk_f32(sc, k)), (S, B, k)
+        k = min(n, 5)
+        idx, out, outb = F.decode_step(ix, qd, Kd, Vd, k, group, 92)
+        bits, qbar = F.allocate(qd, ix.var, 92, group)
+        gi = oracle.topk_f32(F.scan(ix, bits, qbar).cpu().numpy(), k)
+        assert np.array_equal(idx.cpu().numpy(), gi)
+        check_attn(out.cpu().numpy(), outb, oracle.sparse_attn(q, K, V, gi, group))
+        idx, out, outb = F.decode_step(ix, qd, Kd, Vd, n + 3, group, 92)  # every key, then padding
+        want = np.array([list(range(n)) + [-1] * 3] * rows, np.int32)
+        assert np.array_equal(idx.cpu().numpy(), want)
+        check_attn(out.cpu().numpy(), outb, oracle.sparse_attn(q, K, V, want, group))
+
+
 # ------------------------------------------------------------------ top-k ---
 def _score_sets(rng, rows, n):
     yield "normal", rng.standard_normal((rows, n)).astype(np.float32)
