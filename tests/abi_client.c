@@ -1,0 +1,36 @@
+/* A plain C11 client of the library: includes the public headers, links
+ * libfathom.so and calls the host-only entry points (no GPU needed).  Prints
+ * one line: abi version, plane and meta bytes of an index, the top-k
+ * workspace bytes, then the status and message of an invalid index
+ * descriptor.  Used by the ABI tests to show the boundary needs nothing but
+ * C. */
+#include <stdio.h>
+
+#include "fathom.h"
+#include "fathom_probe.h"
+
+int main(void) {
+  fathom_index_desc d = {0};
+  size_t planes = 0, meta = 0, ws = 0;
+  int rc;
+  d.n = (int64_t)1 << 20;
+  d.rows = 8;
+  d.d = 128;
+  d.block = 128;
+  d.superblock = 4096;
+  d.capacity = 0;
+  rc = fathom_index_bytes(&d, &planes, &meta);
+  if (rc != FATHOM_OK) {
+    printf("index_bytes failed %d: %s\n", rc, fathom_last_error());
+    return 1;
+  }
+  rc = fathom_topk_workspace_bytes(8, d.n, 2048, &ws);
+  if (rc != FATHOM_OK) {
+    printf("topk_workspace_bytes failed %d: %s\n", rc, fathom_last_error());
+    return 1;
+  }
+  d.d = 64; /* only 128 channels per row are supported */
+  rc = fathom_index_bytes(&d, &planes, &meta);
+  printf("%d %zu %zu %zu %d %s\n", fathom_abi_version(), planes, meta, ws, rc, fathom_last_error());
+  return 0;
+}

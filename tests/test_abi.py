@@ -126,3 +126,32 @@ def test_index_capacity_sets_the_layout_strides():
     bad = N.IndexDesc(n, 2, 128, 128, S, n - 1)
     assert L.fathom_index_bytes(ctypes.byref(bad), ctypes.byref(pb), ctypes.byref(mb)) == 1
     assert b"capacity" in L.fathom_last_error()
+
+
+def test_plain_c_client_compiles_links_and_runs(F):
+    """The headers are C11 (no C++), and a C program linked against the library alone gets the
+    same answers as the Python binding: the boundary needs nothing but C."""
+    import shutil
+    import subprocess
+    from sparse_top_kv_fathom_gb300 import _native
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("no gcc")
+    out_dir = os.path.join(ROOT, "tests", "_build")
+    os.makedirs(out_dir, exist_ok=True)
+    exe = os.path.join(out_dir, "abi_client")
+    lib_dir = os.path.dirname(_native.LIB_PATH)
+    r = subprocess.run([gcc, "-std=c11", "-Wall", "-Wextra", "-Werror", "-pedantic", "-I", INCLUDE,
+                        os.path.join(ROOT, "tests", "abi_client.c"), "-L", lib_dir, "-lfathom",
+                        "-Wl,-rpath," + lib_dir, "-o", exe], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    r = subprocess.run([exe], capture_output=True, text=True, timeout=60)
+    assert r.returncode == 0, r.stdout + r.stderr
+    version, planes, meta, ws, rc, msg = r.stdout.split(" ", 5)
+    lib = ctypes.CDLL(_native.LIB_PATH)
+    assert int(version) == lib.fathom_abi_version()
+    assert (int(planes), int(meta)) == F.index_bytes(1 << 20, 8, 4096)
+    b = ctypes.c_size_t()
+    assert lib.fathom_topk_workspace_bytes(8, ctypes.c_int64(1 << 20), ctypes.c_int64(2048), ctypes.byref(b)) == 0
+    assert int(ws) == b.value
+    assert int(rc) == 1 and msg.strip()  # FATHOM_EINVAL with a message
