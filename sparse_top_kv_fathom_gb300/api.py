@@ -28,8 +28,21 @@ def _dt(t):
         raise TypeError("unsupported dtype %s" % t.dtype)
 
 
-def _ptr(t):
-    return None if t is None else ctypes.c_void_p(t.data_ptr())
+def _addr(t, strided=False):
+    """Address of a tensor's first element for the C ABI (None for None).  Every array the ABI
+    takes is dense and row-major, except K and V, whose token-row stride travels separately
+    (strided=True; kv_stride checks those views)."""
+    if t is None:
+        return None
+    if not strided and not t.is_contiguous():
+        raise ValueError("the C ABI takes dense row-major arrays; got a view with strides %s "
+                         "(call .contiguous() first)" % (tuple(t.stride()),))
+    return t.data_ptr()
+
+
+def _ptr(t, strided=False):
+    a = _addr(t, strided)
+    return None if a is None else ctypes.c_void_p(a)
 
 
 def _stream(stream=None):
@@ -225,7 +238,7 @@ def sparse_attn(q, K, V, idx, group, stream=None, per_head=False):
     N.check(L.fathom_sparse_attn_workspace_bytes(rows, group, k, ctypes.byref(wsb)))
     ws = _ws(wsb.value, dev)
     fn = L.fathom_sparse_attn_heads if per_head else L.fathom_sparse_attn
-    N.check(fn(rows, group, n, k, _ptr(q), _dt(q), _ptr(K), _ptr(V), _dt(K), kv_stride(K, V), _ptr(idx), _ptr(out),
+    N.check(fn(rows, group, n, k, _ptr(q), _dt(q), _ptr(K, True), _ptr(V, True), _dt(K), kv_stride(K, V), _ptr(idx), _ptr(out),
                _ptr(outb), _ptr(ws), wsb.value, _stream(stream)))
     return out, outb
 
@@ -244,7 +257,7 @@ def sparse_attn_q4(index, q, V, idx, group, stream=None):
     outb = torch.empty((rows * group, D), dtype=torch.bfloat16, device=dev)
     dsc = index.desc
     N.check(L.fathom_sparse_attn_q4(ctypes.byref(dsc), group, k, _ptr(q), _dt(q), _ptr(index.planes),
-                                    _ptr(index.meta), _ptr(V), _dt(V), V.stride(1), _ptr(idx), _ptr(out), _ptr(outb),
+                                    _ptr(index.meta), _ptr(V, True), _dt(V), V.stride(1), _ptr(idx), _ptr(out), _ptr(outb),
                                     _stream(stream)))
     return out, outb
 
@@ -307,13 +320,11 @@ class DecodeStep:
 
     def _bind(self):
         d = self.desc
-        d.planes, d.meta, d.var = self.index.planes.data_ptr(), self.index.meta.data_ptr(), self.index.var.data_ptr()
-        d.budgets = self.budgets.data_ptr() if self.budgets is not None else None
-        d.q, d.V = self.q.data_ptr(), self.V.data_ptr()
-        d.K = self.K.data_ptr() if self.K is not None else None
-        d.idx, d.out, d.out_bf16 = self.idx.data_ptr(), self.out.data_ptr(), self.out_bf16.data_ptr()
-        d.status = self.status.data_ptr() if self.status is not None else None
-        d.hint = self.hint.data_ptr() if self.hint is not None else None
+        d.planes, d.meta, d.var = _addr(self.index.planes), _addr(self.index.meta), _addr(self.index.var)
+        d.budgets = _addr(self.budgets)
+        d.q, d.V, d.K = _addr(self.q), _addr(self.V, True), _addr(self.K, True)
+        d.idx, d.out, d.out_bf16 = _addr(self.idx), _addr(self.out), _addr(self.out_bf16)
+        d.status, d.hint = _addr(self.status), _addr(self.hint)
 
     def __call__(self, stream=None):
         N.check(self.L.fathom_decode_step(ctypes.byref(self.desc), _ptr(self.ws), self.ws_bytes, _stream(stream)))
@@ -371,9 +382,9 @@ class Fixed136Step:
         d = self.desc = N.Fixed136StepDesc()
         d.n, d.rows, d.group, d.k = index.n, index.rows, group, k
         d.q_dtype, d.kv_dtype, d.kv_stride = _dt(q), _dt(K), kv_stride(K, V)
-        d.chans, d.codes, d.exps = index.chans.data_ptr(), index.codes.data_ptr(), index.exps.data_ptr()
-        d.q, d.K, d.V = q.data_ptr(), K.data_ptr(), V.data_ptr()
-        d.idx, d.out, d.out_bf16 = self.idx.data_ptr(), self.out.data_ptr(), self.out_bf16.data_ptr()
+        d.chans, d.codes, d.exps = _addr(index.chans), _addr(index.codes), _addr(index.exps)
+        d.q, d.K, d.V = _addr(q), _addr(K, True), _addr(V, True)
+        d.idx, d.out, d.out_bf16 = _addr(self.idx), _addr(self.out), _addr(self.out_bf16)
         wsb = ctypes.c_size_t()
         N.check(self.L.fathom_fixed136_step_workspace_bytes(ctypes.byref(d), ctypes.byref(wsb)))
         if workspace is not None:

@@ -155,3 +155,23 @@ def test_plain_c_client_compiles_links_and_runs(F):
     assert lib.fathom_topk_workspace_bytes(8, ctypes.c_int64(1 << 20), ctypes.c_int64(2048), ctypes.byref(b)) == 0
     assert int(ws) == b.value
     assert int(rc) == 1 and msg.strip()  # FATHOM_EINVAL with a message
+
+
+def test_binding_refuses_strided_views_except_for_k_and_v():
+    """A pointer alone cannot describe a strided view: the binding refuses one for every dense
+    argument, and takes K/V views whose token-row stride it passes on."""
+    import torch
+    from sparse_top_kv_fathom_gb300 import api
+    x = torch.zeros(8, 128)
+    assert api._addr(x) == x.data_ptr() and api._addr(None) is None
+    assert api._addr(x[2:4]) == x[2:4].data_ptr()  # leading-dim slices stay dense
+    with pytest.raises(ValueError, match="dense"):
+        api._addr(x[::2])
+    with pytest.raises(ValueError, match="dense"):
+        api._addr(torch.zeros(128, 8).t())
+    KV = torch.zeros(2, 16, 2, 128)
+    K, V = KV[:, :, 0], KV[:, :, 1]
+    assert api._addr(K, strided=True) == K.data_ptr()
+    assert api.kv_stride(K, V) == 256
+    with pytest.raises(ValueError):
+        api._ptr(K)
