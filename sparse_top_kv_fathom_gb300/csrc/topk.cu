@@ -2,8 +2,9 @@
 // written in ascending index order (Fathom article, "The first fix: stop
 // attending to everything": score every key and take the top k).
 //
-// Scores are mapped to order-preserving 32-bit keys (-0.0 as +0.0).  The
-// selection is an exact radix select:
+// Scores are mapped to order-preserving 32-bit keys (-0.0 as +0.0; a NaN lands
+// above +inf with its sign bit clear and below -inf with it set, so every input
+// has a place in the order).  The selection is an exact radix select:
 //   1. a 4096-bin histogram of each row's top 12 key bits (fused into the scan
 //      inside the decode step, or a separate pass here);
 //   2. per row, the bin b1 holding the k-th largest key;
@@ -16,9 +17,10 @@
 //      chosen indices in order: through a bitmap of the row in shared memory
 //      (n <= 2^20: set bits, popcount prefix, emit), else a bitonic sort.
 // If the candidate list overflows, or k is larger than the sort buffer when
-// the row is too long for the bitmap, step 4 instead runs the same definition directly over the row's scores (3 digit
-// passes, an ordered count of the keys equal to T, then an ordered compaction);
-// both routes produce the identical result.
+// the row is too long for the bitmap, step 4 instead runs the same definition
+// directly over the row's scores (3 digit passes, an ordered count of the keys
+// equal to T, then an ordered compaction); both routes produce the identical
+// result.
 #include "common.cuh"
 
 namespace fathom {
