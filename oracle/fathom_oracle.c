@@ -361,7 +361,8 @@ void oracle_scan(int64_t n, int rows, int64_t S, const uint32_t* planes, const u
 /* Top-k: the k largest scores of a row, ties to the lower index, returned   */
 /* in ascending index order.  [A] "The first fix: stop attending to          */
 /* everything": score every key, take the top k.  reading: -0.0 equals +0.0;  */
-/* k >= n selects every key and pads idx with -1.                            */
+/* k >= n selects every key and pads idx with -1; a NaN score has no place in */
+/* the order and is rejected.                                                 */
 /* ------------------------------------------------------------------------ */
 typedef struct { double s; int64_t i; } scored;
 
