@@ -181,7 +181,9 @@ int oracle_code_at(const uint32_t* planes, int64_t n, int64_t S, int64_t row, in
 /* reading: w_c = (qbar_c * qbar_c) * var_c in fp32, qbar = left-fold sum of    */
 /*   the group's query heads in fp32; gain of plane j of channel c is          */
 /*   w_c * 4^-j; exactly B (c, j) pairs are taken, ties broken by plane j     */
-/*   ascending then channel c ascending.                                      */
+/*   ascending then channel c ascending.  A variance is finite and never      */
+/*   negative (anything else is invalid input); a zero gain ranks as zero     */
+/*   whatever its sign bit.                                                   */
 /* ------------------------------------------------------------------------ */
 
 /* bit pattern of a gain (finite, >= 0); -0 is the value zero, so it takes +0's
