@@ -8,9 +8,9 @@
 // in HBM (every KV head's cluster starts at once) and of 16 when they are read over
 // the host link (more rows in flight for the address translations).  Each CTA
 // takes a slice of the winners; each warp gathers whole K and V rows (a lane
-// holds 4 channels: 8 contiguous bytes of a 16-bit row) for a batch of 8
-// winners at once, the indices of the next batch loaded while this one is
-// reduced.  The group's dot products are reduced with shuffles and an online
+// holds 4 channels: 8 contiguous bytes of a 16-bit row, 16 of an fp32 one) for
+// a batch of 8 winners at once, the indices of the next batch loaded while this
+// one is reduced.  An index outside [0, n) (the top-k's -1 padding) is skipped.  The group's dot products are reduced with shuffles and an online
 // softmax (one running max per batch, sum and weighted V) is kept per head.
 // The CTA merges its warps in shared memory and stores its partial into CTA 0's
 // shared memory (distributed shared memory); after one cluster barrier CTA 0
