@@ -175,3 +175,15 @@ def test_binding_refuses_strided_views_except_for_k_and_v():
     assert api.kv_stride(K, V) == 256
     with pytest.raises(ValueError):
         api._ptr(K)
+
+
+def test_step_workspace_covers_the_scores_and_grows_with_k(F):
+    """Host-only size queries: the decode step's workspace holds at least the fp32 scores of
+    every row it scores (rows, or rows x group under per-head scoring) and never shrinks as k
+    grows."""
+    for n, rows, S, group in [(1 << 20, 8, 4096, 4), (4096, 1, 1024, 1), (131072, 16, 4096, 4)]:
+        ix = F.BitPlaneIndex(None, None, None, n, rows, S)
+        for gqa, srows in (("sum", rows), ("per_head", rows * group)):
+            sizes = [F.DecodeStep.workspace_bytes(ix, k, group, gqa) for k in (1, 64, 2048, 9000)]
+            assert sizes[0] >= srows * n * 4, (n, rows, gqa)
+            assert sizes == sorted(sizes), (n, rows, gqa, sizes)
