@@ -48,6 +48,11 @@ def test_index_sizes_match_the_pages(F):
     for n in [128, 4096, 1 << 20]:
         pb, mb = F.index_bytes(n, 1, 4096 if n >= 4096 else 128)
         assert (pb + mb) / n == g["fathom_index_bytes_per_token_per_kv_head"]
+    # SparQ on the same store: r channels at all 4 planes plus their blocks' (lo, delta)
+    pb, mb = F.index_bytes(1 << 20, 1, 4096)
+    bits_per_channel_key = (pb + mb) * 8 / ((1 << 20) * 128)
+    for r, bits in g["sparq_read_bits_per_key"].items():
+        assert int(r) * bits_per_channel_key == bits
     # ... 4x the 17-byte (136-bit) fixed index
     assert g["fathom_index_bytes_per_token_per_kv_head"] == g["fathom_vs_double_sparsity_label_cache"] * 136 // 8
     q = g["qwen3_8b"]
