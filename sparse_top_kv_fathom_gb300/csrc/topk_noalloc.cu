@@ -30,7 +30,6 @@ namespace {
 
 static __device__ __align__(256) unsigned char g_topk_scratch[FATHOM_TOPK_NOALLOC_SCRATCH_BYTES];
 
-constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 void* g_scratch_ptr[kMaxDevices] = {};
 
